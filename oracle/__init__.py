@@ -1,0 +1,167 @@
+"""fp64 CPU oracle for the gated delta rule -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares nothing with the CUDA path:
+the arithmetic lives in ``gdn_oracle.c`` (plain C, double precision, one
+token at a time), and this module only converts arrays to float64 and calls
+it through ctypes.
+
+Rule (qwen3_5_text page, Notes -> "The DeltaNet mixer"; qwen3_next page,
+Notes -> "The DeltaNet mixer fuses its projections per key head"), per value
+head h with key head h // (HV // HK):
+
+    S <- exp(g_t) S ;  u = beta_t (v_t - S^T k_t) ;  S <- S + k_t u^T ;  o_t = S^T q_t
+
+with k_t = l2norm(k_t), q_t = l2norm(q_t) * Dk**-0.5.  State layout
+[.., key_dim, value_dim] (linear_attn value table, State).
+
+Pins: every function here is checked in ``tests/test_oracle_pins.py``
+against closed forms (T=1 output, beta=0, g -> -inf), the Widrow-Hoff
+projection property with orthonormal keys, an independent one-chunk WY/UT
+solve, continuation, linearity and the GQA interleave of the pages.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from .build import build_oracle
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build_oracle())
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.gdn_oracle_forward.restype = ctypes.c_int
+        lib.gdn_oracle_forward.argtypes = [
+            dp, dp, dp, dp, dp, dp, dp, dp, dp,
+            ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+            ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int]
+        lib.gdn_oracle_chain.restype = ctypes.c_int
+        lib.gdn_oracle_chain.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            dp, ctypes.c_ssize_t, dp, ctypes.c_ssize_t, dp, ctypes.c_ssize_t,
+            dp, dp, ctypes.c_ssize_t, dp, dp, ctypes.c_ssize_t, dp, dp, ctypes.c_ssize_t,
+            ctypes.c_double, ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    """Exact upcast to a C-contiguous float64 numpy array (bf16/fp32 -> fp64 is exact)."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def forward(queries, keys, values, decays, beta, initial_state=None, cu_seqlens=None,
+            scale=None, use_qk_l2norm=True, want_states=False, chains=None, n_threads=None):
+    """Run the recurrence in fp64.
+
+    Batched form: queries/keys [B, T, HK, Dk], values [B, T, HV, Dv],
+    decays/beta [B, T, HV], initial_state [B, HV, Dk, Dv] or None.
+    Packed (varlen) form: the same tensors with B == 1 and ``cu_seqlens``
+    ([N+1] offsets); initial/final states are then [N, HV, Dk, Dv].
+
+    Returns (out [.., HV, Dv], final_state [N or B, HV, Dk, Dv], states or None),
+    all float64 numpy arrays.  ``chains`` (ids seq*HV + h) limits the work to
+    those chains; other entries of the outputs are left as NaN.
+    """
+    q, k, v = _f64(queries), _f64(keys), _f64(values)
+    g, b = _f64(decays), _f64(beta)
+    s0 = _f64(initial_state)
+    B, T, HK, Dk = q.shape
+    HV, Dv = v.shape[2], v.shape[3]
+    if cu_seqlens is None:
+        cu = np.arange(B + 1, dtype=np.int64) * T
+    else:
+        if B != 1:
+            raise ValueError("packed form needs batch 1")
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64))
+    N = len(cu) - 1
+    if scale is None:
+        scale = Dk ** -0.5
+    out = np.full((B, T, HV, Dv), np.nan)
+    final = np.full((N, HV, Dk, Dv), np.nan)
+    states = np.full((B, T, HV, Dk, Dv), np.nan) if want_states else None
+    ch = None
+    n_ch = 0
+    if chains is not None:
+        ch = np.ascontiguousarray(np.asarray(chains, dtype=np.int32))
+        n_ch = len(ch)
+    rc = _load().gdn_oracle_forward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(s0),
+        _ptr(out), _ptr(final), _ptr(states),
+        cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), N, HK, HV, Dk, Dv,
+        float(scale), int(bool(use_qk_l2norm)),
+        None if ch is None else ch.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n_ch,
+        int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"gdn_oracle_forward failed ({rc})")
+    return out, final, states
+
+
+def decode_step(queries, keys, values, decays, beta, state, scale=None, use_qk_l2norm=True,
+                n_threads=None):
+    """One token per sequence: queries/keys [B, HK, Dk], values [B, HV, Dv],
+    decays/beta [B, HV], state [B, HV, Dk, Dv] (not modified).
+
+    Returns (out [B, HV, Dv], new_state [B, HV, Dk, Dv]) in float64.  This is
+    the same recurrence over sequences of length one, started from ``state``.
+    """
+    q, k, v = _f64(queries), _f64(keys), _f64(values)
+    g, b = _f64(decays), _f64(beta)
+    B = q.shape[0]
+    out, final, _ = forward(q.reshape(1, B, *q.shape[1:]), k.reshape(1, B, *k.shape[1:]),
+                            v.reshape(1, B, *v.shape[1:]), g.reshape(1, B, -1),
+                            b.reshape(1, B, -1), initial_state=state,
+                            cu_seqlens=np.arange(B + 1), scale=scale,
+                            use_qk_l2norm=use_qk_l2norm, n_threads=n_threads)
+    return out.reshape(B, *out.shape[2:]), final
+
+
+def chain(queries, keys, values, decays, beta, initial_state=None, scale=None,
+          use_qk_l2norm=True, want_states=False):
+    """One (sequence, value head) chain: queries/keys [T, Dk], values [T, Dv],
+    decays/beta [T], initial_state [Dk, Dv] or None.
+
+    Returns (out [T, Dv], final [Dk, Dv], states [T, Dk, Dv] or None) in float64.
+    Used for sampled checks on workloads whose full fp64 copy would not fit.
+    """
+    q, k, v = _f64(queries), _f64(keys), _f64(values)
+    g, b = _f64(decays), _f64(beta)
+    s0 = _f64(initial_state)
+    T, Dk = q.shape
+    Dv = v.shape[1]
+    if scale is None:
+        scale = Dk ** -0.5
+    out = np.zeros((T, Dv))
+    final = np.zeros((Dk, Dv))
+    states = np.zeros((T, Dk, Dv)) if want_states else None
+    rc = _load().gdn_oracle_chain(
+        T, Dk, Dv, _ptr(q), Dk, _ptr(k), Dk, _ptr(v), Dv, _ptr(g), _ptr(b), 1, _ptr(s0),
+        _ptr(out), Dv, _ptr(final), _ptr(states), Dk * Dv, float(scale),
+        int(bool(use_qk_l2norm)))
+    if rc != 0:
+        raise RuntimeError("gdn_oracle_chain failed")
+    return out, final, states

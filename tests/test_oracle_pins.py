@@ -1,0 +1,312 @@
+"""Pins of the fp64 oracle to facts that do not come from the oracle itself.
+
+Each test names what fixes the expected value: a closed form the rule reduces
+to, an invariant of the mathematics, a worked example computed by hand, the
+pages' own statements (qwen3_5_text page, Notes -> "The DeltaNet mixer";
+qwen3_next page, Notes -> "The DeltaNet mixer fuses its projections per key
+head"), or an independent solve of the same result.  Together they are meant
+to fail on a plausible slip anywhere in the oracle: a dropped term, a wrong
+sign, a transposed state, the wrong key head, readout before the write, the
+decay applied after the write, a missing l2 norm or scale.
+"""
+import os
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng_seed = 20261202
+
+
+def _rng(k=0):
+    return np.random.default_rng(rng_seed + k)
+
+
+def _l2n(x):
+    return x / np.sqrt((x * x).sum(-1, keepdims=True) + 1e-6)
+
+
+def _rand_case(rng, B, T, HK, HV, Dk, Dv, s0=False, g_scale=1.0):
+    q = rng.standard_normal((B, T, HK, Dk))
+    k = rng.standard_normal((B, T, HK, Dk))
+    v = rng.standard_normal((B, T, HV, Dv))
+    g = -np.log1p(np.exp(rng.standard_normal((B, T, HV)))) * g_scale
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((B, T, HV))))
+    st = rng.standard_normal((B, HV, Dk, Dv)) * 0.3 if s0 else None
+    return q, k, v, g, beta, st
+
+
+# ---------------------------------------------------------------- hand example
+def _parse_golden(path):
+    out = {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        name, rest = line.split(None, 1)
+        if ";" in rest:
+            out[name] = np.array([[float(x) for x in r.split()] for r in rest.split(";")])
+        else:
+            out[name] = np.array([[float(x) for x in r.split()] for r in rest.split("|")])
+    return out
+
+
+@pytest.mark.parametrize("case,l2", [("raw", False), ("normed", True)])
+def test_hand_worked_example(oracle_mod, case, l2):
+    """tests/golden/hand_T2_Dk2_Dv2.txt: two tokens computed by hand (decay, delta
+    write against the decayed state, read after the write, S[key][value])."""
+    G = _parse_golden(os.path.join(GOLDEN, "hand_T2_Dk2_Dv2.txt"))
+    p = lambda f: G[f"{case}.{f}"]
+    q = p("q").reshape(1, 2, 1, 2)
+    k = p("k").reshape(1, 2, 1, 2)
+    v = p("v").reshape(1, 2, 1, 2)
+    g = p("g").reshape(1, 2, 1)
+    b = p("beta").reshape(1, 2, 1)
+    o, sf, _ = oracle_mod.forward(q, k, v, g, b, scale=None if l2 else 1.0, use_qk_l2norm=l2)
+    tol = 1e-6 if l2 else 1e-14
+    np.testing.assert_allclose(o.reshape(2, 2), p("o"), atol=tol, rtol=0)
+    np.testing.assert_allclose(sf.reshape(2, 2), p("S_final"), atol=tol, rtol=0)
+
+
+# ---------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("Dk,Dv", [(5, 7), (32, 32), (128, 128)])
+def test_single_token_closed_form(oracle_mod, Dk, Dv):
+    """T = 1 from a zero state: o = beta (q~ . k^) v and S = beta k^ v^T, with
+    q~ = l2norm(q) Dk^-1/2 and k^ = l2norm(k) (the rule's closed form at T=1)."""
+    rng = _rng(1)
+    q, k, v, g, beta, _ = _rand_case(rng, 3, 1, 2, 4, Dk, Dv)
+    o, sf, _ = oracle_mod.forward(q, k, v, g, beta)
+    for b in range(3):
+        for h in range(4):
+            j = h // 2
+            qt = _l2n(q[b, 0, j]) * Dk ** -0.5
+            kt = _l2n(k[b, 0, j])
+            bb = beta[b, 0, h]
+            np.testing.assert_allclose(o[b, 0, h], bb * (qt @ kt) * v[b, 0, h], rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(sf[b, h], bb * np.outer(kt, v[b, 0, h]), rtol=1e-12, atol=1e-14)
+
+
+def test_beta_zero_no_decay(oracle_mod):
+    """beta = 0, g = 0: nothing is written.  From zero, o = 0 and S = 0; from S0,
+    S stays S0 and o_t = S0^T q~_t."""
+    rng = _rng(2)
+    q, k, v, g, beta, s0 = _rand_case(rng, 2, 9, 1, 2, 6, 4, s0=True)
+    z = np.zeros_like(g)
+    o, sf, _ = oracle_mod.forward(q, k, v, z, z)
+    assert np.all(o == 0) and np.all(sf == 0)
+    o, sf, _ = oracle_mod.forward(q, k, v, z, z, initial_state=s0)
+    np.testing.assert_allclose(sf, s0, rtol=0, atol=0)
+    for b in range(2):
+        for h in range(2):
+            qt = _l2n(q[b, :, 0]) * 6 ** -0.5
+            np.testing.assert_allclose(o[b, :, h], qt @ s0[b, h], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("with_s0", [False, True])
+def test_orthonormal_keys_projection(oracle_mod, with_s0):
+    """beta = 1, g = 0, keys orthonormal (T <= Dk): every write makes S^T k_t = v_t and
+    later writes along orthogonal keys leave it so (Widrow-Hoff projection), while S^T x
+    for x orthogonal to all keys stays S0^T x."""
+    rng = _rng(3)
+    Dk, Dv, T = 16, 8, 11
+    Qm, _ = np.linalg.qr(rng.standard_normal((Dk, Dk)))
+    keys = Qm[:, :T].T                                  # T orthonormal rows
+    k = keys.reshape(1, T, 1, Dk)
+    q = rng.standard_normal((1, T, 1, Dk))
+    v = rng.standard_normal((1, T, 1, Dv))
+    s0 = rng.standard_normal((1, 1, Dk, Dv)) if with_s0 else None
+    # keys already unit length: the l2 norm is switched off so that "exactly" holds to
+    # rounding (its 1e-6 epsilon would shorten k^ by ~5e-7).
+    o, sf, _ = oracle_mod.forward(q, k, v, np.zeros((1, T, 1)), np.ones((1, T, 1)),
+                                  initial_state=s0, use_qk_l2norm=False)
+    S = sf[0, 0]
+    for i in range(T):
+        np.testing.assert_allclose(S.T @ keys[i], v[0, i, 0], rtol=0, atol=1e-12)
+    comp = Qm[:, T:]
+    base = s0[0, 0] if with_s0 else np.zeros((Dk, Dv))
+    np.testing.assert_allclose(comp.T @ S, comp.T @ base, rtol=0, atol=1e-12)
+
+
+def test_fully_forgetting_decay(oracle_mod):
+    """g -> -inf (g = -1e4, exp underflows to 0): a token sees only its own key and
+    value: o_t = beta_t (q~_t . k^_t) v_t, and S_T = beta_T k^_T v_T^T."""
+    rng = _rng(4)
+    q, k, v, g, beta, s0 = _rand_case(rng, 2, 7, 2, 2, 8, 5, s0=True)
+    g = np.full_like(g, -1e4)
+    o, sf, _ = oracle_mod.forward(q, k, v, g, beta, initial_state=s0)
+    for b in range(2):
+        for h in range(2):
+            qt = _l2n(q[b, :, h]) * 8 ** -0.5
+            kt = _l2n(k[b, :, h])
+            exp_o = (beta[b, :, h] * (qt * kt).sum(-1))[:, None] * v[b, :, h]
+            np.testing.assert_allclose(o[b, :, h], exp_o, rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(sf[b, h], beta[b, -1, h] * np.outer(kt[-1], v[b, -1, h]),
+                                       rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- invariants
+def test_prefill_then_decode_equals_prefill(oracle_mod):
+    """The prompt kernel and the decode kernel continue one state (state_input is a copy
+    of the cache's buffer): prefill(t) then T-t decode steps = prefill(T)."""
+    rng = _rng(5)
+    q, k, v, g, beta, s0 = _rand_case(rng, 3, 20, 2, 4, 8, 6, s0=True)
+    o_full, s_full, _ = oracle_mod.forward(q, k, v, g, beta, initial_state=s0)
+    t = 13
+    o_a, s, _ = oracle_mod.forward(q[:, :t], k[:, :t], v[:, :t], g[:, :t], beta[:, :t],
+                                   initial_state=s0)
+    np.testing.assert_allclose(o_a, o_full[:, :t], rtol=0, atol=1e-12)
+    for i in range(t, 20):
+        o_i, s = oracle_mod.decode_step(q[:, i], k[:, i], v[:, i], g[:, i], beta[:, i], s)
+        np.testing.assert_allclose(o_i, o_full[:, i], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(s, s_full, rtol=0, atol=1e-12)
+
+
+def test_linear_in_values_and_state(oracle_mod):
+    """For fixed q, k, g, beta the map (V, S0) -> (O, S_T) is linear."""
+    rng = _rng(6)
+    q, k, v1, g, beta, s1 = _rand_case(rng, 1, 12, 1, 2, 6, 5, s0=True)
+    v2 = rng.standard_normal(v1.shape)
+    s2 = rng.standard_normal(s1.shape)
+    a, c = 0.7, -1.3
+    o1, f1, _ = oracle_mod.forward(q, k, v1, g, beta, initial_state=s1)
+    o2, f2, _ = oracle_mod.forward(q, k, v2, g, beta, initial_state=s2)
+    o3, f3, _ = oracle_mod.forward(q, k, a * v1 + c * v2, g, beta, initial_state=a * s1 + c * s2)
+    np.testing.assert_allclose(o3, a * o1 + c * o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(f3, a * f1 + c * f2, rtol=0, atol=1e-12)
+
+
+def test_gqa_interleave(oracle_mod):
+    """Queries and keys are repeat_interleave'd to the value heads: heads 2j and 2j+1
+    read key head j (not head h mod HK)."""
+    rng = _rng(7)
+    q, k, v, g, beta, s0 = _rand_case(rng, 2, 10, 2, 4, 8, 8, s0=True)
+    o, sf, _ = oracle_mod.forward(q, k, v, g, beta, initial_state=s0)
+    o_r, sf_r, _ = oracle_mod.forward(np.repeat(q, 2, axis=2), np.repeat(k, 2, axis=2), v, g,
+                                      beta, initial_state=s0)
+    np.testing.assert_array_equal(o, o_r)
+    np.testing.assert_array_equal(sf, sf_r)
+    o_t, _, _ = oracle_mod.forward(np.tile(q, (1, 1, 2, 1)), np.tile(k, (1, 1, 2, 1)), v, g,
+                                   beta, initial_state=s0)
+    assert np.abs(o_t - o).max() > 1e-3        # the modulo mapping is a different result
+
+
+def test_l2norm_makes_scale_irrelevant_and_matters(oracle_mod):
+    """With the in-kernel l2 norm, positive row scalings of q and k do not change the
+    result (up to the 1e-6 epsilon); turning the norm off changes it by a lot (the pages
+    report a 42% error in a final state without it)."""
+    rng = _rng(8)
+    q, k, v, g, beta, _ = _rand_case(rng, 1, 16, 2, 2, 16, 16)
+    o, sf, _ = oracle_mod.forward(q, k, v, g, beta)
+    sq = rng.uniform(0.2, 5.0, q.shape[:-1] + (1,))
+    sk = rng.uniform(0.2, 5.0, k.shape[:-1] + (1,))
+    o2, sf2, _ = oracle_mod.forward(q * sq, k * sk, v, g, beta)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-6)
+    np.testing.assert_allclose(sf2, sf, rtol=0, atol=1e-6)
+    o3, sf3, _ = oracle_mod.forward(q, k, v, g, beta, use_qk_l2norm=False)
+    rel = np.linalg.norm(sf3 - sf) / np.linalg.norm(sf)
+    assert rel > 0.1
+
+
+def test_zero_rows_stay_finite(oracle_mod):
+    """An all-zero query or key row gives zeros, not NaN (l2 norm with epsilon)."""
+    rng = _rng(9)
+    q, k, v, g, beta, _ = _rand_case(rng, 1, 6, 1, 1, 8, 8)
+    q[0, 2] = 0
+    k[0, 3] = 0
+    o, sf, _ = oracle_mod.forward(q, k, v, g, beta)
+    assert np.isfinite(o).all() and np.isfinite(sf).all()
+    assert np.all(o[0, 2] == 0)
+
+
+def test_packed_equals_separate(oracle_mod):
+    """A packed batch with cu_seqlens (zero-length sequences allowed) equals the
+    sequences run one by one; a zero-length sequence returns its initial state."""
+    rng = _rng(10)
+    lens = [5, 0, 17, 1, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    Tt = cu[-1]
+    q, k, v, g, beta, _ = _rand_case(rng, 1, Tt, 2, 4, 8, 6)
+    s0 = rng.standard_normal((len(lens), 4, 8, 6))
+    o, sf, st = oracle_mod.forward(q, k, v, g, beta, initial_state=s0, cu_seqlens=cu,
+                                   want_states=True)
+    for i, L in enumerate(lens):
+        a, b = cu[i], cu[i + 1]
+        if L == 0:
+            np.testing.assert_array_equal(sf[i], s0[i])
+            continue
+        oi, fi, sti = oracle_mod.forward(q[:, a:b], k[:, a:b], v[:, a:b], g[:, a:b],
+                                         beta[:, a:b], initial_state=s0[i:i + 1],
+                                         want_states=True)
+        np.testing.assert_array_equal(o[:, a:b], oi)
+        np.testing.assert_array_equal(sf[i], fi[0])
+        np.testing.assert_array_equal(st[:, a:b], sti)
+        np.testing.assert_array_equal(sti[0, -1], fi[0])
+
+
+def test_chain_entry_matches_forward(oracle_mod):
+    """The single-chain entry used for sampled checks is the same computation."""
+    rng = _rng(11)
+    q, k, v, g, beta, s0 = _rand_case(rng, 2, 13, 2, 4, 8, 6, s0=True)
+    o, sf, st = oracle_mod.forward(q, k, v, g, beta, initial_state=s0, want_states=True)
+    for b, h in [(0, 0), (1, 3), (0, 2)]:
+        oc, fc, sc = oracle_mod.chain(q[b, :, h // 2], k[b, :, h // 2], v[b, :, h],
+                                      g[b, :, h], beta[b, :, h], initial_state=s0[b, h],
+                                      want_states=True)
+        np.testing.assert_array_equal(oc, o[b, :, h])
+        np.testing.assert_array_equal(fc, sf[b, h])
+        np.testing.assert_array_equal(sc, st[b, :, h])
+
+
+def test_chain_subset_only_touches_listed(oracle_mod):
+    rng = _rng(12)
+    q, k, v, g, beta, _ = _rand_case(rng, 2, 5, 1, 2, 4, 4)
+    o, sf, _ = oracle_mod.forward(q, k, v, g, beta, chains=[1, 2])
+    assert np.isnan(o[0, :, 0]).all() and np.isfinite(o[0, :, 1]).all()
+    assert np.isfinite(o[1, :, 0]).all() and np.isnan(o[1, :, 1]).all()
+
+
+# ---------------------------------------------------------------- independent solve
+def _wy_one_chunk(q, k, v, g, beta, s0, scale):
+    """The whole sequence as one chunk, solved in closed form with numpy:
+    with G_t = sum_{s<=t} g_s, A_tj = beta_t e^{G_t-G_j} (k^_t . k^_j) for j < t,
+    (I + A) U = diag(beta) (V - diag(e^G) K^ S0), O = diag(e^G) Q~ S0 + (M o Q~K^^T) U
+    with M_tj = e^{G_t-G_j} for j <= t, S_T = e^{G_T} S0 + sum_j e^{G_T-G_j} k^_j u_j^T.
+    Derived by unrolling the recurrence over one chunk; np.linalg.solve does the
+    triangular solve."""
+    T = q.shape[0]
+    qn = _l2n(q) * scale
+    kn = _l2n(k)
+    G = np.cumsum(g)
+    D = np.exp(G[:, None] - G[None, :])
+    low = np.tril(np.ones((T, T)), -1)
+    A = beta[:, None] * D * (kn @ kn.T) * low
+    rhs = beta[:, None] * (v - np.exp(G)[:, None] * (kn @ s0))
+    U = np.linalg.solve(np.eye(T) + A, rhs)
+    P = D * (qn @ kn.T) * np.tril(np.ones((T, T)))
+    O = np.exp(G)[:, None] * (qn @ s0) + P @ U
+    ST = np.exp(G[-1]) * s0 + (np.exp(G[-1] - G)[:, None] * kn).T @ U
+    return O, ST
+
+
+@pytest.mark.parametrize("T,Dk,Dv,g_scale", [(1, 8, 8, 1.0), (37, 16, 12, 1.0),
+                                             (64, 32, 32, 0.05), (128, 32, 16, 0.01)])
+def test_matches_independent_one_chunk_solve(oracle_mod, T, Dk, Dv, g_scale):
+    rng = _rng(13 + T)
+    q, k, v, g, beta, s0 = _rand_case(rng, 1, T, 1, 1, Dk, Dv, s0=True, g_scale=g_scale)
+    o, sf, _ = oracle_mod.forward(q, k, v, g, beta, initial_state=s0)
+    O, ST = _wy_one_chunk(q[0, :, 0], k[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0],
+                          s0[0, 0], Dk ** -0.5)
+    np.testing.assert_allclose(o[0, :, 0], O, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(sf[0, 0], ST, rtol=0, atol=1e-10)
+
+
+def test_per_token_states_are_the_running_state(oracle_mod):
+    """states[t] is the state after token t: o_t = states[t]^T q~_t and the last one is
+    the final state."""
+    rng = _rng(14)
+    q, k, v, g, beta, s0 = _rand_case(rng, 1, 10, 1, 1, 6, 5, s0=True)
+    o, sf, st = oracle_mod.forward(q, k, v, g, beta, initial_state=s0, want_states=True)
+    qn = _l2n(q[0, :, 0]) * 6 ** -0.5
+    for t in range(10):
+        np.testing.assert_allclose(o[0, t, 0], st[0, t, 0].T @ qn[t], rtol=0, atol=1e-13)
+    np.testing.assert_array_equal(st[0, -1, 0], sf[0, 0])
