@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Throughput of the gated delta rule kernels on one GB300 (or N, weak scaling).
+
+One step = one chunked prefill of the Qwen3-Next-shaped workload (batch 1,
+4096 tokens, 16 key heads over 32 value heads, 128 x 128 heads, bf16 q/k/v,
+fp32 decays/beta, zero initial state) through the C ABI.  The JSON line's
+``value`` is prefill tokens/s over all ranks; the decode step (B=256, state
+[256,32,128,128] fp32 in place), the packed varlen prefill, the long-context
+prefill and the per-token state emission are measured in the same run and
+reported as sub-objects with their own rooflines.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Inputs are seeded synthetic tensors resident in HBM before timing; between
+timed prefill iterations a 256 MiB buffer is written to flush the 129 MB L2
+(the decode state, 512 MiB, is larger than L2 by itself).  Kernel times are
+CUDA-event times on the launching stream.  ``--impl reference`` times the fp64
+CPU oracle on the host cores instead (bounded sample of the same workload).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "GDN prefill tokens/s and decode steps/s (1 GB300) + % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic work
+def prefill_bytes(B_tokens, HK, HV, D, elt, n_states_in, n_states_out, states_tokens=0):
+    """Bytes a prefill must move at least once: q, k, v, o (elt bytes), g and beta (fp32),
+    initial states read, final states written, per-token states written."""
+    io = B_tokens * (2 * HK * D * elt + 2 * HV * D * elt + 2 * HV * 4)
+    st = (n_states_in + n_states_out) * HV * D * D * 4
+    return io + st + states_tokens * HV * D * D * 4
+
+
+def prefill_flops(tokens, HV, D, C=64):
+    """Chunked-form flops per token per value head: five C x C x D and three C x D x D
+    products per chunk -> 10 C D + 6 D^2."""
+    return tokens * HV * (10 * C * D + 6 * D * D)
+
+
+def decode_bytes(B, HK, HV, D, elt):
+    return B * HV * D * D * 4 * 2 + B * (2 * HK * D * elt + 2 * HV * D * elt + 2 * HV * 4)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+        self.out = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.out):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 power=float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.out)
+        if not rows:
+            return None
+        smax = max(r["smax"] for r in rows)
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
+
+
+# ---------------------------------------------------------------- timing helpers
+class Timer:
+    """Per-iteration CUDA-event timing on the current stream, L2 flushed in between."""
+
+    def __init__(self, flush=True):
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda") \
+            if flush else None
+        self.times = []
+
+    def run(self, fn, iters, warmup):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(iters):
+            if self.flush_buf is not None:
+                self.flush_buf.fill_(1.0)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]   # ms
+
+
+def bench_prefill(gdn, w, iters, warmup, states=False, T_override=None):
+    d = workloads.workload_inputs(w, device="cuda", T_override=T_override)
+    q, k, v, g, b = d["queries"], d["keys"], d["values"], d["decays"], d["beta"]
+    s0 = d["initial_state"]
+    dev = q.device
+    if w.n_seqs:
+        cu = d["cu_seqlens"]
+        N, T_total = w.n_seqs, q.shape[1]
+    else:
+        N, T_total = w.B, w.B * q.shape[1]
+    HV, D = w.HV, w.Dk
+    out = torch.empty_like(v)
+    fin = torch.empty(N, HV, D, D, dtype=torch.float32, device=dev)
+    st = torch.empty(*v.shape[:-1], D, D, dtype=torch.float32, device=dev) if states else None
+    ws = torch.empty(gdn.workspace_size(T_total, N, HV, D, D), dtype=torch.uint8, device=dev)
+    if w.n_seqs:
+        fn = lambda: gdn.prefill_varlen(q, k, v, g, b, cu, s0, out=out, final_state=fin,
+                                        states=st, workspace=ws)
+    else:
+        fn = lambda: gdn.prefill(q, k, v, g, b, s0, out=out, final_state=fin, states=st,
+                                 workspace=ws)
+    times = Timer(flush=True).run(fn, iters, warmup)
+    elt = q.element_size()
+    nbytes = prefill_bytes(T_total, w.HK, HV, D, elt, N if s0 is not None else 0, N,
+                           T_total if states else 0)
+    flops = prefill_flops(T_total, HV, D)
+    res = dict(tokens=T_total, ms=statistics.mean(times), ms_min=min(times), bytes=nbytes,
+               flops=flops, launches_per_call=(3 if w.n_seqs else 2))
+    del q, k, v, g, b, s0, out, fin, st, ws, d
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode(gdn, w, iters, warmup):
+    d = workloads.decode_inputs(w, steps=16, device="cuda")
+    state = d["initial_state"]
+    out = torch.empty(w.B, w.HV, w.Dv, dtype=w.dtype, device="cuda")
+    i = [0]
+
+    def fn():
+        s = i[0] % 16
+        i[0] += 1
+        gdn.decode_step(d["queries"][s], d["keys"][s], d["values"][s], d["decays"][s],
+                        d["beta"][s], state, out=out)
+
+    # the 512 MiB state is larger than L2: no flush needed between steps
+    times = Timer(flush=False).run(fn, iters, warmup)
+    nbytes = decode_bytes(w.B, w.HK, w.HV, w.Dk, 2)
+    res = dict(ms=statistics.mean(times), ms_min=min(times), bytes=nbytes)
+    del d, state, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_e2e(gdn, w, iters, warmup):
+    """Public API end to end: pinned host inputs -> device, prefill, out and final state
+    back to pinned host memory, every step."""
+    d = workloads.workload_inputs(w, device="cpu")
+    names = ("queries", "keys", "values", "decays", "beta")
+    host = {n: d[n].pin_memory() for n in names}
+    dev = {n: torch.empty_like(host[n], device="cuda") for n in names}
+    B, T = w.B, w.T
+    out_h = torch.empty(B, T, w.HV, w.Dv, dtype=w.dtype).pin_memory()
+    fin_h = torch.empty(B, w.HV, w.Dk, w.Dv, dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(out_h, device="cuda")
+    fin_d = torch.empty_like(fin_h, device="cuda")
+    ws = torch.empty(gdn.workspace_size(B * T, B, w.HV, w.Dk, w.Dv), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        gdn.prefill(dev["queries"], dev["keys"], dev["values"], dev["decays"], dev["beta"],
+                    None, out=out_d, final_state=fin_d, workspace=ws)
+        out_h.copy_(out_d, non_blocking=True)
+        fin_h.copy_(fin_d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(iters):
+        step()
+    dt = (time.perf_counter() - t0) / iters
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * 4
+    return dict(s=dt, h2d=h2d, d2h=d2h, tokens=B * T)
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def oracle_sample(w, target_s=12.0, max_chains=None):
+    """Time the fp64 oracle on a bounded sample of the workload: whole chains (all of a
+    sequence's tokens for one value head), as many as fit in ~target_s on the host cores.
+    Returns (tokens/s equivalent for all heads, cores, description)."""
+    import oracle
+    d = workloads.workload_inputs(w, device="cpu", T_override=min(w.T, 4096) if w.T else None)
+    T = d["queries"].shape[1]
+    cores = oracle.default_threads()
+    # one chain first, to size the sample
+    t0 = time.perf_counter()
+    oracle.forward(d["queries"][:1], d["keys"][:1], d["values"][:1], d["decays"][:1],
+                   d["beta"][:1], chains=[0], n_threads=1)
+    one = time.perf_counter() - t0
+    n = max(1, min(w.HV * w.B if not max_chains else max_chains,
+                   int(target_s * cores / max(one, 1e-6))))
+    n = min(n, w.B * w.HV)
+    chains = list(range(n))
+    t0 = time.perf_counter()
+    oracle.forward(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                   chains=chains, n_threads=cores)
+    el = time.perf_counter() - t0
+    tok_per_s = (n / w.HV) * T / el
+    return tok_per_s, cores, f"{n} (sequence, value head) chains x {T} tokens of {w.name}, fp64", el
+
+
+# ---------------------------------------------------------------- main
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS["next_prefill_T4096_hk16_hv32_d128"]
+    vals = []
+    desc = cores = None
+    for _ in range(args.warmup):
+        pass   # the oracle has no warm-up state; nothing to do
+    for _ in range(args.steps):
+        v, cores, desc, _ = oracle_sample(w, target_s=max(2.0, 60.0 / max(args.steps, 1)))
+        vals.append(v)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * 4096 / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "HK": w.HK, "HV": w.HV,
+                       "Dk": w.Dk, "Dv": w.Dv},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline and decode only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import gated_deltanet_mixer_delta_gb300 as gdn
+    gdn.load_library(build_if_missing=True)
+    torch.cuda.set_device(local)
+    P, peak_src = peaks()
+    hbm = P["hbm_gbs"]
+    clocks = ClockSampler(local)
+    clocks.start()
+
+    W = workloads.WORKLOADS
+    head_w = W["next_prefill_T4096_hk16_hv32_d128"]
+    barrier(ws)
+    head = bench_prefill(gdn, head_w, args.steps, args.warmup)
+    barrier(ws)
+    ms = max_over_ranks(head["ms"], ws)
+    value = ws * head["tokens"] / (ms * 1e-3)
+    dec = bench_decode(gdn, W["decode_B256_hk16_hv32_d128"], max(args.steps, 20), args.warmup)
+    dec_ms = max_over_ranks(dec["ms"], ws)
+
+    subs = {}
+    if not args.quick:
+        for key, name, kw in (("varlen", "varlen8_512to8192_hk16_hv32_d128", {}),
+                              ("long_prefill", "long_prefill_B2_T65536_hk16_hv32_d128", {}),
+                              ("states", "states_B4_T1024_hk16_hv32_d128", {"states": True})):
+            r = bench_prefill(gdn, W[name], max(3, min(args.steps, 5)), 3, **kw)
+            subs[key] = dict(workload=name, tokens=r["tokens"], ms=r["ms"],
+                             tokens_per_s=r["tokens"] / (r["ms"] * 1e-3),
+                             roofline={"bound": "hbm", "achieved": r["bytes"] / (r["ms"] * 1e-3) / 1e9,
+                                       "peak": hbm, "unit": "GB/s",
+                                       "frac": r["bytes"] / (r["ms"] * 1e-3) / 1e9 / hbm,
+                                       "algorithmic_bytes": r["bytes"]})
+    e2e = bench_e2e(gdn, head_w, max(5, min(args.steps, 20)), 2)
+    clk = clocks.stop()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_sample(head_w)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return
+    achieved = head["bytes"] / (head["ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": head_w.name, "B": head_w.B, "T": head_w.T, "HK": head_w.HK,
+                   "HV": head_w.HV, "Dk": head_w.Dk, "Dv": head_w.Dv,
+                   "l2": "flushed between timed iterations (256 MiB write)",
+                   "parallelism": f"replicas x{ws} (independent batches)"},
+        "roofline": {"bound": "hbm", "kernel": "gdn_prefill (prep + scan)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "peak_source": peak_src,
+                     "algorithmic_bytes": head["bytes"], "flops": head["flops"]},
+        "decode": {"workload": "decode_B256_hk16_hv32_d128", "value": 1e3 / dec_ms * ws,
+                   "unit": "steps/s", "ms_per_step": dec_ms,
+                   "roofline": {"bound": "hbm", "kernel": "decode_kernel",
+                                "achieved": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9 / hbm,
+                                "algorithmic_bytes": dec["bytes"]}},
+        "e2e": {"value": e2e["tokens"] / e2e["s"] * ws, "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": args.steps * head["launches_per_call"],
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    line.update(subs)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,269 @@
+"""Gated delta rule kernels for GB300 (sm_103a): Python binding of ``libgdn.so``.
+
+The gated delta rule is the recurrence of the Gated DeltaNet mixer in the
+Qwen3.5 / Qwen3-Next hybrid models (qwen3_5_text page, Notes -> "The DeltaNet
+mixer"; qwen3_next page, Notes -> "The DeltaNet mixer fuses its projections per
+key head").  This module only marshals arguments: it checks tensors, allocates
+outputs with PyTorch when the caller passes none, and calls the C ABI of
+``include/gdn.h`` on the current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels; there is no other implementation to fall
+back to, and a missing library is an error.
+
+Layouts (the pages' linear_attn value table):
+    queries, keys  [B, T, HK, Dk]        values, out  [B, T, HV, Dv]
+    decays, beta   [B, T, HV] float32    state        [B, HV, Dk, Dv] float32
+    states         [B, T, HV, Dk, Dv] float32 (state after every token)
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = ["prefill", "prefill_varlen", "decode_step", "state_layout", "workspace_size",
+           "workspace_status", "GdnError", "library_path", "load_library", "abi"]
+
+GDN_OK = 0
+_STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported shape or dtype",
+           -3: "pointer not aligned", -4: "workspace missing or too small",
+           -5: "CUDA launch or runtime error", -6: "bounded device wait timed out",
+           -7: "cu_seqlens malformed"}
+_DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, 'unknown status')} ({status})")
+
+
+class _StateLayout(ctypes.Structure):
+    _fields_ = [("bytes", ctypes.c_size_t), ("bytes_per_head", ctypes.c_size_t),
+                ("stride", ctypes.c_int64 * 4), ("shape", ctypes.c_int64 * 4),
+                ("alignment", ctypes.c_int)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False):
+    """Load libgdn.so (the C ABI).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if build_if_missing:
+            _build.build()
+        else:
+            raise RuntimeError(f"libgdn.so not built ({path}); run "
+                               "gated_deltanet_mixer_delta_gb300.build.build() first")
+    lib = ctypes.CDLL(path)
+    vp, fp, i, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    f = ctypes.c_float
+    lib.gdn_prefill.restype = i
+    lib.gdn_prefill.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, i, i, i, i, f, i,
+                                vp, sz, vp]
+    lib.gdn_prefill_varlen.restype = i
+    lib.gdn_prefill_varlen.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, vp, i, i, i, i, i, i,
+                                       i, f, i, vp, sz, vp]
+    lib.gdn_decode_step.restype = i
+    lib.gdn_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.gdn_state_layout.restype = i
+    lib.gdn_state_layout.argtypes = [i, i, i, i, ctypes.POINTER(_StateLayout)]
+    lib.gdn_prefill_workspace_size.restype = sz
+    lib.gdn_prefill_workspace_size.argtypes = [ctypes.c_int64, i, i, i, i]
+    lib.gdn_workspace_status.restype = i
+    lib.gdn_workspace_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [i]
+    lib.gdn_abi_version.restype = i
+    lib.gdn_abi_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def abi():
+    """The loaded ctypes library (raw C ABI)."""
+    return load_library()
+
+
+def _check(rc, where):
+    if rc != GDN_OK:
+        raise GdnError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype=None, device=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def state_layout(batch, HV, Dk, Dv):
+    """Shape, strides and bytes of the recurrent state buffer [batch, HV, Dk, Dv] float32."""
+    lay = _StateLayout()
+    _check(load_library().gdn_state_layout(batch, HV, Dk, Dv, ctypes.byref(lay)), "gdn_state_layout")
+    return dict(bytes=lay.bytes, bytes_per_head=lay.bytes_per_head, stride=tuple(lay.stride),
+                shape=tuple(lay.shape), alignment=lay.alignment)
+
+
+def workspace_size(T_total, n_seqs, HV, Dk, Dv) -> int:
+    return int(load_library().gdn_prefill_workspace_size(T_total, n_seqs, HV, Dk, Dv))
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Device status word of the last prefill that used ``workspace`` (0 = ok)."""
+    st = ctypes.c_int(0)
+    _check(load_library().gdn_workspace_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
+           "gdn_workspace_status")
+    return st.value
+
+
+def _workspace(workspace, nbytes, device):
+    if workspace is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    _need(workspace, "workspace", torch.uint8, device)
+    if workspace.numel() < nbytes:
+        raise GdnError(-4, "workspace")
+    return workspace
+
+
+def prefill(queries, keys, values, decays, beta, initial_state=None, *, scale=None,
+            use_qk_l2norm=True, output_states=False, out=None, final_state=None, states=None,
+            workspace=None, stream=None):
+    """Chunked prefill over a batch of equal-length sequences (gdn_prefill).
+
+    Returns ``(out, final_state, states)``; ``states`` is None unless
+    ``output_states`` is set or a ``states`` tensor is passed.
+    """
+    _need(queries, "queries")
+    dev, dt = queries.device, queries.dtype
+    if dt not in _DTYPES:
+        raise ValueError("queries/keys/values must be bfloat16 or float32")
+    B, T, HK, Dk = queries.shape
+    HV, Dv = values.shape[2], values.shape[3]
+    _need(keys, "keys", dt, dev, (B, T, HK, Dk))
+    _need(values, "values", dt, dev, (B, T, HV, Dv))
+    _need(decays, "decays", torch.float32, dev, (B, T, HV))
+    _need(beta, "beta", torch.float32, dev, (B, T, HV))
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev, (B, HV, Dk, Dv))
+    if out is None:
+        out = torch.empty(B, T, HV, Dv, dtype=dt, device=dev)
+    _need(out, "out", dt, dev, (B, T, HV, Dv))
+    if final_state is None:
+        final_state = torch.empty(B, HV, Dk, Dv, dtype=torch.float32, device=dev)
+    _need(final_state, "final_state", torch.float32, dev, (B, HV, Dk, Dv))
+    if states is None and output_states:
+        states = torch.empty(B, T, HV, Dk, Dv, dtype=torch.float32, device=dev)
+    if states is not None:
+        _need(states, "states", torch.float32, dev, (B, T, HV, Dk, Dv))
+    lib = load_library()
+    nbytes = lib.gdn_prefill_workspace_size(B * T, B, HV, Dk, Dv)
+    ws = _workspace(workspace, nbytes, dev)
+    rc = lib.gdn_prefill(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays), _ptr(beta),
+                         _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(states),
+                         B, T, HK, HV, Dk, Dv, _DTYPES[dt], float(scale or 0.0),
+                         int(bool(use_qk_l2norm)), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "gdn_prefill")
+    return out, final_state, states
+
+
+def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_state=None, *,
+                   scale=None, use_qk_l2norm=True, output_states=False, out=None,
+                   final_state=None, states=None, workspace=None, stream=None):
+    """Chunked prefill over sequences packed back to back (gdn_prefill_varlen).
+
+    queries/keys [1, T_total, HK, Dk] (or [T_total, HK, Dk]), values [.., T_total, HV, Dv],
+    decays/beta [.., T_total, HV], ``cu_seqlens`` int32 [N+1] on the device,
+    initial_state [N, HV, Dk, Dv] or None.  Returns ``(out, final_state [N, HV, Dk, Dv],
+    states)``; out and states keep the leading shape of ``values``.
+    """
+    _need(queries, "queries")
+    dev, dt = queries.device, queries.dtype
+    if dt not in _DTYPES:
+        raise ValueError("queries/keys/values must be bfloat16 or float32")
+    lead = tuple(values.shape[:-2])
+    T_total = queries.shape[-3]
+    HK, Dk = queries.shape[-2], queries.shape[-1]
+    HV, Dv = values.shape[-2], values.shape[-1]
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    N = cu_seqlens.numel() - 1
+    if N < 0:
+        raise ValueError("cu_seqlens needs at least one entry")
+    _need(keys, "keys", dt, dev, queries.shape)
+    _need(values, "values", dt, dev)
+    _need(decays, "decays", torch.float32, dev, lead)
+    _need(beta, "beta", torch.float32, dev, lead)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev, (N, HV, Dk, Dv))
+    if out is None:
+        out = torch.empty(*lead, HV, Dv, dtype=dt, device=dev)
+    _need(out, "out", dt, dev, values.shape)
+    if final_state is None:
+        final_state = torch.empty(N, HV, Dk, Dv, dtype=torch.float32, device=dev)
+    _need(final_state, "final_state", torch.float32, dev, (N, HV, Dk, Dv))
+    if states is None and output_states:
+        states = torch.empty(*lead, HV, Dk, Dv, dtype=torch.float32, device=dev)
+    if states is not None:
+        _need(states, "states", torch.float32, dev, (*lead, HV, Dk, Dv))
+    lib = load_library()
+    nbytes = lib.gdn_prefill_workspace_size(T_total, N, HV, Dk, Dv)
+    ws = _workspace(workspace, nbytes, dev)
+    rc = lib.gdn_prefill_varlen(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays),
+                                _ptr(beta), _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                _ptr(states), _ptr(cu_seqlens), N, T_total, HK, HV, Dk, Dv,
+                                _DTYPES[dt], float(scale or 0.0), int(bool(use_qk_l2norm)),
+                                _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "gdn_prefill_varlen")
+    return out, final_state, states
+
+
+def decode_step(queries, keys, values, decays, beta, state, *, scale=None, use_qk_l2norm=True,
+                out=None, stream=None):
+    """One decode step (gdn_decode_step): queries/keys [B, HK, Dk], values [B, HV, Dv],
+    decays/beta [B, HV], state [B, HV, Dk, Dv] float32 updated in place.  Returns out
+    [B, HV, Dv]."""
+    _need(queries, "queries")
+    dev, dt = queries.device, queries.dtype
+    if dt not in _DTYPES:
+        raise ValueError("queries/keys/values must be bfloat16 or float32")
+    B, HK, Dk = queries.shape
+    HV, Dv = values.shape[1], values.shape[2]
+    _need(keys, "keys", dt, dev, (B, HK, Dk))
+    _need(values, "values", dt, dev, (B, HV, Dv))
+    _need(decays, "decays", torch.float32, dev, (B, HV))
+    _need(beta, "beta", torch.float32, dev, (B, HV))
+    _need(state, "state", torch.float32, dev, (B, HV, Dk, Dv))
+    if out is None:
+        out = torch.empty(B, HV, Dv, dtype=dt, device=dev)
+    _need(out, "out", dt, dev, (B, HV, Dv))
+    rc = load_library().gdn_decode_step(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays),
+                                        _ptr(beta), _ptr(state), _ptr(out), B, HK, HV, Dk, Dv,
+                                        _DTYPES[dt], float(scale or 0.0),
+                                        int(bool(use_qk_l2norm)), _stream(stream))
+    _check(rc, "gdn_decode_step")
+    return out

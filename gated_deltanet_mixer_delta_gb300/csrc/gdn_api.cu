@@ -1,0 +1,198 @@
+// gdn_api.cu -- the C ABI (include/gdn.h): argument checks, workspace layout, dispatch.
+//
+// Every check that can be made on the host is made here, before anything is
+// enqueued; nothing here allocates device memory or keeps state between calls.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+static inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int max_chunks_for(int64_t T_total, int n_seqs, bool packed, int T_seq) {
+    if (!packed) return n_seqs * ((T_seq + kChunk - 1) / kChunk);
+    return (int)((T_total + kChunk - 1) / kChunk + n_seqs);
+}
+
+// header | chunk_seq[max_chunks] | chunk_first[N+1] | records[max_chunks][HV]
+static size_t table_bytes(int max_chunks, int n_seqs) {
+    return round_up(sizeof(int32_t) * ((size_t)max_chunks + n_seqs + 1), 256);
+}
+
+size_t prefill_workspace_bytes(int64_t T_total, int n_seqs, int HV, int Dk, int Dv) {
+    // sized for the packed bound, which also covers equal-length batches
+    const int mc = max_chunks_for(T_total, n_seqs, true, 0);
+    return kWsHeader + table_bytes(mc, n_seqs) +
+           (size_t)mc * HV * record_floats(Dk, Dv) * sizeof(float);
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+namespace {
+
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_common(int HK, int HV, int Dk, int Dv, gdn_dtype dtype, float scale) {
+    if (HK <= 0 || HV <= 0 || HV % HK != 0) return GDN_ERR_INVALID_ARG;
+    if (!dim_ok(Dk) || Dv != Dk) return GDN_ERR_UNSUPPORTED;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+    if (isnan(scale) || isinf(scale)) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+float resolve_scale(float scale, int Dk) { return scale > 0.f ? scale : 1.0f / sqrtf((float)Dk); }
+
+int prefill_common(const void *queries, const void *keys, const void *values,
+                   const float *decays, const float *beta, const float *initial_state,
+                   void *out, float *final_state, float *states, const int32_t *cu_seqlens,
+                   int N, int T_seq, int64_t T_total, int HK, int HV, int Dk, int Dv,
+                   gdn_dtype dtype, float scale, int use_qk_l2norm, void *workspace,
+                   size_t workspace_bytes, void *cuda_stream) {
+    int rc = check_common(HK, HV, Dk, Dv, dtype, scale);
+    if (rc != GDN_OK) return rc;
+    if (N < 0 || T_total < 0 || T_seq < 0) return GDN_ERR_INVALID_ARG;
+    if (T_total > INT32_MAX || N > 65535 || HV > 65535) return GDN_ERR_UNSUPPORTED;
+    if (N > 0 && !final_state) return GDN_ERR_INVALID_ARG;
+    if (T_total > 0 && (!queries || !keys || !values || !decays || !beta || !out))
+        return GDN_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && N > 0 && T_seq > 0 && (int64_t)N * T_seq != T_total)
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {queries, keys, values, decays, beta, initial_state, out,
+                          final_state, states, cu_seqlens};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    // final_state may be initial_state (in place); no other overlap is checked here
+    if (!workspace) return GDN_ERR_WORKSPACE;
+    if ((uintptr_t)workspace & 255u) return GDN_ERR_MISALIGNED;
+    if (workspace_bytes < prefill_workspace_bytes(T_total, N, HV, Dk, Dv)) return GDN_ERR_WORKSPACE;
+
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    const bool packed = cu_seqlens != nullptr;
+    const int mc = max_chunks_for(T_total, N, packed, T_seq);
+    char *ws = (char *)workspace;
+    PrefillParams p;
+    memset(&p, 0, sizeof p);
+    p.q = queries; p.k = keys; p.v = values; p.g = decays; p.beta = beta;
+    p.s0 = initial_state; p.out = out; p.s_final = final_state; p.states = states;
+    p.cu_seqlens = cu_seqlens;
+    p.N = N; p.T_seq = T_seq; p.T_total = T_total;
+    p.HK = HK; p.HV = HV; p.Dk = Dk; p.Dv = Dv;
+    p.scale = resolve_scale(scale, Dk);
+    p.l2norm = use_qk_l2norm ? 1 : 0;
+    p.max_chunks = mc;
+    p.status = (int32_t *)ws;
+    p.chunk_seq = (int32_t *)(ws + kWsHeader);
+    p.chunk_first = p.chunk_seq + mc;
+    p.rec = (float *)(ws + kWsHeader + table_bytes(mc, N));
+    p.rec_floats = record_floats(Dk, Dv);
+
+    if (N == 0) {
+        // nothing to run; leave a clean status word
+        if (cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), st) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        return GDN_OK;
+    }
+    cudaError_t e = launch_prefill_generic(p, dtype, st);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_prefill(const void *queries, const void *keys, const void *values, const float *decays,
+                const float *beta, const float *initial_state, void *out, float *final_state,
+                float *states, int B, int T, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                float scale, int use_qk_l2norm, void *workspace, size_t workspace_bytes,
+                void *cuda_stream) {
+    if (B < 0 || T < 0) return GDN_ERR_INVALID_ARG;
+    return prefill_common(queries, keys, values, decays, beta, initial_state, out, final_state,
+                          states, nullptr, B, T, (int64_t)B * T, HK, HV, Dk, Dv, dtype, scale,
+                          use_qk_l2norm, workspace, workspace_bytes, cuda_stream);
+}
+
+int gdn_prefill_varlen(const void *queries, const void *keys, const void *values,
+                       const float *decays, const float *beta, const float *initial_state,
+                       void *out, float *final_state, float *states, const int32_t *cu_seqlens,
+                       int N, int T_total, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                       float scale, int use_qk_l2norm, void *workspace, size_t workspace_bytes,
+                       void *cuda_stream) {
+    if (N < 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+    return prefill_common(queries, keys, values, decays, beta, initial_state, out, final_state,
+                          states, cu_seqlens, N, 0, T_total, HK, HV, Dk, Dv, dtype, scale,
+                          use_qk_l2norm, workspace, workspace_bytes, cuda_stream);
+}
+
+int gdn_decode_step(const void *queries, const void *keys, const void *values,
+                    const float *decays, const float *beta, float *state, void *out, int B,
+                    int HK, int HV, int Dk, int Dv, gdn_dtype dtype, float scale,
+                    int use_qk_l2norm, void *cuda_stream) {
+    int rc = check_common(HK, HV, Dk, Dv, dtype, scale);
+    if (rc != GDN_OK) return rc;
+    if (B < 0) return GDN_ERR_INVALID_ARG;
+    if (B == 0) return GDN_OK;
+    if (!queries || !keys || !values || !decays || !beta || !state || !out)
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {queries, keys, values, decays, beta, state, out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    if ((int64_t)B * HV > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+    cudaError_t e = launch_decode(queries, keys, values, decays, beta, state, out, B, HK, HV, Dk,
+                                  Dv, dtype, resolve_scale(scale, Dk), use_qk_l2norm ? 1 : 0,
+                                  (cudaStream_t)cuda_stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_state_layout(int batch, int HV, int Dk, int Dv, gdn_state_layout_t *layout) {
+    if (!layout || batch < 0 || HV <= 0 || Dk <= 0 || Dv <= 0) return GDN_ERR_INVALID_ARG;
+    layout->bytes_per_head = (size_t)Dk * Dv * sizeof(float);
+    layout->bytes = (size_t)batch * HV * layout->bytes_per_head;
+    layout->shape[0] = batch; layout->shape[1] = HV; layout->shape[2] = Dk; layout->shape[3] = Dv;
+    layout->stride[3] = 1;
+    layout->stride[2] = Dv;
+    layout->stride[1] = (int64_t)Dk * Dv;
+    layout->stride[0] = (int64_t)HV * Dk * Dv;
+    layout->alignment = 16;
+    return GDN_OK;
+}
+
+size_t gdn_prefill_workspace_size(int64_t T_total, int n_seqs, int HV, int Dk, int Dv) {
+    if (T_total < 0 || n_seqs < 0 || HV <= 0 || !dim_ok(Dk) || !dim_ok(Dv)) return 0;
+    return prefill_workspace_bytes(T_total, n_seqs, HV, Dk, Dv);
+}
+
+int gdn_workspace_status(const void *workspace, void *cuda_stream, int *status) {
+    if (!workspace || !status) return GDN_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+    *status = v;
+    return GDN_OK;
+}
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case GDN_ERR_MISALIGNED: return "pointer not aligned";
+    case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+    case GDN_ERR_CUDA: return "CUDA launch or runtime error";
+    case GDN_ERR_TIMEOUT: return "bounded device wait timed out";
+    case GDN_ERR_BAD_SEQLENS: return "cu_seqlens is not 0 = c0 <= ... <= cN = T_total";
+    default: return "unknown status";
+    }
+}
+
+int gdn_abi_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// gdn_internal.cuh -- shared definitions of the CUDA path (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;            // tokens per chunk of the chunked prefill
+constexpr float kL2Eps = 1e-6f;       // l2norm(x) = x / sqrt(sum x^2 + eps)
+
+// Workspace header: status words, then the chunk table of a packed batch.
+constexpr size_t kWsHeader = 256;     // int32 status[64]: [0] status, [1] number of chunks
+enum { kStatusWord = 0, kChunkCountWord = 1 };
+
+// Everything a prefill launch needs; passed by value to the kernels.
+struct PrefillParams {
+    const void *q, *k, *v;        // [T_total, HK, Dk], [T_total, HV, Dv]
+    const float *g, *beta;        // [T_total, HV]
+    const float *s0;              // [N, HV, Dk, Dv] or null
+    void *out;                    // [T_total, HV, Dv]
+    float *s_final;               // [N, HV, Dk, Dv]
+    float *states;                // [T_total, HV, Dk, Dv] or null
+    const int32_t *cu_seqlens;    // [N+1] or null (equal lengths T_seq)
+    int N, T_seq;
+    int64_t T_total;
+    int HK, HV, Dk, Dv;
+    float scale;
+    int l2norm;
+    int max_chunks;               // grid bound on chunks
+    int32_t *status;              // workspace status words
+    int32_t *chunk_seq;           // [max_chunks] sequence of chunk (packed batches)
+    int32_t *chunk_first;         // [N + 1] first chunk of each sequence (packed batches)
+    float *rec;                   // per (chunk, value head) records of the prep pass
+    size_t rec_floats;            // floats per record
+};
+
+// Record of one (chunk, value head) written by the prep pass (all float32):
+//   W    [C][Dk]  = T diag(beta * gamma * rk) K       (rows t >= len are zero)
+//   Ut   [C][Dv]  = T diag(beta) V
+//   P    [C][C]   = e^{G_t - G_j} rq_t rk_j (q_t . k_j) for j <= t, else 0
+//   qd   [C]      = rq_t * gamma_t            kd [C] = rk_t e^{G_last - G_t}
+//   rk   [C]      = key normaliser            alpha [C] = e^{g_t}
+//   misc [C]      = { gamma_last, ... }
+inline size_t record_floats(int Dk, int Dv) {
+    return (size_t)kChunk * (Dk + Dv + kChunk) + 5 * kChunk;
+}
+
+size_t prefill_workspace_bytes(int64_t T_total, int n_seqs, int HV, int Dk, int Dv);
+int max_chunks_for(int64_t T_total, int n_seqs, bool packed, int T_seq);
+
+// Launchers (return cudaError_t of the launches).
+cudaError_t launch_prefill_generic(const PrefillParams &p, gdn_dtype dtype, cudaStream_t st);
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float *state, void *out, int B, int HK, int HV,
+                          int Dk, int Dv, gdn_dtype dtype, float scale, int l2norm,
+                          cudaStream_t st);
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace gdn

@@ -1,0 +1,193 @@
+/*
+ * gdn.h -- C ABI of the gated delta rule kernels (sm_103a).
+ *
+ * The gated delta rule is the recurrence inside the Gated DeltaNet mixer of
+ * the Qwen3.5 and Qwen3-Next hybrid models (qwen3_5_text page, Notes -> "The
+ * DeltaNet mixer"; qwen3_next page, Notes -> "The DeltaNet mixer fuses its
+ * projections per key head").  Per value head h it keeps a state S of shape
+ * [key_dim][value_dim] and, for every token t,
+ *
+ *     q~ = l2norm(q_t) * scale      k^ = l2norm(k_t)    (scale = key_dim^-1/2)
+ *     S  <- exp(g_t) * S
+ *     u   = beta_t * (v_t - S^T k^)
+ *     S  <- S + k^ u^T
+ *     o_t = S^T q~
+ *
+ * Value head h reads key head h / (HV / HK): queries and keys are
+ * repeat_interleave'd up to the value heads, heads 2j and 2j+1 being copies of
+ * key head j on a 2:1 model (same passages).  l2norm(x) = x / sqrt(sum x^2 +
+ * 1e-6) (the pages give no epsilon; this is the reading taken).
+ *
+ * Argument names follow the pages' linear_attn value table (qwen3_5_text page,
+ * "02 . support() -> Values, by host"): queries, keys, values, decays, beta,
+ * initial state ("state_input ... or None at the start of a prompt (a copy of
+ * the cache's buffer)"), outputs ("attention_head_outputs") and the final
+ * state ("state_output"), with the layouts given there:
+ *
+ *     queries, keys  [batch, seq, key_heads,   key_dim]    (LinearQK)
+ *     values, out    [batch, seq, value_heads, value_dim]  (LinearV)
+ *     decays, beta   [batch, seq, value_heads]             (Gates, float32)
+ *     state          [batch, value_heads, key_dim, value_dim]  float32
+ *     states         [batch, seq, value_heads, key_dim, value_dim]  float32
+ *
+ * All tensors are dense, row-major (last index fastest) and on the device.
+ * decays are natural-log decays (exp(g) of the state is kept), finite and
+ * <= 0 (qwen3_next page: "float32, at most 0"); they are not validated.
+ *
+ * Conventions of every entry point:
+ *   - Every pointer argument that names a tensor is a DEVICE pointer of the
+ *     current CUDA device, 16-byte aligned.  The caller owns every buffer; the
+ *     library allocates no device memory and keeps no state between calls.
+ *   - Work is enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously; the call returns after enqueueing.
+ *   - A negative return is an error detected before anything was enqueued
+ *     (bad arguments), except GDN_ERR_CUDA, which reports a failed launch.
+ *     Errors found in device data (a malformed cu_seqlens) are written to the
+ *     status word at the start of the workspace; read it with
+ *     gdn_workspace_status().  No entry point traps or aborts.
+ *   - Supported shapes: key_dim = value_dim in {32, 64, 128} (every model on
+ *     the pages has 128 x 128 heads); value_heads a multiple of key_heads;
+ *     dtype GDN_BF16 or GDN_F32 for queries, keys, values and out (decays,
+ *     beta and states are always float32).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = -1,   /* null pointer, negative size, HV % HK != 0, ... */
+    GDN_ERR_UNSUPPORTED = -2,   /* key_dim / value_dim / dtype not supported       */
+    GDN_ERR_MISALIGNED = -3,    /* a tensor pointer is not 16-byte aligned         */
+    GDN_ERR_WORKSPACE = -4,     /* workspace NULL or smaller than required         */
+    GDN_ERR_CUDA = -5,          /* a CUDA launch or runtime call failed            */
+    GDN_ERR_TIMEOUT = -6,       /* a bounded device-side wait gave up (status word) */
+    GDN_ERR_BAD_SEQLENS = -7    /* cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T     */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
+
+/*
+ * Chunked prefill over a batch of equal-length sequences ("a prompt's chunked
+ * one", linear_attn value table).  Runs the rule over every (batch row, value
+ * head) from `initial_state` (NULL = zeros, the start of a prompt) and writes
+ * the per-token outputs, the final state and, if `states` is not NULL, the
+ * state after every token (the pages' `states`, num_v_heads x key_dim x
+ * value_dim float32 per token; qwen3_5_text page, Notes -> "Loading").
+ *
+ *   queries, keys   [B, T, HK, Dk]   dtype
+ *   values          [B, T, HV, Dv]   dtype
+ *   decays, beta    [B, T, HV]       float32
+ *   initial_state   [B, HV, Dk, Dv]  float32 or NULL
+ *   out             [B, T, HV, Dv]   dtype
+ *   final_state     [B, HV, Dk, Dv]  float32; may equal initial_state (the
+ *                                    cache continued in place); other overlap
+ *                                    is not allowed
+ *   states          [B, T, HV, Dk, Dv] float32 or NULL
+ *   scale           multiplier of the normalised queries; <= 0 -> Dk^-1/2
+ *   use_qk_l2norm   1: l2-normalise queries and keys in the kernel (the
+ *                   model's convention); 0: use them as given
+ *   workspace       device scratch of gdn_prefill_workspace_size(B*T, B, HV,
+ *                   Dk, Dv) bytes, 256-byte aligned; owned by the caller; it
+ *                   must not be used by another call still running.
+ * B == 0 or T == 0 is allowed: the final state is then the initial state.
+ */
+int gdn_prefill(const void *queries, const void *keys, const void *values,
+                const float *decays, const float *beta, const float *initial_state,
+                void *out, float *final_state, float *states,
+                int B, int T, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                float scale, int use_qk_l2norm,
+                void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * Chunked prefill over N sequences packed back to back (batch 1, T_total
+ * tokens), sequence i owning tokens [cu_seqlens[i], cu_seqlens[i+1]) -- the
+ * cu_seqlens packing convention the pages use for per-image attention
+ * (qwen3_5_text page, vision notes).  Chunks restart at every sequence start,
+ * so the result equals N separate prefills.  Zero-length sequences are
+ * allowed (their final state is their initial state).
+ *
+ *   queries, keys   [T_total, HK, Dk]    values, out  [T_total, HV, Dv]
+ *   decays, beta    [T_total, HV]
+ *   cu_seqlens      device int32 [N + 1]; must satisfy 0 = c0 <= ... <= cN =
+ *                   T_total, checked on the device: a violation sets
+ *                   GDN_ERR_BAD_SEQLENS in the workspace status word and the
+ *                   kernels then write nothing
+ *   initial_state   [N, HV, Dk, Dv] or NULL      final_state [N, HV, Dk, Dv]
+ *   states          [T_total, HV, Dk, Dv] or NULL
+ *   workspace       gdn_prefill_workspace_size(T_total, N, HV, Dk, Dv) bytes
+ */
+int gdn_prefill_varlen(const void *queries, const void *keys, const void *values,
+                       const float *decays, const float *beta, const float *initial_state,
+                       void *out, float *final_state, float *states,
+                       const int32_t *cu_seqlens, int N, int T_total,
+                       int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                       float scale, int use_qk_l2norm,
+                       void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/*
+ * One decode step ("a decode step's recurrent one", linear_attn value
+ * table): one token per sequence, continuing the cache's state in place.
+ *
+ *   queries, keys   [B, HK, Dk]      dtype
+ *   values          [B, HV, Dv]      dtype
+ *   decays, beta    [B, HV]          float32
+ *   state           [B, HV, Dk, Dv]  float32, read and overwritten in place
+ *   out             [B, HV, Dv]      dtype
+ * Needs no workspace.  B == 0 is allowed (nothing is done).
+ */
+int gdn_decode_step(const void *queries, const void *keys, const void *values,
+                    const float *decays, const float *beta,
+                    float *state, void *out,
+                    int B, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                    float scale, int use_qk_l2norm, void *cuda_stream);
+
+/*
+ * Layout of the recurrent state buffer [batch, value_heads, key_dim,
+ * value_dim] float32, row = key index, column = value index (the pages'
+ * State layout).  The kernels use this layout internally too, so a cache
+ * buffer of this layout is passed to them as is.  Host-only; never fails
+ * for positive sizes.
+ */
+typedef struct {
+    size_t bytes;          /* total bytes for `batch` states                    */
+    size_t bytes_per_head; /* key_dim * value_dim * 4                           */
+    int64_t stride[4];     /* element strides of [batch, head, key, value]      */
+    int64_t shape[4];
+    int alignment;         /* required pointer alignment in bytes (16)          */
+} gdn_state_layout_t;
+
+int gdn_state_layout(int batch, int HV, int Dk, int Dv, gdn_state_layout_t *layout);
+
+/*
+ * Bytes of device workspace gdn_prefill / gdn_prefill_varlen need for
+ * `T_total` tokens in `n_seqs` sequences (B for gdn_prefill).  Host-only.
+ * Returns 0 for invalid sizes.
+ */
+size_t gdn_prefill_workspace_size(int64_t T_total, int n_seqs, int HV, int Dk, int Dv);
+
+/*
+ * Read the device status word a prefill wrote into `workspace`: GDN_OK, or
+ * the GDN_ERR_* code of an error found in device data.  Enqueues a 4-byte
+ * copy on `cuda_stream` and waits for that stream.  Returns GDN_OK or
+ * GDN_ERR_CUDA / GDN_ERR_INVALID_ARG for the read itself.
+ */
+int gdn_workspace_status(const void *workspace, void *cuda_stream, int *status);
+
+/* Static description of a status code (never NULL). */
+const char *gdn_status_string(int status);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

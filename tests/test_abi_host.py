@@ -1,0 +1,142 @@
+"""Host-side tests of the C ABI (include/gdn.h): no GPU needed.
+
+The library must load, export every function the header declares, and reject
+bad arguments on the host before touching the device (the pointers passed
+here are never dereferenced: each call fails its checks first).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_mixer_delta_gb300 import build as b
+    import gated_deltanet_mixer_delta_gb300 as gdn
+    b.build()
+    return gdn.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ["gdn_prefill", "gdn_prefill_varlen", "gdn_decode_step", "gdn_state_layout",
+              "gdn_prefill_workspace_size", "gdn_workspace_status", "gdn_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from gated_deltanet_mixer_delta_gb300 import library_path
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(gdn_\w+)", out))
+    for n in header_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_state_layout(lib):
+    import gated_deltanet_mixer_delta_gb300 as gdn
+    lay = gdn.state_layout(256, 32, 128, 128)
+    assert lay["shape"] == (256, 32, 128, 128)
+    assert lay["stride"] == (32 * 128 * 128, 128 * 128, 128, 1)
+    assert lay["bytes"] == 256 * 32 * 128 * 128 * 4 == 512 * 2 ** 20
+    assert lay["bytes_per_head"] == 65536
+    assert lay["alignment"] == 16
+    with pytest.raises(gdn.GdnError):
+        gdn.state_layout(1, 0, 128, 128)
+
+
+def test_state_bytes_per_token_match_the_pages(lib):
+    """tests/golden/state_bytes_per_token.txt: the pages give the float32 per-token
+    state size (num_v_heads x 128 x 128) of each model: 1, 2 or 3 MiB per block."""
+    import gated_deltanet_mixer_delta_gb300 as gdn
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "state_bytes_per_token.txt"))
+            if l.strip() and not l.startswith("#")]
+    assert len(rows) == 6
+    for model, hv, dk, dv, mib in rows:
+        lay = gdn.state_layout(1, int(hv), int(dk), int(dv))
+        assert lay["bytes"] == int(mib) * 2 ** 20, model
+
+
+def test_workspace_size(lib):
+    import gated_deltanet_mixer_delta_gb300 as gdn
+    a = gdn.workspace_size(4096, 1, 32, 128, 128)
+    b = gdn.workspace_size(8192, 1, 32, 128, 128)
+    assert 0 < a < b
+    assert gdn.workspace_size(0, 0, 32, 128, 128) > 0
+    assert gdn.workspace_size(10, 1, 32, 96, 96) == 0
+    assert gdn.workspace_size(-1, 1, 32, 128, 128) == 0
+
+
+def test_status_strings(lib):
+    for s in [0, -1, -2, -3, -4, -5, -6, -7, 12345]:
+        assert lib.gdn_status_string(s)
+    assert lib.gdn_abi_version() >= 100
+
+
+P = 0x10000          # fake, 16-byte aligned device address: never dereferenced
+BIG = 1 << 40
+
+
+def _prefill(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, b=P, s0=None, out=P, fin=P, st=None, B=1, T=64, HK=2, HV=4,
+             Dk=128, Dv=128, dtype=0, scale=0.0, l2=1, ws=P, wsb=BIG, stream=None)
+    a.update(kw)
+    return lib.gdn_prefill(a["q"], a["k"], a["v"], a["g"], a["b"], a["s0"], a["out"], a["fin"],
+                           a["st"], a["B"], a["T"], a["HK"], a["HV"], a["Dk"], a["Dv"],
+                           a["dtype"], a["scale"], a["l2"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(HV=3), -1), (dict(HK=0), -1), (dict(B=-1), -1), (dict(T=-5), -1),
+    (dict(Dk=96, Dv=96), -2), (dict(Dk=128, Dv=64), -2), (dict(dtype=7), -2),
+    (dict(q=P + 4), -3), (dict(out=P + 8), -3), (dict(st=P + 2), -3),
+    (dict(ws=None), -4), (dict(wsb=100), -4), (dict(ws=P + 16), -3),
+    (dict(q=None), -1), (dict(fin=None), -1), (dict(scale=float("nan")), -1),
+])
+def test_prefill_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _prefill(lib, **kw) == code
+
+
+def test_varlen_rejects_bad_arguments_on_host(lib):
+    f = lib.gdn_prefill_varlen
+    args = [P, P, P, P, P, None, P, P, None, P, 2, 100, 2, 4, 128, 128, 0, 0.0, 1, P, BIG, None]
+    a = list(args); a[9] = None
+    assert f(*a) == -1                           # cu_seqlens required
+    a = list(args); a[10] = -1
+    assert f(*a) == -1
+    a = list(args); a[9] = P + 4
+    assert f(*a) == -3
+    a = list(args); a[20] = 10
+    assert f(*a) == -4
+
+
+def _decode(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, b=P, s=P, out=P, B=4, HK=2, HV=4, Dk=128, Dv=128, dtype=0,
+             scale=0.0, l2=1, stream=None)
+    a.update(kw)
+    return lib.gdn_decode_step(a["q"], a["k"], a["v"], a["g"], a["b"], a["s"], a["out"], a["B"],
+                               a["HK"], a["HV"], a["Dk"], a["Dv"], a["dtype"], a["scale"],
+                               a["l2"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(HV=5), -1), (dict(B=-2), -1), (dict(Dk=48, Dv=48), -2), (dict(dtype=3), -2),
+    (dict(s=None), -1), (dict(s=P + 4), -3), (dict(v=P + 2), -3), (dict(B=0), 0),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _decode(lib, **kw) == code

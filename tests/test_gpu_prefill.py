@@ -1,0 +1,197 @@
+"""GPU parity of the chunked prefill (gdn_prefill, gdn_prefill_varlen) against the
+fp64 oracle, on small seeded cases that span several chunks and ragged tails, plus
+the invariants the CUDA path must keep exactly."""
+import pytest
+import torch
+
+import workloads
+from parity import assert_out_close, assert_states_close, oracle_chains
+
+pytestmark = pytest.mark.gpu
+import oracle  # noqa: E402  (test infrastructure)
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_deltanet_mixer_delta_gb300 as m
+    m.build.build()
+    m.load_library()
+    return m
+
+
+def _inputs(B, T, HK, HV, D, dtype, seed, s0=False, g_mode="std"):
+    d = workloads.draw_inputs(B, T, HK, HV, D, D, dtype, seed,
+                              init_state_std=0.02 if s0 else None)
+    if g_mode == "weak":
+        d["decays"] = d["decays"] * 0.01
+    elif g_mode == "zero":
+        d["decays"] = torch.zeros_like(d["decays"])
+    elif g_mode == "forget":
+        d["decays"] = torch.full_like(d["decays"], -1e4)
+    return d
+
+
+def _cuda(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def _check_vs_oracle(gdn, d, states=False):
+    g = _cuda(d)
+    out, fin, st = gdn.prefill(g["queries"], g["keys"], g["values"], g["decays"], g["beta"],
+                               g["initial_state"], output_states=states)
+    torch.cuda.synchronize()
+    o_ref, f_ref, s_ref = oracle.forward(d["queries"], d["keys"], d["values"], d["decays"],
+                                         d["beta"], d["initial_state"], want_states=states)
+    dt = d["queries"].dtype
+    assert_out_close(out, o_ref, dt)
+    assert_states_close(fin, f_ref, "final_state")
+    if states:
+        B, T, HV = st.shape[:3]
+        assert_states_close(st, s_ref, "states")
+        if T:
+            assert torch.equal(st[:, -1], fin)
+    return out, fin, st
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 200])
+@pytest.mark.parametrize("D,dtype", [(128, torch.bfloat16), (32, torch.float32),
+                                     (64, torch.bfloat16)])
+def test_prefill_ragged_lengths(gdn, T, D, dtype):
+    d = _inputs(2, T, 2, 4, D, dtype, seed=100 + T + D, s0=(T % 2 == 1))
+    _check_vs_oracle(gdn, d)
+
+
+@pytest.mark.parametrize("g_mode", ["std", "weak", "zero", "forget"])
+def test_prefill_decay_regimes(gdn, g_mode):
+    d = _inputs(1, 197, 2, 4, 128, torch.bfloat16, seed=7, s0=True, g_mode=g_mode)
+    _check_vs_oracle(gdn, d)
+
+
+@pytest.mark.parametrize("D,dtype", [(128, torch.bfloat16), (32, torch.float32)])
+def test_prefill_per_token_states(gdn, D, dtype):
+    d = _inputs(2, 150, 1, 2, D, dtype, seed=11, s0=True, g_mode="weak")
+    _check_vs_oracle(gdn, d, states=True)
+
+
+def test_prefill_zero_length_returns_initial_state(gdn):
+    d = _cuda(_inputs(2, 0, 2, 4, 128, torch.bfloat16, seed=3, s0=True))
+    out, fin, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                              d["initial_state"])
+    assert out.numel() == 0
+    assert torch.equal(fin, d["initial_state"])
+    out, fin, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"])
+    assert torch.count_nonzero(fin) == 0
+
+
+def test_prefill_in_place_cache(gdn):
+    """final_state may be the initial_state buffer (the cache continued in place)."""
+    d = _cuda(_inputs(1, 100, 2, 4, 128, torch.bfloat16, seed=4, s0=True))
+    ref_out, ref_fin, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"],
+                                      d["beta"], d["initial_state"].clone())
+    cache = d["initial_state"].clone()
+    out, fin, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                              cache, final_state=cache)
+    assert fin.data_ptr() == cache.data_ptr()
+    assert torch.equal(out, ref_out) and torch.equal(cache, ref_fin)
+
+
+def test_gqa_equals_repeated_heads_exactly(gdn):
+    """Value head h reads key head h // (HV/HK): HK=2/HV=4 is bitwise the same as HK=HV=4
+    with queries and keys repeat_interleave'd."""
+    d = _cuda(_inputs(2, 130, 2, 4, 128, torch.bfloat16, seed=5, s0=True))
+    o1, f1, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                            d["initial_state"])
+    q2 = d["queries"].repeat_interleave(2, dim=2).contiguous()
+    k2 = d["keys"].repeat_interleave(2, dim=2).contiguous()
+    o2, f2, _ = gdn.prefill(q2, k2, d["values"], d["decays"], d["beta"], d["initial_state"])
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_varlen_matches_oracle_and_separate_runs(gdn):
+    lens = [5, 0, 64, 130, 1, 77]
+    T = sum(lens)
+    d = workloads.draw_inputs(1, T, 2, 4, 128, 128, torch.bfloat16, 21, init_state_std=0.02,
+                              n_states=len(lens))
+    cu = torch.tensor([0] + torch.tensor(lens).cumsum(0).tolist(), dtype=torch.int32)
+    g = _cuda(d)
+    out, fin, st = gdn.prefill_varlen(g["queries"], g["keys"], g["values"], g["decays"], g["beta"],
+                                      cu.cuda(), g["initial_state"], output_states=True)
+    torch.cuda.synchronize()
+    o_ref, f_ref, s_ref = oracle.forward(d["queries"], d["keys"], d["values"], d["decays"],
+                                         d["beta"], d["initial_state"], cu_seqlens=cu,
+                                         want_states=True)
+    assert_out_close(out, o_ref, torch.bfloat16)
+    assert_states_close(fin, f_ref)
+    assert_states_close(st, s_ref, "states")
+    # bitwise equal to one prefill per sequence
+    for i, L in enumerate(lens):
+        a, b = int(cu[i]), int(cu[i + 1])
+        sl = lambda t: t[:, a:b].contiguous()
+        oi, fi, sti = gdn.prefill(sl(g["queries"]), sl(g["keys"]), sl(g["values"]),
+                                  sl(g["decays"]), sl(g["beta"]),
+                                  g["initial_state"][i:i + 1].contiguous(), output_states=True)
+        assert torch.equal(oi, out[:, a:b]) and torch.equal(fi[0], fin[i])
+        assert torch.equal(sti, st[:, a:b])
+
+
+def test_varlen_bad_cu_seqlens_sets_status_and_writes_nothing(gdn):
+    lens = [10, 20, 30]
+    T = sum(lens)
+    d = _cuda(workloads.draw_inputs(1, T, 2, 4, 128, 128, torch.bfloat16, 22))
+    for bad in ([0, 30, 20, 60], [0, 10, 30, 59], [1, 10, 30, 60]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        out = torch.full_like(d["values"], 7.0)
+        fin = torch.full((3, 4, 128, 128), 7.0, device="cuda")
+        ws = torch.empty(gdn.workspace_size(T, 3, 4, 128, 128), dtype=torch.uint8, device="cuda")
+        gdn.prefill_varlen(d["queries"], d["keys"], d["values"], d["decays"], d["beta"], cu,
+                           out=out, final_state=fin, workspace=ws)
+        assert gdn.workspace_status(ws) == -7
+        assert torch.all(out == 7.0) and torch.all(fin == 7.0)
+    cu = torch.tensor([0, 10, 30, 60], dtype=torch.int32, device="cuda")
+    gdn.prefill_varlen(d["queries"], d["keys"], d["values"], d["decays"], d["beta"], cu,
+                       workspace=ws)
+    assert gdn.workspace_status(ws) == 0
+
+
+def test_prefill_then_decode_continues_the_state(gdn):
+    """prefill(t) then T-t decode steps gives the same outputs and state as prefill(T)."""
+    d = _cuda(_inputs(3, 96, 2, 4, 128, torch.bfloat16, seed=8, s0=True, g_mode="weak"))
+    o_full, f_full, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                                    d["initial_state"])
+    t = 70
+    sl = lambda x: x[:, :t].contiguous()
+    _, cache, _ = gdn.prefill(sl(d["queries"]), sl(d["keys"]), sl(d["values"]), sl(d["decays"]),
+                              sl(d["beta"]), d["initial_state"])
+    for i in range(t, 96):
+        o_i = gdn.decode_step(d["queries"][:, i].contiguous(), d["keys"][:, i].contiguous(),
+                              d["values"][:, i].contiguous(), d["decays"][:, i].contiguous(),
+                              d["beta"][:, i].contiguous(), cache)
+        assert_out_close(o_i, o_full[:, i], torch.bfloat16, f"decode step {i}")
+    assert_states_close(cache, f_full.cpu().double().numpy())
+
+
+def test_unnormalised_path_and_sensitivity(gdn):
+    """use_qk_l2norm=0 matches the oracle without the norm, and differs from the
+    normalised result (the pages report a 42% state error without it)."""
+    d = _inputs(1, 80, 2, 2, 32, torch.float32, seed=9)
+    d["queries"] = d["queries"] * 0.1
+    d["keys"] = d["keys"] * 0.1
+    g = _cuda(d)
+    out, fin, _ = gdn.prefill(g["queries"], g["keys"], g["values"], g["decays"], g["beta"],
+                              use_qk_l2norm=False)
+    o_ref, f_ref, _ = oracle.forward(d["queries"], d["keys"], d["values"], d["decays"],
+                                     d["beta"], use_qk_l2norm=False)
+    assert_out_close(out, o_ref, torch.float32)
+    assert_states_close(fin, f_ref)
+    _, f_norm, _ = oracle.forward(d["queries"], d["keys"], d["values"], d["decays"], d["beta"])
+    with pytest.raises(AssertionError):
+        assert_states_close(fin, f_norm)
+
+
+def test_tiny_workload(gdn):
+    """T=64, 2 heads, d=32, fp32, pre-normalised q and k, zero initial state."""
+    w = workloads.WORKLOADS["tiny_T64_H2_d32_f32"]
+    d = workloads.workload_inputs(w)
+    _check_vs_oracle(gdn, d)
