@@ -216,8 +216,8 @@ def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_stat
         raise ValueError("cu_seqlens needs at least one entry")
     _need(keys, "keys", dt, dev, queries.shape)
     _need(values, "values", dt, dev)
-    _need(decays, "decays", torch.float32, dev, lead)
-    _need(beta, "beta", torch.float32, dev, lead)
+    _need(decays, "decays", torch.float32, dev, (*lead, HV))
+    _need(beta, "beta", torch.float32, dev, (*lead, HV))
     if initial_state is not None:
         _need(initial_state, "initial_state", torch.float32, dev, (N, HV, Dk, Dv))
     if out is None:
