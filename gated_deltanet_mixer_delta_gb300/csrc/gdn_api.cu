@@ -98,7 +98,8 @@ int prefill_common(const void *queries, const void *keys, const void *values,
             return GDN_ERR_CUDA;
         return GDN_OK;
     }
-    cudaError_t e = launch_prefill_generic(p, dtype, st);
+    cudaError_t e = tc_supported(Dk, Dv, dtype) ? launch_prefill_tc(p, st)
+                                                : launch_prefill_generic(p, dtype, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -55,6 +55,11 @@ int max_chunks_for(int64_t T_total, int n_seqs, bool packed, int T_seq);
 
 // Launchers (return cudaError_t of the launches).
 cudaError_t launch_prefill_generic(const PrefillParams &p, gdn_dtype dtype, cudaStream_t st);
+cudaError_t launch_chunk_table(const PrefillParams &p, cudaStream_t st);
+// Tensor-core path (key_dim = value_dim = 128, bf16): prep + chain kernels.
+bool tc_supported(int Dk, int Dv, gdn_dtype dtype);
+size_t tc_record_bytes();
+cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st);
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int B, int HK, int HV,
                           int Dk, int Dv, gdn_dtype dtype, float scale, int l2norm,

@@ -495,6 +495,11 @@ cudaError_t dispatch(const PrefillParams &p, cudaStream_t st) {
 
 }  // namespace
 
+cudaError_t launch_chunk_table(const PrefillParams &p, cudaStream_t st) {
+    chunk_table_kernel<<<1, 1024, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_generic(const PrefillParams &p, gdn_dtype dtype, cudaStream_t st) {
     return dtype == GDN_BF16 ? dispatch<__nv_bfloat16>(p, st) : dispatch<float>(p, st);
 }
