@@ -97,30 +97,17 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bflo
     hi = __float2bfloat16_rn(x);
     lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
+// the same for two values at once, packed (a in the low half): one conversion per word
+__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
 
 __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
-}
-
-// Write one 64-element fp32 row (scaled elementwise by f[]) as hi and lo bf16 rows of
-// two K-major 128B-swizzled operand images ([rows][64 elements]).
-__device__ __forceinline__ void store_row_hilo(uint8_t *img_hi, uint8_t *img_lo, int row,
-                                               const float (&x)[64]) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            __nv_bfloat16 h0, l0, h1, l1;
-            split_bf16(x[q * 8 + 2 * e], h0, l0);
-            split_bf16(x[q * 8 + 2 * e + 1], h1, l1);
-            h[e] = pack2(h0, h1);
-            l[e] = pack2(l0, l1);
-        }
-        const uint32_t off = sw128_offset(row, q * 16);
-        *reinterpret_cast<uint4 *>(img_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(img_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
 }
 
 // ================================================================== prep kernel
@@ -314,8 +301,10 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
 
 // ================================================================== chain kernel
 constexpr int kChainThreads = 384;
+// stage: key tile | query tile | value slice | the record's per-token factor rows
+constexpr int kStageK = 0, kStageQ = 16384, kStageV = 32768, kStageF = 36864;
+constexpr int kStageBytes = 38912;
 // shared memory map (bytes from a 1024-aligned base)
-constexpr int kStageBytes = 16384 + 16384 + 4096;          // K | Q | V slice
 constexpr int OFF_STAGE = 0;                               // [2]
 constexpr int OFF_W = OFF_STAGE + 2 * kStageBytes;         // -W hi | lo   [2][64][128B] each
 constexpr int OFF_P = OFF_W + 2 * 16384;                   // P hi | lo    [64][128B] each
@@ -326,23 +315,56 @@ constexpr int OFF_S = OFF_VT + 4096;                       // S hi | lo   [2][32
 constexpr int OFF_Z = OFF_S + 2 * 8192;                    // Z hi | lo   [32][128B]
 constexpr int OFF_U = OFF_Z + 2 * 4096;                    // U hi | lo
 constexpr int OFF_UF = OFF_U + 2 * 4096;                   // U fp32 [64][32] (states)
-constexpr int OFF_SC = OFF_UF + C * NV * 4;                // factors [2][16][64] fp32
-constexpr int OFF_BAR = OFF_SC + 2 * 16 * C * 4;
+constexpr int OFF_RQ = OFF_UF + C * NV * 4;                // query normalisers [2][64] (pre)
+constexpr int OFF_BAR = OFF_RQ + 2 * C * 4;
 constexpr int kChainSmem = OFF_BAR + 256 + 1024;
-// factor rows in smem (beyond the 8 record rows)
-enum { SCX_RQ = 8, SCX_QD = 9 };
+constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM columns
-constexpr uint32_t TM_QK = 0, TM_W = 64, TM_U0 = 128, TM_QS = 192, TM_S = 224, TM_O = 256;
+constexpr uint32_t TM_QK = 0, TM_W = 64, TM_U0 = 128, TM_QS = 192, TM_S = 224, TM_O = 256,
+                   TM_U2 = 288, TM_QK1 = 320;
+// D_QK is double-buffered: chunk cc uses TM_QK (cc even) or TM_QK1 (cc odd)
+__device__ __forceinline__ uint32_t tm_qk(int st) { return st ? TM_QK1 : TM_QK; }
 constexpr uint32_t kTmemCols = 512;
 
 // barriers
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_PRE_MMA, B_PRE_U, B_PRE_DONE, B_S_READY,
-    B_D1, B_E1, B_D2, B_DO, B_DRAIN, B_DRAIN2, B_COUNT
+    B_D1, B_D1Q, B_E1, B_D2, B_DO, B_TIMG, B_DRAIN, B_DRAIN2, B_DRAIN3, B_COUNT
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
+
+// 32 consecutive elements of a row (chunks c0 .. c0+3 of 16 bytes) of two K-major,
+// 128B-swizzled bf16 operand images: hi and lo parts of x.
+__device__ __forceinline__ void store_half_row_hilo(uint8_t *img_hi, uint8_t *img_lo, int row,
+                                                    int c0, const float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2_bf16(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1], h[e], l[e]);
+        const uint32_t off = sw128_offset(row, (c0 + q) * 16);
+        *reinterpret_cast<uint4 *>(img_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(img_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// sum of squares of 64 bf16 (8 swizzled 16-byte chunks: chunk order does not matter)
+__device__ __forceinline__ float sumsq_row64(const uint8_t *row128) {
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(row128 + q * 16);
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(b2[e]);
+            ss += f.x * f.x + f.y * f.y;
+        }
+    }
+    return ss;
+}
 
 template <bool STATES>
 __global__ void __launch_bounds__(kChainThreads, 1)
@@ -359,8 +381,12 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     SeqRange sr;
     if (!seq_range(p, s, sr)) return;
+    if (!p.cu_seqlens && vs == 0 && h == 0 && s == 0 && tid == 0) p.status[kStatusWord] = GDN_OK;
     const int j = h / (p.HV / p.HK);
     const int nch = sr.count;
+    auto rec_of = [&](int cc) -> const float * {
+        return p.rec + ((size_t)(sr.first + cc) * p.HV + h) * kRecFloats;
+    };
 
     if (tid == 0) {
         mbar_init(&bars[B_FULL0], 1);
@@ -372,11 +398,14 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         mbar_init(&bars[B_PRE_DONE], 128);
         mbar_init(&bars[B_S_READY], 128);
         mbar_init(&bars[B_D1], 1);
+        mbar_init(&bars[B_D1Q], 1);
         mbar_init(&bars[B_E1], 128);
         mbar_init(&bars[B_D2], 1);
         mbar_init(&bars[B_DO], 1);
         mbar_init(&bars[B_DRAIN], 1);
         mbar_init(&bars[B_DRAIN2], 1);
+        mbar_init(&bars[B_DRAIN3], 1);
+        mbar_init(&bars[B_TIMG], 128);
         *s_err = 0;
         fence_mbar_init();
         if (nch > 0) {
@@ -415,12 +444,14 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 if (u >= 1 && !wait(B_EMPTY0 + st, (u - 1) & 1)) break;
                 uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
                 const int tok = (int)(sr.t0 + (int64_t)cc * C);
-                mbar_arrive_expect_tx(&bars[B_FULL0 + st], kStageBytes);
-                tma_load_3d(stg, &mapK, &bars[B_FULL0 + st], 0, j, tok);
-                tma_load_3d(stg + 8192, &mapK, &bars[B_FULL0 + st], 64, j, tok);
-                tma_load_3d(stg + 16384, &mapQ, &bars[B_FULL0 + st], 0, j, tok);
-                tma_load_3d(stg + 24576, &mapQ, &bars[B_FULL0 + st], 64, j, tok);
-                tma_load_3d(stg + 32768, &mapV, &bars[B_FULL0 + st], vs * NV, h, tok);
+                uint64_t *fb = &bars[B_FULL0 + st];
+                mbar_arrive_expect_tx(fb, kStageBytes);
+                tma_load_3d(stg + kStageK, &mapK, fb, 0, j, tok);
+                tma_load_3d(stg + kStageK + 8192, &mapK, fb, 64, j, tok);
+                tma_load_3d(stg + kStageQ, &mapQ, fb, 0, j, tok);
+                tma_load_3d(stg + kStageQ + 8192, &mapQ, fb, 64, j, tok);
+                tma_load_3d(stg + kStageV, &mapV, fb, vs * NV, h, tok);
+                bulk_load(stg + kStageF, rec_of(cc) + C * C, 8 * C * 4, fb);
             }
         }
     } else if (warp == 1) {
@@ -436,21 +467,17 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     !wait(B_S_READY, cc & 1))
                     break;
                 tc_fence_after();
-                // MMA1: D_U += (-W) S  (3 hi/lo terms);  D_QS = Q S  (2 terms)
+                // MMA1: D_U += (-W_hi) S_hi + (-W_hi) S_lo on top of Ut = T'' V; the third
+                // term (-W_lo) S_hi goes to D_U2 from the second issuer
                 const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
                     const int kb = ks >> 2, ko = (ks & 3) * 32;
                     const uint32_t wh = smem_u32(sm + OFF_W + kb * 8192 + ko);
-                    const uint32_t wl = wh + 16384;
                     const uint32_t sh = smem_u32(sm + OFF_S + kb * 4096 + ko);
                     const uint32_t sl = sh + 8192;
-                    const uint32_t qa = smem_u32(stg + 16384 + kb * 8192 + ko);
                     mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, 1);
                     mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sl, 16, 1024, kSwizzle128B), id_64x32, 1);
-                    mma_bf16(dU, smem_desc(wl, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, 1);
-                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, ks > 0);
-                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sl, 16, 1024, kSwizzle128B), id_64x32, 1);
                 }
                 mma_commit(&bars[B_D1]);
                 issued = true;
@@ -459,7 +486,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 // MMA2: D_S = K^T (Z hi + Z lo)   (A = key tile, MN-major)
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ka = smem_u32(stg + ks * 2048);
+                    const uint32_t ka = smem_u32(stg + kStageK + ks * 2048);
                     const uint32_t zh = smem_u32(sm + OFF_Z + ks * 32);
                     mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh, 16, 1024, kSwizzle128B), id_128x32_amn, ks > 0);
                     mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh + 4096, 16, 1024, kSwizzle128B), id_128x32_amn, 1);
@@ -482,99 +509,76 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 mbar_wait(&bars[B_DRAIN], 0);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ pre warpgroup
-        const int ptid = tid - 128, pw = warp & 3;
-        const bool lead = (ptid == 0);
-        const uint32_t lb = lane_base(warp);
-        const uint32_t id_qk = instr_desc(64, 64, kFmtBF16, 0, 0);
-        const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
-        const uint32_t id_u = instr_desc(64, NV, kFmtBF16, 0, 0);
-        float *scs = reinterpret_cast<float *>(sm + OFF_SC);   // pre-private factors
-        bool leader_issued = false;
-        uint32_t pre_mma_phase = 0, pre_u_phase = 0;
-        for (int cc = 0; cc < nch; ++cc) {
-            const int st = cc & 1, u = cc >> 1;
-            uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-            const float *rec = p.rec + ((size_t)(sr.first + cc) * p.HV + h) * kRecFloats;
-            if (!wg_wait(B_FULL0 + st, u & 1, 1, lead)) break;
-            // factors: c1, c2, G, rk from the record; rq from the query tile (the swizzle
-            // only permutes 16-byte chunks inside a row, so the sum needs no unswizzle)
-            for (int e = ptid; e < 8 * C; e += 128) scs[e] = rec[C * C + e];
-            if (ptid < C) {
-                float ss = 0.f;
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 w4 = *reinterpret_cast<const uint4 *>(stg + 16384 + kb * 8192 + ptid * 128 + q * 16);
-                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(b2[e]);
-                            ss += f.x * f.x + f.y * f.y;
-                        }
-                    }
-                scs[SCX_RQ * C + ptid] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
-            }
-            if (lead) {
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ second MMA issuer
+        // D_QS = Q S (2 hi/lo terms): needs only the staged queries and the state, so it
+        // runs while the first issuer still waits for the pre warpgroup.
+        if (lane == 0) {
+            const uint32_t id_64x32 = instr_desc(64, NV, kFmtBF16, 0, 0);
+            bool issued = false;
+            for (int cc = 0; cc < nch; ++cc) {
+                const int st = cc & 1;
+                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
+                if (!wait(B_FULL0 + st, (cc >> 1) & 1) || !wait(B_S_READY, cc & 1)) break;
                 tc_fence_after();
-                // Q K^T (M = 64, N = 64, K = 128) into D_QK
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
                     const int kb = ks >> 2, ko = (ks & 3) * 32;
-                    const uint32_t qa = smem_u32(stg + 16384 + kb * 8192 + ko);
-                    const uint32_t ka = smem_u32(stg + kb * 8192 + ko);
-                    mma_bf16(tmem + TM_QK, smem_desc(qa, 16, 1024, kSwizzle128B),
+                    const uint32_t sh = smem_u32(sm + OFF_S + kb * 4096 + ko);
+                    const uint32_t qa = smem_u32(stg + kStageQ + kb * 8192 + ko);
+                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, ks > 0);
+                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sh + 8192, 16, 1024, kSwizzle128B), id_64x32, 1);
+                }
+                issued = true;
+                if (!wait(B_PRE_DONE, cc & 1)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int kb = ks >> 2, ko = (ks & 3) * 32;
+                    const uint32_t wl = smem_u32(sm + OFF_W + 16384 + kb * 8192 + ko);
+                    const uint32_t sh = smem_u32(sm + OFF_S + kb * 4096 + ko);
+                    mma_bf16(tmem + TM_U2, smem_desc(wl, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, ks > 0);
+                }
+                mma_commit(&bars[B_D1Q]);
+                // the next chunk's D_QS overwrites this one: the epilogue reads it before
+                // it arrives on s_ready, which the next iteration waits for
+            }
+            if (issued) {
+                mma_commit(&bars[B_DRAIN3]);
+                mbar_wait(&bars[B_DRAIN3], 0);
+            }
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ pre-stage MMA issuer
+        // Q K^T as soon as the tiles land; W^T = K^T T'^T and Ut = T'' V once the pre
+        // warpgroup has written the T', T'' and V^T operands.
+        if (lane == 0) {
+            const uint32_t id_qk = instr_desc(64, 64, kFmtBF16, 0, 0);
+            const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
+            const uint32_t id_u = instr_desc(64, NV, kFmtBF16, 0, 0);
+            bool issued = false;
+            for (int cc = 0; cc < nch; ++cc) {
+                const int st = cc & 1;
+                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
+                if (!wait(B_FULL0 + st, (cc >> 1) & 1)) break;
+                tc_fence_after();
+                // Q K^T (M = 64, N = 64, K = 128) into D_QK[cc % 2]; its previous reader (the
+                // P step of chunk cc - 2) finished before the T-operand handshake of cc - 1
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int kb = ks >> 2, ko = (ks & 3) * 32;
+                    const uint32_t qa = smem_u32(stg + kStageQ + kb * 8192 + ko);
+                    const uint32_t ka = smem_u32(stg + kStageK + kb * 8192 + ko);
+                    mma_bf16(tmem + tm_qk(st), smem_desc(qa, 16, 1024, kSwizzle128B),
                              smem_desc(ka, 16, 1024, kSwizzle128B), id_qk, ks > 0);
                 }
-                leader_issued = true;
-            }
-            named_sync(1, 128);            // factors visible
-            // T' = T diag(c1), T'' = T diag(c2) as hi/lo operands; V^T operand
-            if (ptid < C) {
-                const int t = ptid;
-                float x[64];
-                const float4 *tr = reinterpret_cast<const float4 *>(rec + t * C);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float4 v4 = tr[q];
-                    x[4 * q] = v4.x * scs[SC_C1 * C + 4 * q];
-                    x[4 * q + 1] = v4.y * scs[SC_C1 * C + 4 * q + 1];
-                    x[4 * q + 2] = v4.z * scs[SC_C1 * C + 4 * q + 2];
-                    x[4 * q + 3] = v4.w * scs[SC_C1 * C + 4 * q + 3];
-                }
-                store_row_hilo(sm + OFF_T1, sm + OFF_T1 + 8192, t, x);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float4 v4 = tr[q];
-                    x[4 * q] = v4.x * scs[SC_C2 * C + 4 * q];
-                    x[4 * q + 1] = v4.y * scs[SC_C2 * C + 4 * q + 1];
-                    x[4 * q + 2] = v4.z * scs[SC_C2 * C + 4 * q + 2];
-                    x[4 * q + 3] = v4.w * scs[SC_C2 * C + 4 * q + 3];
-                }
-                store_row_hilo(sm + OFF_T2, sm + OFF_T2 + 8192, t, x);
-            } else {
-                // V^T: [32 value rows][64 tokens] from the staged [64 tokens][32 values]
-                const __nv_bfloat16 *vsrc = reinterpret_cast<const __nv_bfloat16 *>(stg + 32768);
-                for (int e = ptid - 64; e < NV * 8; e += 64) {
-                    const int cv = e >> 3, q = e & 7;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int ee = 0; ee < 4; ++ee)
-                        w[ee] = pack2(vsrc[(q * 8 + 2 * ee) * NV + cv], vsrc[(q * 8 + 2 * ee + 1) * NV + cv]);
-                    *reinterpret_cast<uint4 *>(sm + OFF_VT + sw128_offset(cv, q * 16)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            fence_async_smem();
-            named_sync(1, 128);
-            if (lead) {
+                issued = true;
+                if (!wait(B_TIMG, cc & 1)) break;
                 tc_fence_after();
                 // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens), A MN-major
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ka = smem_u32(stg + ks * 2048);
+                    const uint32_t ka = smem_u32(stg + kStageK + ks * 2048);
                     const uint32_t th = smem_u32(sm + OFF_T1 + ks * 32);
                     mma_bf16(tmem + TM_W, smem_desc(ka, 8192, 1024, kSwizzle128B),
                              smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
@@ -582,13 +586,10 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                              smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
                 }
                 mma_commit(&bars[B_PRE_MMA]);
-            }
-            // the previous chunk's MMA1 must have consumed the -W operand and, through the
-            // s_ready handshake, the epilogue must be done with D_U[cc % 2]
-            if (cc >= 1 && !wg_wait(B_D1, (cc - 1) & 1, 1, lead)) break;
-            if (lead) {
+                // D_U[cc % 2] was last read by the epilogue for chunk cc - 2, which is done
+                // once MMA1 of chunk cc - 1 has run (s_ready handshake)
+                if (cc >= 1 && !wait(B_D1, (cc - 1) & 1)) break;
                 tc_fence_after();
-                // Ut = T'' V into D_U[cc % 2] (M = 64, N = 32, K = 64)
                 const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
@@ -601,61 +602,134 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 }
                 mma_commit(&bars[B_PRE_U]);
             }
-            // W^T from TMEM (lane = key i) -> -W hi/lo into the MMA1 A operand
+            if (issued) {
+                mma_commit(&bars[B_DRAIN2]);
+                mbar_wait(&bars[B_DRAIN2], 0);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ pre warpgroup
+        const int ptid = tid - 128, pw = warp & 3;
+        const bool lead = (ptid == 0);
+        const uint32_t lb = lane_base(warp);
+        const int trow = ptid >> 1, thalf = ptid & 1;       // T row / half handled here
+        float4 tn[8];                                        // T row half, prefetched
+        auto load_t = [&](int cc) {
+            const float4 *src = reinterpret_cast<const float4 *>(rec_of(cc) + trow * C + thalf * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) tn[q] = src[q];
+        };
+        if (nch > 0) load_t(0);
+        uint32_t pre_mma_phase = 0, pre_u_phase = 0;
+        for (int cc = 0; cc < nch; ++cc) {
+            const int st = cc & 1, u = cc >> 1;
+            uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
+            const float *F = reinterpret_cast<const float *>(stg + kStageF);
+            float *rq = reinterpret_cast<float *>(sm + OFF_RQ) + st * C;
+            if (!wg_wait(B_FULL0 + st, u & 1, 1, lead)) break;
+            // query normalisers: two threads per row
+            {
+                float ss = sumsq_row64(stg + kStageQ + thalf * 8192 + trow * 128);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (thalf == 0) rq[trow] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
+            }
+            // T' = T diag(c1), T'' = T diag(c2): hi/lo operand half rows
+            {
+                float x[32];
+                const float *c1 = F + SC_C1 * C + thalf * 32, *c2 = F + SC_C2 * C + thalf * 32;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    x[4 * q] = tn[q].x * c1[4 * q]; x[4 * q + 1] = tn[q].y * c1[4 * q + 1];
+                    x[4 * q + 2] = tn[q].z * c1[4 * q + 2]; x[4 * q + 3] = tn[q].w * c1[4 * q + 3];
+                }
+                store_half_row_hilo(sm + OFF_T1, sm + OFF_T1 + 8192, trow, thalf * 4, x);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    x[4 * q] = tn[q].x * c2[4 * q]; x[4 * q + 1] = tn[q].y * c2[4 * q + 1];
+                    x[4 * q + 2] = tn[q].z * c2[4 * q + 2]; x[4 * q + 3] = tn[q].w * c2[4 * q + 3];
+                }
+                store_half_row_hilo(sm + OFF_T2, sm + OFF_T2 + 8192, trow, thalf * 4, x);
+            }
+            if (cc + 1 < nch) load_t(cc + 1);               // prefetch the next chunk's T
+            // V^T: [32 value rows][64 tokens] from the staged [64 tokens][32 values]
+            {
+                const __nv_bfloat16 *vsrc = reinterpret_cast<const __nv_bfloat16 *>(stg + kStageV);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int e = ptid + 128 * r, cv = e >> 3, q = e & 7;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int ee = 0; ee < 4; ++ee)
+                        w[ee] = pack2(vsrc[(q * 8 + 2 * ee) * NV + cv], vsrc[(q * 8 + 2 * ee + 1) * NV + cv]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_VT + sw128_offset(cv, q * 16)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(&bars[B_TIMG]);            // T', T'' and V^T operands written
+            // the previous chunk's MMA1 (both issuers) must have consumed the -W operand
+            if (cc >= 1 && !wg_wait(B_D1, (cc - 1) & 1, 1, lead)) break;
+            if (cc >= 1 && !wg_wait(B_D1Q, (cc - 1) & 1, 1, lead)) break;
+            // W^T from TMEM (lane = key i) -> -W hi/lo into the MMA1 A operand; key pairs
+            // (i, i^1) swap one value so that each thread stores 4-byte words
             if (!wg_wait(B_PRE_MMA, pre_mma_phase & 1, 1, lead)) break;
             ++pre_mma_phase;
             tc_fence_after();
             {
                 const int i = ptid;
-                float wv[32];
-                uint8_t *wh = sm + OFF_W + (i >> 6) * 8192;
-                const uint32_t byte = (uint32_t)(i & 63) * 2;
+                const bool odd = i & 1;
+                uint8_t *wbase = sm + OFF_W + (i >> 6) * 8192;
+                const uint32_t byte = (uint32_t)((i & 63) & ~1) * 2;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
+                    float wv[32];
                     tmem_ld32(tmem + lb + TM_W + half * 32, wv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        __nv_bfloat16 hi, lo;
-                        split_bf16(-wv[q], hi, lo);
-                        const uint32_t off = sw128_offset(half * 32 + q, byte);
-                        *reinterpret_cast<__nv_bfloat16 *>(wh + off) = hi;
-                        *reinterpret_cast<__nv_bfloat16 *>(wh + 16384 + off) = lo;
+                    for (int tp = 0; tp < 16; ++tp) {
+                        const float send = odd ? wv[2 * tp] : wv[2 * tp + 1];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                        const float a = odd ? recv : wv[2 * tp];
+                        const float b = odd ? wv[2 * tp + 1] : recv;
+                        const int row = half * 32 + 2 * tp + (odd ? 1 : 0);
+                        uint32_t hw, lw;
+                        split2_bf16(-a, -b, hw, lw);
+                        const uint32_t off = sw128_offset(row, byte);
+                        *reinterpret_cast<uint32_t *>(wbase + off) = hw;
+                        *reinterpret_cast<uint32_t *>(wbase + 16384 + off) = lw;
                     }
                 }
             }
-            // P from Q K^T (rows t = 16 pw + lane, lane < 16), once the previous chunk's
-            // MMA_O has consumed the P operand
+            // P from Q K^T once the previous chunk's MMA_O has consumed the P operand.
+            // D_QK rows sit in lanes 0-15 (M = 64 layout): lanes 16-31 take their upper
+            // 32 columns through a shuffle.
             if (cc >= 1 && !wg_wait(B_DO, (cc - 1) & 1, 1, lead)) break;
             tc_fence_after();
             {
-                float qk[64], v[32];
-                tmem_ld32(tmem + lb + TM_QK, v);
+                float v1[32], v2[32], x[32];
+                tmem_ld32(tmem + lb + tm_qk(st), v1);
+                tmem_ld32(tmem + lb + tm_qk(st) + 32, v2);
                 tmem_ld_wait();
+                const int src = lane & 15, cb = lane >> 4;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) qk[q] = v[q];
-                tmem_ld32(tmem + lb + TM_QK + 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 32; ++q) qk[32 + q] = v[q];
-                if (lane < 16) {
-                    const int t = pw * 16 + lane;
-                    const float Gt = scs[SC_G * C + t], rq = scs[SCX_RQ * C + t];
-#pragma unroll
-                    for (int q = 0; q < 64; ++q)
-                        qk[q] = (q <= t) ? expf(Gt - scs[SC_G * C + q]) * rq * scs[SC_RK * C + q] * qk[q] : 0.f;
-                    store_row_hilo(sm + OFF_P, sm + OFF_P + 8192, t, qk);
+                for (int q = 0; q < 32; ++q) {
+                    const float r2 = __shfl_sync(0xffffffffu, v2[q], src);
+                    x[q] = cb ? r2 : v1[q];
                 }
+                const int t = pw * 16 + src;
+                const float Gt = F[SC_G * C + t] * kLog2e, rqt = rq[t];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int jj = cb * 32 + q;
+                    x[q] = (jj <= t) ? exp2f(Gt - F[SC_G * C + jj] * kLog2e) * rqt * F[SC_RK * C + jj] * x[q] : 0.f;
+                }
+                store_half_row_hilo(sm + OFF_P, sm + OFF_P + 8192, t, cb * 4, x);
             }
             fence_async_smem();
             tc_fence_before();
             if (!wg_wait(B_PRE_U, pre_u_phase & 1, 1, lead)) break;
             ++pre_u_phase;
             mbar_arrive(&bars[B_PRE_DONE]);
-        }
-        if (lead && leader_issued) {
-            mma_commit(&bars[B_DRAIN2]);
-            mbar_wait(&bars[B_DRAIN2], 0);
         }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ epilogue warpgroup
@@ -679,69 +753,74 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             uint8_t *img = sm + OFF_S + (i >> 6) * 4096;
             const uint32_t byte = (uint32_t)(i & 63) * 2;
 #pragma unroll
-            for (int c = 0; c < NV; ++c) {
-                __nv_bfloat16 hi, lo;
-                split_bf16(S[c], hi, lo);
-                const uint32_t off = sw128_offset(c, byte);
-                *reinterpret_cast<__nv_bfloat16 *>(img + off) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(img + 8192 + off) = lo;
+            for (int c = 0; c < NV; c += 2) {
+                uint32_t hw, lw;
+                split2_bf16(S[c], S[c + 1], hw, lw);
+                const uint32_t off0 = sw128_offset(c, byte), off1 = sw128_offset(c + 1, byte);
+                *reinterpret_cast<uint16_t *>(img + off0) = (uint16_t)hw;
+                *reinterpret_cast<uint16_t *>(img + off1) = (uint16_t)(hw >> 16);
+                *reinterpret_cast<uint16_t *>(img + 8192 + off0) = (uint16_t)lw;
+                *reinterpret_cast<uint16_t *>(img + 8192 + off1) = (uint16_t)(lw >> 16);
             }
         };
         write_state_operand();
         fence_async_smem();
         mbar_arrive(&bars[B_S_READY]);
         float *uf = reinterpret_cast<float *>(sm + OFF_UF);
+        const int tq = ew * 16 + (lane & 15);      // token row of the M = 64 results
         for (int cc = 0; cc < nch; ++cc) {
             const int st = cc & 1, u = cc >> 1;
             const uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-            const float *fac = p.rec + ((size_t)(sr.first + cc) * p.HV + h) * kRecFloats + C * C;
+            const float *F = reinterpret_cast<const float *>(stg + kStageF);
             const int64_t tok0 = sr.t0 + (int64_t)cc * C;
             const int len = (int)min((int64_t)C, sr.t_end - tok0);
-            // the stage's tiles (query norms here, key rows for the states) are loaded
+            // the stage (query rows, key rows, factors) of this chunk is loaded
             if (!wg_wait(B_FULL0 + st, u & 1, 2, lead)) break;
+            // query normaliser of row tq: two lanes per row, overlapping MMA1
+            float qd, kd;
+            {
+                float ss = sumsq_row64(stg + kStageQ + (lane >> 4) * 8192 + tq * 128);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+                const float rqt = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
+                qd = rqt * F[SC_GAMMA * C + tq];
+                kd = F[SC_KD * C + tq];
+            }
             if (!wg_wait(B_D1, cc & 1, 2, lead)) break;
+            if (!wg_wait(B_D1Q, cc & 1, 2, lead)) break;
             tc_fence_after();
-            // E1: U rows and Q S rows (M = 64 layout: row t = 16 ew + lane for lane < 16)
+            // E1: U rows and Q S rows (M = 64 layout: row tq in lanes 0-15)
             float op[NV];
             {
-                float uu[NV], qs[NV];
+                float uu[NV], qs[NV], u2[NV];
                 tmem_ld32(tmem + lb + TM_U0 + (uint32_t)(st * NV), uu);
+                tmem_ld32(tmem + lb + TM_U2, u2);
                 tmem_ld32(tmem + lb + TM_QS, qs);
                 tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < NV; ++c) uu[c] += u2[c];
                 if (lane < 16) {
-                    const int t = ew * 16 + lane;
-                    float ss = 0.f;
+                    const uint32_t byte = (uint32_t)tq * 2;
 #pragma unroll
-                    for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const uint4 w4 = *reinterpret_cast<const uint4 *>(stg + 16384 + kb * 8192 + t * 128 + q * 16);
-                            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = __bfloat1622float2(b2[e]);
-                                ss += f.x * f.x + f.y * f.y;
-                            }
-                        }
-                    const float rq = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
-                    const float qd = rq * fac[SC_GAMMA * C + t], kd = fac[SC_KD * C + t];
-                    const uint32_t byte = (uint32_t)t * 2;
-#pragma unroll
-                    for (int c = 0; c < NV; ++c) {
+                    for (int c = 0; c < NV; c += 2) {
                         op[c] = qd * qs[c];
-                        __nv_bfloat16 hi, lo;
-                        const uint32_t off = sw128_offset(c, byte);
-                        split_bf16(kd * uu[c], hi, lo);
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_Z + off) = hi;
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_Z + 4096 + off) = lo;
-                        split_bf16(uu[c], hi, lo);
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_U + off) = hi;
-                        *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_U + 4096 + off) = lo;
+                        op[c + 1] = qd * qs[c + 1];
+                        const uint32_t off0 = sw128_offset(c, byte), off1 = sw128_offset(c + 1, byte);
+                        uint32_t hw, lw;
+                        split2_bf16(kd * uu[c], kd * uu[c + 1], hw, lw);
+                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + off0) = (uint16_t)hw;
+                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + off1) = (uint16_t)(hw >> 16);
+                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + 4096 + off0) = (uint16_t)lw;
+                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + 4096 + off1) = (uint16_t)(lw >> 16);
+                        split2_bf16(uu[c], uu[c + 1], hw, lw);
+                        *reinterpret_cast<uint16_t *>(sm + OFF_U + off0) = (uint16_t)hw;
+                        *reinterpret_cast<uint16_t *>(sm + OFF_U + off1) = (uint16_t)(hw >> 16);
+                        *reinterpret_cast<uint16_t *>(sm + OFF_U + 4096 + off0) = (uint16_t)lw;
+                        *reinterpret_cast<uint16_t *>(sm + OFF_U + 4096 + off1) = (uint16_t)(lw >> 16);
                     }
                     if (STATES) {
 #pragma unroll
                         for (int c = 0; c < NV; c += 4)
-                            *reinterpret_cast<float4 *>(uf + t * NV + c) =
+                            *reinterpret_cast<float4 *>(uf + tq * NV + c) =
                                 make_float4(uu[c], uu[c + 1], uu[c + 2], uu[c + 3]);
                     }
                 }
@@ -755,9 +834,9 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             float ds[NV];
             tmem_ld32(tmem + lb + TM_S, ds);
             tmem_ld_wait();
-            const float gl = fac[SC_MISC * C + 0];
+            const float gl = F[SC_MISC * C + 0];
             if (STATES) {
-                const uint8_t *ktile = stg + (i >> 6) * 8192;
+                const uint8_t *ktile = stg + kStageK + (i >> 6) * 8192;
                 const uint32_t kbyte = (uint32_t)(i & 63) * 2;
                 float run[NV];
 #pragma unroll
@@ -765,7 +844,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 for (int t = 0; t < len; ++t) {
                     const float kt = __bfloat162float(
                         *reinterpret_cast<const __nv_bfloat16 *>(ktile + sw128_offset(t, kbyte)));
-                    const float al = fac[SC_ALPHA * C + t], f = fac[SC_RK * C + t] * kt;
+                    const float al = F[SC_ALPHA * C + t], f = F[SC_RK * C + t] * kt;
                     float *dst = p.states + (((size_t)(tok0 + t) * p.HV + h) * D + i) * D + (size_t)vs * NV;
                     const bool last = (t == len - 1);
 #pragma unroll
@@ -794,19 +873,16 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 float dov[NV];
                 tmem_ld32(tmem + lb + TM_O, dov);
                 tmem_ld_wait();
-                if (lane < 16) {
-                    const int t = ew * 16 + lane;
-                    if (t < len) {
-                        __nv_bfloat16 *dst = p.out + ((size_t)(tok0 + t) * p.HV + h) * D + (size_t)vs * NV;
+                if (lane < 16 && tq < len) {
+                    __nv_bfloat16 *dst = p.out + ((size_t)(tok0 + tq) * p.HV + h) * D + (size_t)vs * NV;
 #pragma unroll
-                        for (int c = 0; c < NV; c += 8) {
-                            uint32_t w[4];
+                    for (int c = 0; c < NV; c += 8) {
+                        uint32_t w[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                w[e] = pack2(__float2bfloat16_rn(op[c + 2 * e] + dov[c + 2 * e]),
-                                             __float2bfloat16_rn(op[c + 2 * e + 1] + dov[c + 2 * e + 1]));
-                            *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack2(__float2bfloat16_rn(op[c + 2 * e] + dov[c + 2 * e]),
+                                         __float2bfloat16_rn(op[c + 2 * e + 1] + dov[c + 2 * e + 1]));
+                        *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
@@ -827,7 +903,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     __syncthreads();
     if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
-
 // ================================================================== host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -48,13 +48,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: the waiting thread is parked by the hardware for
+// up to `hint_ns` (or until the phase completes) instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete; gives up after `limit_ns`
 // and returns false (the caller records a timeout and stops waiting).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t limit_ns = 1000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait_sleep(bar, parity, 20000u))
         if (globaltimer_ns() - t0 > limit_ns) return false;
     return true;
 }
