@@ -149,6 +149,36 @@ int gdn_decode_step(const void *queries, const void *keys, const void *values,
                     float scale, int use_qk_l2norm, void *cuda_stream);
 
 /*
+ * gdn_prefill for callers that cannot allocate device memory (no counterpart on the
+ * pages: it exists for deployments, not for the method).  Engines that carve up
+ * device memory once in their own pool, plugins that only see the buffers their
+ * host hands them, and paths where an allocation (and the device synchronisation it
+ * may cause) is not allowed can call this instead: it takes no workspace and uses a
+ * scratch array of 64 MiB that the library keeps in device memory.
+ *
+ *   Arguments, layouts, results and error codes are those of gdn_prefill, minus the
+ *   workspace.  Shapes whose scratch would exceed 64 MiB are rejected with
+ *   GDN_ERR_WORKSPACE (for 128 x 128 bf16 heads a record is 18 KiB per 64-token chunk
+ *   and value head: B * ceil(T / 64) * HV records must fit, e.g. T = 4096 tokens at
+ *   32 value heads uses 37.8 MB).
+ *   - The array is a file-scope __device__ variable: every GPU that loads the
+ *     library holds its 64 MiB until the process exits.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents; the call
+ *     clears the status word it reads, everything else is written before it is read.
+ *     Calls whose GPU work overlaps (two streams, two host threads) race on it: order
+ *     them on one stream or serialise them.
+ *   - gdn_workspace_status() does not apply (there is no caller workspace).
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+int gdn_prefill_noalloc(const void *queries, const void *keys, const void *values,
+                        const float *decays, const float *beta, const float *initial_state,
+                        void *out, float *final_state, float *states,
+                        int B, int T, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                        float scale, int use_qk_l2norm, void *cuda_stream);
+
+/*
  * Layout of the recurrent state buffer [batch, value_heads, key_dim,
  * value_dim] float32, row = key index, column = value index (the pages'
  * State layout).  The kernels use this layout internally too, so a cache
