@@ -111,10 +111,19 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
 }
 
 // ================================================================== prep kernel
-// smem: key tile (2 x 8 KB, 128B swizzle) | A [64][65] | T [64][65] | X [16][65] | factors
+// smem: key tile (2 x 8 KB, 128B swizzle; reused as the X scratch of the solve once the
+// Gram is done) | A [64][65] | T [64][65] | per-token factors
 constexpr int kPrepThreads = 128;
 constexpr int LDA = C + 1;
-constexpr size_t kPrepSmem = 1024 /*align*/ + 16384 + 3 * C * LDA * 4 + 8 * C * 4 + 64;
+constexpr size_t kPrepSmem = 1024 /*align*/ + 16384 + 2 * C * LDA * 4 + 8 * C * 4 + 64;
+
+// 2^x on the MUFU unit (relative error ~2^-22); x <= 0 here, underflows to 0.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2eP = 1.4426950408889634f;
 
 __global__ void __launch_bounds__(kPrepThreads)
 prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
@@ -122,14 +131,15 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
     const uint32_t su = smem_u32(smem_raw);
     uint8_t *sm = smem_raw + (((su + 1023u) & ~1023u) - su);
     uint8_t *sK = sm;                                   // [2][64][128 B]
+    float *sX = reinterpret_cast<float *>(sm);          // [16][65], after the Gram
     float *sA = reinterpret_cast<float *>(sm + 16384);  // [64][65]
     float *sT = sA + C * LDA;                           // [64][65]
-    float *sX = sT + C * LDA;                           // [64][65] scratch (16 rows used)
-    float *sG = sX + C * LDA;                           // decay prefix
-    float *sB = sG + C;                                 // beta
+    float *sG = sT + C * LDA;                           // decay prefix (natural log)
+    float *sG2 = sG + C;                                // decay prefix * log2(e)
+    float *sB = sG2 + C;                                // beta
     float *sRk = sB + C;                                // key normaliser
     float *sg = sRk + C;                                // g
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sg + 4 * C);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sg + 3 * C);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
 
     const int c = blockIdx.x, h = blockIdx.y;
@@ -182,6 +192,8 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
         }
         sG[tid] = x;   // inclusive within the warp
     }
+    // T starts as zero (its upper part stays zero)
+    for (int e = tid; e < C * LDA; e += kPrepThreads) sT[e] = 0.f;
     bool ok = mbar_wait(&bar[0], 0);
     __syncthreads();
     if (tid >= 32 && tid < C) sG[tid] += sG[31];
@@ -196,6 +208,8 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
         }
         mma_commit(&bar[1]);
     }
+    __syncthreads();
+    if (tid < C) sG2[tid] = sG[tid] * kLog2eP;
     ok = ok && mbar_wait(&bar[1], 0);
     __syncthreads();
     tc_fence_after();
@@ -227,22 +241,20 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
         for (int q = 0; q < 64; ++q) diag = (q == t) ? kk[q] : diag;
         sRk[t] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
     }
+    tc_fence_before();
     __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
     if (lane < 16) {
-        const float bt = sB[t], Gt = sG[t], rt = sRk[t];
+        const float bt = sB[t], G2t = sG2[t], rt = sRk[t];
         const bool live = t < len;
 #pragma unroll
         for (int q = 0; q < 64; ++q) {
             float a = 0.f;
-            if (live && q < t) a = bt * expf(Gt - sG[q]) * rt * sRk[q] * kk[q];
+            if (live && q < t) a = bt * ex2_fast(G2t - sG2[q]) * rt * sRk[q] * kk[q];
             sA[t * LDA + q] = a;
         }
     }
-    // zero T (upper part stays zero)
-    for (int e = tid; e < C * LDA; e += kPrepThreads) sT[e] = 0.f;
-    tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
 
     // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution
     if (tid < C) {
@@ -260,29 +272,44 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
     }
     __syncthreads();
     // ---- block rows i = 1..3: X = A[i-block, 0:16i] T[0:16i, 0:16i]; T[i, 0:16i] = -T_ii X
+    // (2 x 2 register tiles; T is lower triangular so column c only needs rows m >= c)
     for (int i = 1; i < 4; ++i) {
-        const int ncol = 16 * i, nent = 16 * ncol;
-        for (int e = tid; e < nent; e += kPrepThreads) {
-            const int r = e / ncol, col = e - r * ncol;
-            const float *arow = sA + (16 * i + r) * LDA;
-            float acc = 0.f;
-            for (int m = col; m < ncol; ++m) acc += arow[m] * sT[m * LDA + col];
-            sX[r * LDA + col] = acc;
+        const int ncol = 16 * i, tpr = ncol / 2, ntile = 8 * tpr;
+        for (int e = tid; e < ntile; e += kPrepThreads) {
+            const int r0 = 2 * (e / tpr), c0 = 2 * (e % tpr);
+            const float *a0 = sA + (16 * i + r0) * LDA, *a1 = a0 + LDA;
+            float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+            for (int m = c0; m < ncol; ++m) {
+                const float t0v = sT[m * LDA + c0], t1v = sT[m * LDA + c0 + 1];
+                const float av = a0[m], bv = a1[m];
+                x00 += av * t0v; x01 += av * t1v; x10 += bv * t0v; x11 += bv * t1v;
+            }
+            sX[r0 * LDA + c0] = x00; sX[r0 * LDA + c0 + 1] = x01;
+            sX[(r0 + 1) * LDA + c0] = x10; sX[(r0 + 1) * LDA + c0 + 1] = x11;
         }
         __syncthreads();
-        for (int e = tid; e < nent; e += kPrepThreads) {
-            const int r = e / ncol, col = e - r * ncol;
-            const float *trow = sT + (16 * i + r) * LDA + 16 * i;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m) acc += trow[m] * sX[m * LDA + col];
-            sT[(16 * i + r) * LDA + col] = -acc;
+        for (int e = tid; e < ntile; e += kPrepThreads) {
+            const int r0 = 2 * (e / tpr), c0 = 2 * (e % tpr);
+            const float *t0r = sT + (16 * i + r0) * LDA + 16 * i, *t1r = t0r + LDA;
+            float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+            for (int m = 0; m <= r0 + 1; ++m) {
+                const float x0 = sX[m * LDA + c0], x1 = sX[m * LDA + c0 + 1];
+                const float ta = t0r[m], tb = t1r[m];
+                y00 += ta * x0; y01 += ta * x1; y10 += tb * x0; y11 += tb * x1;
+            }
+            float *o0 = sT + (16 * i + r0) * LDA;
+            o0[c0] = -y00; o0[c0 + 1] = -y01; o0[LDA + c0] = -y10; o0[LDA + c0 + 1] = -y11;
         }
         __syncthreads();
     }
 
     // ---- record: T row-major, then the per-token factors
     float *rec = p.rec + ((size_t)c * p.HV + h) * kRecFloats;
-    for (int e = tid; e < C * C; e += kPrepThreads) rec[e] = sT[(e >> 6) * LDA + (e & 63)];
+    for (int e = tid; e < C * C / 4; e += kPrepThreads) {
+        const int row = e >> 4, col = (e & 15) * 4;
+        const float *src = sT + row * LDA + col;
+        reinterpret_cast<float4 *>(rec)[e] = make_float4(src[0], src[1], src[2], src[3]);
+    }
     float *sc = rec + C * C;
     if (tid < C) {
         const bool in = tid < len;
@@ -721,7 +748,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int jj = cb * 32 + q;
-                    x[q] = (jj <= t) ? exp2f(Gt - F[SC_G * C + jj] * kLog2e) * rqt * F[SC_RK * C + jj] * x[q] : 0.f;
+                    x[q] = (jj <= t) ? ex2_fast(Gt - F[SC_G * C + jj] * kLog2e) * rqt * F[SC_RK * C + jj] * x[q] : 0.f;
                 }
                 store_half_row_hilo(sm + OFF_P, sm + OFF_P + 8192, t, cb * 4, x);
             }
