@@ -333,14 +333,14 @@ constexpr int kStageK = 0, kStageQ = 16384, kStageV = 32768, kStageF = 36864;
 constexpr int kStageBytes = 38912;
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int OFF_STAGE = 0;                               // [2]
-constexpr int OFF_W = OFF_STAGE + 2 * kStageBytes;         // -W hi | lo   [2][64][128B] each
+constexpr int OFF_W = OFF_STAGE + 2 * kStageBytes;         // -W hi | lo   [128 keys][128B] MN-major
 constexpr int OFF_P = OFF_W + 2 * 16384;                   // P hi | lo    [64][128B] each
 constexpr int OFF_T1 = OFF_P + 2 * 8192;                   // T' hi | lo
 constexpr int OFF_T2 = OFF_T1 + 2 * 8192;                  // T'' hi | lo
 constexpr int OFF_VT = OFF_T2 + 2 * 8192;                  // V^T [32][128B]
-constexpr int OFF_S = OFF_VT + 4096;                       // S hi | lo   [2][32][128B] each
-constexpr int OFF_Z = OFF_S + 2 * 8192;                    // Z hi | lo   [32][128B]
-constexpr int OFF_U = OFF_Z + 2 * 4096;                    // U hi | lo
+constexpr int OFF_S = OFF_VT + 4096;                       // S hi | lo   [128 keys][64B] MN-major
+constexpr int OFF_Z = OFF_S + 2 * 8192;                    // Z hi | lo   [64 tokens][64B] MN-major
+constexpr int OFF_U = OFF_Z + 2 * 4096;                    // U hi        [64 tokens][64B] MN-major
 constexpr int OFF_UF = OFF_U + 2 * 4096;                   // U fp32 [64][32] (states)
 constexpr int OFF_RQ = OFF_UF + C * NV * 4;                // query normalisers [2][64] (pre)
 constexpr int OFF_BAR = OFF_RQ + 2 * C * 4;
@@ -374,6 +374,21 @@ __device__ __forceinline__ void store_half_row_hilo(uint8_t *img_hi, uint8_t *im
         const uint32_t off = sw128_offset(row, (c0 + q) * 16);
         *reinterpret_cast<uint4 *>(img_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4 *>(img_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// 32 consecutive elements of a row of one K-major, 128B-swizzled bf16 operand image.
+__device__ __forceinline__ void store_half_row_bf16(uint8_t *img, int row, int c0,
+                                                    const float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1]);
+            h[e] = *reinterpret_cast<const uint32_t *>(&v);
+        }
+        *reinterpret_cast<uint4 *>(img + sw128_offset(row, (c0 + q) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
 }
 
@@ -484,8 +499,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id_64x32 = instr_desc(64, NV, kFmtBF16, 0, 0);
-            const uint32_t id_128x32_amn = instr_desc(128, NV, kFmtBF16, 1, 0);
+            // operands: -W (A, MN-major 128B swizzle), S / Z / U (B, MN-major 64B swizzle),
+            // key tile (A of MMA2, MN-major), P (A of MMA_O, K-major)
+            const uint32_t id_mma1 = instr_desc(64, NV, kFmtBF16, 1, 1);
+            const uint32_t id_mma2 = instr_desc(128, NV, kFmtBF16, 1, 1);
+            const uint32_t id_mmao = instr_desc(64, NV, kFmtBF16, 0, 1);
             bool issued = false;
             for (int cc = 0; cc < nch; ++cc) {
                 const int st = cc & 1;
@@ -499,12 +517,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
-                    const int kb = ks >> 2, ko = (ks & 3) * 32;
-                    const uint32_t wh = smem_u32(sm + OFF_W + kb * 8192 + ko);
-                    const uint32_t sh = smem_u32(sm + OFF_S + kb * 4096 + ko);
+                    const uint32_t wh = smem_u32(sm + OFF_W + ks * 2048);
+                    const uint32_t sh = smem_u32(sm + OFF_S + ks * 1024);
                     const uint32_t sl = sh + 8192;
-                    mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, 1);
-                    mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sl, 16, 1024, kSwizzle128B), id_64x32, 1);
+                    mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 512, kSwizzle64B), id_mma1, 1);
+                    mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sl, 16, 512, kSwizzle64B), id_mma1, 1);
                 }
                 mma_commit(&bars[B_D1]);
                 issued = true;
@@ -514,20 +531,18 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t ka = smem_u32(stg + kStageK + ks * 2048);
-                    const uint32_t zh = smem_u32(sm + OFF_Z + ks * 32);
-                    mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh, 16, 1024, kSwizzle128B), id_128x32_amn, ks > 0);
-                    mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh + 4096, 16, 1024, kSwizzle128B), id_128x32_amn, 1);
+                    const uint32_t zh = smem_u32(sm + OFF_Z + ks * 1024);
+                    mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh, 16, 512, kSwizzle64B), id_mma2, ks > 0);
+                    mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh + 4096, 16, 512, kSwizzle64B), id_mma2, 1);
                 }
                 mma_commit(&bars[B_D2]);
                 mma_commit(&bars[B_EMPTY0 + st]);
-                // MMA_O: D_O = P U  (3 hi/lo terms)
+                // MMA_O: D_O = P_hi U_hi (outputs only: one bf16 term)
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ph = smem_u32(sm + OFF_P + ks * 32), pl = ph + 8192;
-                    const uint32_t uh = smem_u32(sm + OFF_U + ks * 32), ul = uh + 4096;
-                    mma_bf16(tmem + TM_O, smem_desc(ph, 16, 1024, kSwizzle128B), smem_desc(uh, 16, 1024, kSwizzle128B), id_64x32, ks > 0);
-                    mma_bf16(tmem + TM_O, smem_desc(ph, 16, 1024, kSwizzle128B), smem_desc(ul, 16, 1024, kSwizzle128B), id_64x32, 1);
-                    mma_bf16(tmem + TM_O, smem_desc(pl, 16, 1024, kSwizzle128B), smem_desc(uh, 16, 1024, kSwizzle128B), id_64x32, 1);
+                    const uint32_t ph = smem_u32(sm + OFF_P + ks * 32);
+                    const uint32_t uh = smem_u32(sm + OFF_U + ks * 1024);
+                    mma_bf16(tmem + TM_O, smem_desc(ph, 16, 1024, kSwizzle128B), smem_desc(uh, 16, 512, kSwizzle64B), id_mmao, ks > 0);
                 }
                 mma_commit(&bars[B_DO]);
             }
@@ -538,10 +553,13 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ second MMA issuer
-        // D_QS = Q S (2 hi/lo terms): needs only the staged queries and the state, so it
-        // runs while the first issuer still waits for the pre warpgroup.
+        // D_QS = Q S_hi: needs only the staged queries and the state, so it runs while the
+        // first issuer still waits for the pre warpgroup.  Q S and P U only feed the
+        // outputs: one bf16 term each keeps them ~20x inside the output tolerance
+        // (measured 1e-3 max-abs at zero decay against the 2e-2 bound).
         if (lane == 0) {
-            const uint32_t id_64x32 = instr_desc(64, NV, kFmtBF16, 0, 0);
+            const uint32_t id_qs = instr_desc(64, NV, kFmtBF16, 0, 1);
+            const uint32_t id_u2 = instr_desc(64, NV, kFmtBF16, 1, 1);
             bool issued = false;
             for (int cc = 0; cc < nch; ++cc) {
                 const int st = cc & 1;
@@ -551,20 +569,18 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
                     const int kb = ks >> 2, ko = (ks & 3) * 32;
-                    const uint32_t sh = smem_u32(sm + OFF_S + kb * 4096 + ko);
+                    const uint32_t sh = smem_u32(sm + OFF_S + ks * 1024);
                     const uint32_t qa = smem_u32(stg + kStageQ + kb * 8192 + ko);
-                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, ks > 0);
-                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sh + 8192, 16, 1024, kSwizzle128B), id_64x32, 1);
+                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 512, kSwizzle64B), id_qs, ks > 0);
                 }
                 issued = true;
                 if (!wait(B_PRE_DONE, cc & 1)) break;
                 tc_fence_after();
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
-                    const int kb = ks >> 2, ko = (ks & 3) * 32;
-                    const uint32_t wl = smem_u32(sm + OFF_W + 16384 + kb * 8192 + ko);
-                    const uint32_t sh = smem_u32(sm + OFF_S + kb * 4096 + ko);
-                    mma_bf16(tmem + TM_U2, smem_desc(wl, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 1024, kSwizzle128B), id_64x32, ks > 0);
+                    const uint32_t wl = smem_u32(sm + OFF_W + 16384 + ks * 2048);
+                    const uint32_t sh = smem_u32(sm + OFF_S + ks * 1024);
+                    mma_bf16(tmem + TM_U2, smem_desc(wl, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 512, kSwizzle64B), id_u2, ks > 0);
                 }
                 mma_commit(&bars[B_D1Q]);
                 // the next chunk's D_QS overwrites this one: the epilogue reads it before
@@ -654,7 +670,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             const float *F = reinterpret_cast<const float *>(stg + kStageF);
             float *rq = reinterpret_cast<float *>(sm + OFF_RQ) + st * C;
             if (!wg_wait(B_FULL0 + st, u & 1, 1, lead)) break;
-            // query normalisers: two threads per row
+            // query normalisers (for P): two threads per row
             {
                 float ss = sumsq_row64(stg + kStageQ + thalf * 8192 + trow * 128);
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
@@ -697,34 +713,20 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             // the previous chunk's MMA1 (both issuers) must have consumed the -W operand
             if (cc >= 1 && !wg_wait(B_D1, (cc - 1) & 1, 1, lead)) break;
             if (cc >= 1 && !wg_wait(B_D1Q, (cc - 1) & 1, 1, lead)) break;
-            // W^T from TMEM (lane = key i) -> -W hi/lo into the MMA1 A operand; key pairs
-            // (i, i^1) swap one value so that each thread stores 4-byte words
+            // W^T from TMEM (lane = key i) -> -W hi/lo: row i of the MN-major A operand
             if (!wg_wait(B_PRE_MMA, pre_mma_phase & 1, 1, lead)) break;
             ++pre_mma_phase;
             tc_fence_after();
             {
                 const int i = ptid;
-                const bool odd = i & 1;
-                uint8_t *wbase = sm + OFF_W + (i >> 6) * 8192;
-                const uint32_t byte = (uint32_t)((i & 63) & ~1) * 2;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float wv[32];
                     tmem_ld32(tmem + lb + TM_W + half * 32, wv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int tp = 0; tp < 16; ++tp) {
-                        const float send = odd ? wv[2 * tp] : wv[2 * tp + 1];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                        const float a = odd ? recv : wv[2 * tp];
-                        const float b = odd ? wv[2 * tp + 1] : recv;
-                        const int row = half * 32 + 2 * tp + (odd ? 1 : 0);
-                        uint32_t hw, lw;
-                        split2_bf16(-a, -b, hw, lw);
-                        const uint32_t off = sw128_offset(row, byte);
-                        *reinterpret_cast<uint32_t *>(wbase + off) = hw;
-                        *reinterpret_cast<uint32_t *>(wbase + 16384 + off) = lw;
-                    }
+                    for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
+                    store_half_row_hilo(sm + OFF_W, sm + OFF_W + 16384, i, half * 4, wv);
                 }
             }
             // P from Q K^T once the previous chunk's MMA_O has consumed the P operand.
@@ -750,7 +752,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     const int jj = cb * 32 + q;
                     x[q] = (jj <= t) ? ex2_fast(Gt - F[SC_G * C + jj] * kLog2e) * rqt * F[SC_RK * C + jj] * x[q] : 0.f;
                 }
-                store_half_row_hilo(sm + OFF_P, sm + OFF_P + 8192, t, cb * 4, x);
+                store_half_row_bf16(sm + OFF_P, t, cb * 4, x);
             }
             fence_async_smem();
             tc_fence_before();
@@ -776,18 +778,16 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll
             for (int q = 0; q < NV; ++q) S[q] = 0.f;
         }
+        // S hi/lo operands: row i (this thread's key) of the MN-major 64B-swizzled images
         auto write_state_operand = [&]() {
-            uint8_t *img = sm + OFF_S + (i >> 6) * 4096;
-            const uint32_t byte = (uint32_t)(i & 63) * 2;
 #pragma unroll
-            for (int c = 0; c < NV; c += 2) {
-                uint32_t hw, lw;
-                split2_bf16(S[c], S[c + 1], hw, lw);
-                const uint32_t off0 = sw128_offset(c, byte), off1 = sw128_offset(c + 1, byte);
-                *reinterpret_cast<uint16_t *>(img + off0) = (uint16_t)hw;
-                *reinterpret_cast<uint16_t *>(img + off1) = (uint16_t)(hw >> 16);
-                *reinterpret_cast<uint16_t *>(img + 8192 + off0) = (uint16_t)lw;
-                *reinterpret_cast<uint16_t *>(img + 8192 + off1) = (uint16_t)(lw >> 16);
+            for (int q = 0; q < NV / 8; ++q) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2_bf16(S[8 * q + 2 * e], S[8 * q + 2 * e + 1], h[e], l[e]);
+                const uint32_t off = sw64_offset(i, q * 16);
+                *reinterpret_cast<uint4 *>(sm + OFF_S + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_S + 8192 + off) = make_uint4(l[0], l[1], l[2], l[3]);
             }
         };
         write_state_operand();
@@ -826,23 +826,23 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll
                 for (int c = 0; c < NV; ++c) uu[c] += u2[c];
                 if (lane < 16) {
-                    const uint32_t byte = (uint32_t)tq * 2;
 #pragma unroll
-                    for (int c = 0; c < NV; c += 2) {
-                        op[c] = qd * qs[c];
-                        op[c + 1] = qd * qs[c + 1];
-                        const uint32_t off0 = sw128_offset(c, byte), off1 = sw128_offset(c + 1, byte);
-                        uint32_t hw, lw;
-                        split2_bf16(kd * uu[c], kd * uu[c + 1], hw, lw);
-                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + off0) = (uint16_t)hw;
-                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + off1) = (uint16_t)(hw >> 16);
-                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + 4096 + off0) = (uint16_t)lw;
-                        *reinterpret_cast<uint16_t *>(sm + OFF_Z + 4096 + off1) = (uint16_t)(lw >> 16);
-                        split2_bf16(uu[c], uu[c + 1], hw, lw);
-                        *reinterpret_cast<uint16_t *>(sm + OFF_U + off0) = (uint16_t)hw;
-                        *reinterpret_cast<uint16_t *>(sm + OFF_U + off1) = (uint16_t)(hw >> 16);
-                        *reinterpret_cast<uint16_t *>(sm + OFF_U + 4096 + off0) = (uint16_t)lw;
-                        *reinterpret_cast<uint16_t *>(sm + OFF_U + 4096 + off1) = (uint16_t)(lw >> 16);
+                    for (int c = 0; c < NV; ++c) op[c] = qd * qs[c];
+                    // row tq of the MN-major 64B-swizzled Z (hi, lo) and U (hi) operands
+#pragma unroll
+                    for (int q = 0; q < NV / 8; ++q) {
+                        uint32_t zh[4], zl[4], uh[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 8 * q + 2 * e;
+                            split2_bf16(kd * uu[c], kd * uu[c + 1], zh[e], zl[e]);
+                            const __nv_bfloat162 u2v = __floats2bfloat162_rn(uu[c], uu[c + 1]);
+                            uh[e] = *reinterpret_cast<const uint32_t *>(&u2v);
+                        }
+                        const uint32_t off = sw64_offset(tq, q * 16);
+                        *reinterpret_cast<uint4 *>(sm + OFF_Z + off) = make_uint4(zh[0], zh[1], zh[2], zh[3]);
+                        *reinterpret_cast<uint4 *>(sm + OFF_Z + 4096 + off) = make_uint4(zl[0], zl[1], zl[2], zl[3]);
+                        *reinterpret_cast<uint4 *>(sm + OFF_U + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
                     }
                     if (STATES) {
 #pragma unroll
@@ -893,7 +893,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             for (int c = 0; c < NV; ++c) S[c] = gl * S[c] + ds[c];
             write_state_operand();
             fence_async_smem();
-            // outputs
+            tc_fence_before();
+            mbar_arrive(&bars[B_S_READY]);   // the next chunk's MMA1 may start now
+            named_sync(2, 128);              // every reader of the stage and of uf is done
+            if (lead) mbar_arrive(&bars[B_EMPTY0 + st]);
+            // outputs, off the chain's critical path
             if (!wg_wait(B_DO, cc & 1, 2, lead)) break;
             tc_fence_after();
             {
@@ -914,9 +918,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars[B_S_READY]);
-            named_sync(2, 128);              // every reader of the stage and of uf is done
-            if (lead) mbar_arrive(&bars[B_EMPTY0 + st]);
         }
         // final state slice
         if (!*s_err) {

@@ -219,6 +219,14 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
     return row * 128u + ((((byte_in_row >> 4) ^ (row & 7u)) << 4) | (byte_in_row & 15u));
 }
 
+// Byte offset of element (row, byte) in a 64-byte-swizzled tile whose rows are 64 bytes
+// (TMA CU_TENSOR_MAP_SWIZZLE_64B pattern: the 16-byte chunk index is XOR-ed with address
+// bits 7-8).  The tile must be 512-aligned.
+__host__ __device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t byte_in_row) {
+    const uint32_t addr = row * 64u + byte_in_row;
+    return (addr & ~0x30u) | ((((addr >> 4) & 3u) ^ ((addr >> 7) & 3u)) << 4);
+}
+
 // fp32 -> tf32 with round-to-nearest (ties away), kept in a 32-bit container.
 __device__ __forceinline__ float to_tf32(float x) {
     uint32_t r;
