@@ -239,57 +239,71 @@ def bench_e2e(gdn, w, iters, warmup):
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
-def oracle_sample(w, target_s=12.0, max_chains=None):
-    """Time the fp64 oracle on a bounded sample of the workload: whole chains (all of a
-    sequence's tokens for one value head), as many as fit in ~target_s on the host cores.
-    Returns (tokens/s equivalent for all heads, cores, description)."""
-    import oracle
-    d = workloads.workload_inputs(w, device="cpu", T_override=min(w.T, 4096) if w.T else None)
-    T = d["queries"].shape[1]
-    cores = oracle.default_threads()
-    # one chain first, to size the sample
-    t0 = time.perf_counter()
-    oracle.forward(d["queries"][:1], d["keys"][:1], d["values"][:1], d["decays"][:1],
-                   d["beta"][:1], chains=[0], n_threads=1)
-    one = time.perf_counter() - t0
-    n = max(1, min(w.HV * w.B if not max_chains else max_chains,
-                   int(target_s * cores / max(one, 1e-6))))
-    n = min(n, w.B * w.HV)
-    chains = list(range(n))
-    t0 = time.perf_counter()
-    oracle.forward(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
-                   chains=chains, n_threads=cores)
-    el = time.perf_counter() - t0
-    tok_per_s = (n / w.HV) * T / el
-    return tok_per_s, cores, f"{n} (sequence, value head) chains x {T} tokens of {w.name}, fp64", el
+class OracleSample:
+    """The fp64 oracle on a bounded sample of a workload: whole (sequence, value head)
+    chains, as many as run in about `target_s` seconds on the host cores.  Inputs are
+    drawn once; each call of run() times the same sample."""
+
+    def __init__(self, w, target_s=12.0):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.d = workloads.workload_inputs(w, device="cpu", T_override=min(w.T, 4096) if w.T else None)
+        self.T = self.d["queries"].shape[1]
+        self.cores = oracle.default_threads()
+        t0 = time.perf_counter()
+        oracle.forward(*(self.d[k][:1] for k in ("queries", "keys", "values", "decays", "beta")),
+                       chains=[0], n_threads=1)
+        one = time.perf_counter() - t0
+        self.n = max(1, min(w.B * w.HV, int(target_s * self.cores / max(one, 1e-6))))
+        self.desc = (f"{self.n} (sequence, value head) chains x {self.T} tokens of {w.name}, "
+                     f"fp64, {self.cores} threads")
+
+    def run(self):
+        """Tokens/s (all value heads of a token counted once) of one timed pass."""
+        d = self.d
+        t0 = time.perf_counter()
+        self.oracle.forward(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                            chains=list(range(self.n)), n_threads=self.cores)
+        el = time.perf_counter() - t0
+        return (self.n / self.w.HV) * self.T / el
 
 
 # ---------------------------------------------------------------- main
-def dist_setup():
+def dist_setup(backend="nccl"):
+    """One process per GPU (torchrun): rank, local rank and world size from the env."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
     return ws, rank, local
 
 
-def max_over_ranks(x, ws):
+def max_over_ranks(x, ws, device="cuda"):
+    """Slowest rank's time: the job is done when every replica is."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
-def barrier(ws):
+def job_rate(units_per_rank, seconds_max, ws):
+    """Whole-job throughput of a weak-scaled run: every rank processes its own batch."""
+    return ws * units_per_rank / seconds_max
+
+
+def barrier(ws, cuda=True):
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if cuda:
+        torch.cuda.synchronize()
 
 
 def run_reference(args, ws, rank):
@@ -297,14 +311,13 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return
     w = workloads.WORKLOADS["next_prefill_T4096_hk16_hv32_d128"]
-    vals = []
-    desc = cores = None
+    # each step a bounded sample, sized so that all steps take about two minutes
+    sample = OracleSample(w, target_s=max(1.0, 120.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
-        pass   # the oracle has no warm-up state; nothing to do
-    for _ in range(args.steps):
-        v, cores, desc, _ = oracle_sample(w, target_s=max(2.0, 60.0 / max(args.steps, 1)))
-        vals.append(v)
+        sample.run()
+    vals = [sample.run() for _ in range(args.steps)]
     value = statistics.mean(vals)
+    cores, desc = sample.cores, sample.desc
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * 4096 / value, "higher_is_better": True, "scaling": "weak",
@@ -326,6 +339,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline and decode only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-T", type=int, default=0,
+                    help="override the headline prefill length (profiling a case larger than L2)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -345,10 +360,10 @@ def main():
     W = workloads.WORKLOADS
     head_w = W["next_prefill_T4096_hk16_hv32_d128"]
     barrier(ws)
-    head = bench_prefill(gdn, head_w, args.steps, args.warmup)
+    head = bench_prefill(gdn, head_w, args.steps, args.warmup, T_override=args.prefill_T or None)
     barrier(ws)
     ms = max_over_ranks(head["ms"], ws)
-    value = ws * head["tokens"] / (ms * 1e-3)
+    value = job_rate(head["tokens"], ms * 1e-3, ws)
     dec = bench_decode(gdn, W["decode_B256_hk16_hv32_d128"], max(args.steps, 20), args.warmup)
     dec_ms = max_over_ranks(dec["ms"], ws)
 
@@ -369,8 +384,9 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, cores, desc, _ = oracle_sample(head_w)
-        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        sample = OracleSample(head_w)
+        cpu = {"value": sample.run(), "unit": "tokens/s", "cores": sample.cores, "kind": "oracle",
+               "sample": sample.desc}
 
     if rank != 0:
         return
