@@ -15,15 +15,18 @@
 //  prep  -- one CTA per (chunk, value head), all independent: TMA the key tile, Gram
 //           K K^T on the tensor core, norms, decay prefix, A, then T = (I + A)^{-1} by a
 //           blocked forward substitution in fp32 (16 x 16 diagonal blocks, then block
-//           rows).  Writes T and the per-token factors (18 KB per record).
+//           rows).  Writes T' = T diag(beta gamma rk) and T'' = T diag(beta) as hi/lo
+//           bf16 operand images, ready for the tensor core, and the per-token factors
+//           (34 KiB per record).
 //  chain -- one CTA per (sequence, value head, 32-wide value slice), the sequential
 //           chunk loop, warp-specialised:
-//             warp 0       TMA producer (key, query tiles, value slice; 2-stage ring)
+//             warp 0       TMA producer (key, query tiles, value slice, the chunk's
+//                          record; 2-stage ring)
 //             warp 1       MMA issuer of the state-dependent products
-//             warps 4-7    "pre" warpgroup, one chunk ahead: query norms, Q K^T -> P,
-//                          T' = T diag(beta gamma rk), T'' = T diag(beta) as hi/lo
-//                          operands, W^T = K^T T'^T and Ut = T'' V on the tensor core,
-//                          W -> -W hi/lo operand
+//             warp 2       MMA issuer of Q S and of the -W_lo S term
+//             warp 3       MMA issuer of Q K^T, W^T = K^T T'^T and Ut = T'' V
+//             warps 4-7    "pre" warpgroup, one chunk ahead: query norms, V^T operand,
+//                          W -> -W hi/lo operand, Q K^T -> P
 //             warps 8-11   epilogue warpgroup: holds the fp32 state slice in registers
 //                          (thread i = key row i), forms U, Z = kd U, O, the new state,
 //                          writes outputs (and the per-token states when asked).
@@ -44,7 +47,14 @@ using namespace sm100;
 constexpr int C = 64;          // chunk
 constexpr int D = 128;         // key_dim = value_dim
 constexpr int NV = 32;         // value columns per chain CTA
-constexpr int kRecFloats = C * C + 8 * C;   // T, then 8 per-token factor rows
+// Record of one (chunk, value head), written by the prep kernel and bulk-copied as is
+// into the chain kernel's stage: T' = T diag(beta gamma rk) and T'' = T diag(beta) as
+// bf16 hi and lo MMA operand images (K-major, 128B swizzle, 8 KiB each), then 8 rows
+// of per-token factors.
+constexpr int kRecImgBytes = 4 * 8192;
+constexpr int kRecFactorOff = kRecImgBytes / 4;           // in floats
+constexpr int kRecFloats = kRecFactorOff + 8 * C;
+constexpr int kRecBytes = kRecFloats * 4;                  // 34 KiB
 enum { SC_C1 = 0, SC_C2, SC_KD, SC_G, SC_RK, SC_ALPHA, SC_GAMMA, SC_MISC };
 
 struct Params {
@@ -108,6 +118,52 @@ __device__ __forceinline__ void split2_bf16(float a, float b, uint32_t &hi, uint
 
 __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
     return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
+// 32 consecutive elements of a row (chunks c0 .. c0+3 of 16 bytes) of two K-major,
+// 128B-swizzled bf16 operand images: hi and lo parts of x.
+__device__ __forceinline__ void store_half_row_hilo(uint8_t *img_hi, uint8_t *img_lo, int row,
+                                                    int c0, const float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2_bf16(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1], h[e], l[e]);
+        const uint32_t off = sw128_offset(row, (c0 + q) * 16);
+        *reinterpret_cast<uint4 *>(img_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(img_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+// 32 consecutive elements of a row of one K-major, 128B-swizzled bf16 operand image.
+__device__ __forceinline__ void store_half_row_bf16(uint8_t *img, int row, int c0,
+                                                    const float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1]);
+            h[e] = *reinterpret_cast<const uint32_t *>(&v);
+        }
+        *reinterpret_cast<uint4 *>(img + sw128_offset(row, (c0 + q) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// sum of squares of 64 bf16 (8 swizzled 16-byte chunks: chunk order does not matter)
+__device__ __forceinline__ float sumsq_row64(const uint8_t *row128) {
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(row128 + q * 16);
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(b2[e]);
+            ss += f.x * f.x + f.y * f.y;
+        }
+    }
+    return ss;
 }
 
 // ================================================================== prep kernel
@@ -303,14 +359,29 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
         __syncthreads();
     }
 
-    // ---- record: T row-major, then the per-token factors
+    // ---- record: T' = T diag(c1) and T'' = T diag(c2) as hi/lo operand images (two
+    // threads per row, 32 columns each), then the per-token factors
     float *rec = p.rec + ((size_t)c * p.HV + h) * kRecFloats;
-    for (int e = tid; e < C * C / 4; e += kPrepThreads) {
-        const int row = e >> 4, col = (e & 15) * 4;
-        const float *src = sT + row * LDA + col;
-        reinterpret_cast<float4 *>(rec)[e] = make_float4(src[0], src[1], src[2], src[3]);
+    float *sC1 = reinterpret_cast<float *>(sm);      // the key tile is free by now
+    float *sC2 = sC1 + C;
+    if (tid < C) {
+        const bool in = tid < len;
+        sC1[tid] = in ? sB[tid] * expf(sG[tid]) * sRk[tid] : 0.f;
+        sC2[tid] = in ? sB[tid] : 0.f;
     }
-    float *sc = rec + C * C;
+    __syncthreads();
+    {
+        const int t = tid >> 1, hh = tid & 1;
+        float x[32];
+        uint8_t *img = reinterpret_cast<uint8_t *>(rec);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) x[q] = sT[t * LDA + hh * 32 + q] * sC1[hh * 32 + q];
+        store_half_row_hilo(img, img + 8192, t, hh * 4, x);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) x[q] = sT[t * LDA + hh * 32 + q] * sC2[hh * 32 + q];
+        store_half_row_hilo(img + 16384, img + 24576, t, hh * 4, x);
+    }
+    float *sc = rec + kRecFactorOff;
     if (tid < C) {
         const bool in = tid < len;
         const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid], b = sB[tid];
@@ -328,20 +399,20 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
 
 // ================================================================== chain kernel
 constexpr int kChainThreads = 384;
-// stage: key tile | query tile | value slice | the record's per-token factor rows
-constexpr int kStageK = 0, kStageQ = 16384, kStageV = 32768, kStageF = 36864;
-constexpr int kStageBytes = 38912;
+// stage: key tile | query tile | value slice | the chunk's record (T', T'' operand
+// images, then the per-token factor rows)
+constexpr int kStageK = 0, kStageQ = 16384, kStageV = 32768, kStageT1 = 36864,
+              kStageT2 = kStageT1 + 16384, kStageF = kStageT1 + kRecImgBytes;
+constexpr int kStageBytes = kStageT1 + kRecBytes;           // 70 KiB
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int OFF_STAGE = 0;                               // [2]
 constexpr int OFF_W = OFF_STAGE + 2 * kStageBytes;         // -W hi | lo   [128 keys][128B] MN-major
-constexpr int OFF_P = OFF_W + 2 * 16384;                   // P hi | lo    [64][128B] each
-constexpr int OFF_T1 = OFF_P + 2 * 8192;                   // T' hi | lo
-constexpr int OFF_T2 = OFF_T1 + 2 * 8192;                  // T'' hi | lo
-constexpr int OFF_VT = OFF_T2 + 2 * 8192;                  // V^T [32][128B]
+constexpr int OFF_P = OFF_W + 2 * 16384;                   // P hi        [64][128B] K-major
+constexpr int OFF_VT = OFF_P + 8192;                       // V^T [32][128B]
 constexpr int OFF_S = OFF_VT + 4096;                       // S hi | lo   [128 keys][64B] MN-major
 constexpr int OFF_Z = OFF_S + 2 * 8192;                    // Z hi | lo   [64 tokens][64B] MN-major
 constexpr int OFF_U = OFF_Z + 2 * 4096;                    // U hi        [64 tokens][64B] MN-major
-constexpr int OFF_UF = OFF_U + 2 * 4096;                   // U fp32 [64][32] (states)
+constexpr int OFF_UF = OFF_U + 4096;                       // U fp32 [64][32] (states)
 constexpr int OFF_RQ = OFF_UF + C * NV * 4;                // query normalisers [2][64] (pre)
 constexpr int OFF_BAR = OFF_RQ + 2 * C * 4;
 constexpr int kChainSmem = OFF_BAR + 256 + 1024;
@@ -349,64 +420,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM columns
 constexpr uint32_t TM_QK = 0, TM_W = 64, TM_U0 = 128, TM_QS = 192, TM_S = 224, TM_O = 256,
-                   TM_U2 = 288, TM_QK1 = 320;
-// D_QK is double-buffered: chunk cc uses TM_QK (cc even) or TM_QK1 (cc odd)
+                   TM_U2 = 288, TM_QK1 = 320, TM_W1 = 384;
+// D_QK and D_W are double-buffered: chunk cc uses the first (cc even) or second copy
 __device__ __forceinline__ uint32_t tm_qk(int st) { return st ? TM_QK1 : TM_QK; }
+__device__ __forceinline__ uint32_t tm_w(int st) { return st ? TM_W1 : TM_W; }
 constexpr uint32_t kTmemCols = 512;
 
 // barriers
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_PRE_MMA, B_PRE_U, B_PRE_DONE, B_S_READY,
+    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_PRE_MMA0, B_PRE_MMA1, B_PRE_U, B_PRE_DONE, B_S_READY,
     B_D1, B_D1Q, B_E1, B_D2, B_DO, B_TIMG, B_DRAIN, B_DRAIN2, B_DRAIN3, B_COUNT
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
-
-// 32 consecutive elements of a row (chunks c0 .. c0+3 of 16 bytes) of two K-major,
-// 128B-swizzled bf16 operand images: hi and lo parts of x.
-__device__ __forceinline__ void store_half_row_hilo(uint8_t *img_hi, uint8_t *img_lo, int row,
-                                                    int c0, const float (&x)[32]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) split2_bf16(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1], h[e], l[e]);
-        const uint32_t off = sw128_offset(row, (c0 + q) * 16);
-        *reinterpret_cast<uint4 *>(img_hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(img_lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
-}
-
-// 32 consecutive elements of a row of one K-major, 128B-swizzled bf16 operand image.
-__device__ __forceinline__ void store_half_row_bf16(uint8_t *img, int row, int c0,
-                                                    const float (&x)[32]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t h[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 v = __floats2bfloat162_rn(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1]);
-            h[e] = *reinterpret_cast<const uint32_t *>(&v);
-        }
-        *reinterpret_cast<uint4 *>(img + sw128_offset(row, (c0 + q) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
-}
-
-// sum of squares of 64 bf16 (8 swizzled 16-byte chunks: chunk order does not matter)
-__device__ __forceinline__ float sumsq_row64(const uint8_t *row128) {
-    float ss = 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const uint4 w4 = *reinterpret_cast<const uint4 *>(row128 + q * 16);
-        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(b2[e]);
-            ss += f.x * f.x + f.y * f.y;
-        }
-    }
-    return ss;
-}
 
 template <bool STATES>
 __global__ void __launch_bounds__(kChainThreads, 1)
@@ -435,7 +461,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         mbar_init(&bars[B_FULL1], 1);
         mbar_init(&bars[B_EMPTY0], 2);      // MMA2 commit + epilogue warpgroup
         mbar_init(&bars[B_EMPTY1], 2);
-        mbar_init(&bars[B_PRE_MMA], 1);
+        mbar_init(&bars[B_PRE_MMA0], 1);
+        mbar_init(&bars[B_PRE_MMA1], 1);
         mbar_init(&bars[B_PRE_U], 1);
         mbar_init(&bars[B_PRE_DONE], 128);
         mbar_init(&bars[B_S_READY], 128);
@@ -493,7 +520,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 tma_load_3d(stg + kStageQ, &mapQ, fb, 0, j, tok);
                 tma_load_3d(stg + kStageQ + 8192, &mapQ, fb, 64, j, tok);
                 tma_load_3d(stg + kStageV, &mapV, fb, vs * NV, h, tok);
-                bulk_load(stg + kStageF, rec_of(cc) + C * C, 8 * C * 4, fb);
+                bulk_load(stg + kStageT1, rec_of(cc), kRecBytes, fb);
             }
         }
     } else if (warp == 1) {
@@ -616,19 +643,20 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                              smem_desc(ka, 16, 1024, kSwizzle128B), id_qk, ks > 0);
                 }
                 issued = true;
-                if (!wait(B_TIMG, cc & 1)) break;
-                tc_fence_after();
-                // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens), A MN-major
+                // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens), A MN-major,
+                // T' from the staged record; D_W[cc % 2] was last read by the W
+                // conversion of chunk cc - 2, done before the T-operand handshake of cc - 1
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t ka = smem_u32(stg + kStageK + ks * 2048);
-                    const uint32_t th = smem_u32(sm + OFF_T1 + ks * 32);
-                    mma_bf16(tmem + TM_W, smem_desc(ka, 8192, 1024, kSwizzle128B),
+                    const uint32_t th = smem_u32(stg + kStageT1 + ks * 32);
+                    mma_bf16(tmem + tm_w(st), smem_desc(ka, 8192, 1024, kSwizzle128B),
                              smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
-                    mma_bf16(tmem + TM_W, smem_desc(ka, 8192, 1024, kSwizzle128B),
+                    mma_bf16(tmem + tm_w(st), smem_desc(ka, 8192, 1024, kSwizzle128B),
                              smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
                 }
-                mma_commit(&bars[B_PRE_MMA]);
+                mma_commit(&bars[B_PRE_MMA0 + st]);
+                if (!wait(B_TIMG, cc & 1)) break;
                 // D_U[cc % 2] was last read by the epilogue for chunk cc - 2, which is done
                 // once MMA1 of chunk cc - 1 has run (s_ready handshake)
                 if (cc >= 1 && !wait(B_D1, (cc - 1) & 1)) break;
@@ -636,7 +664,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ta = smem_u32(sm + OFF_T2 + ks * 32);
+                    const uint32_t ta = smem_u32(stg + kStageT2 + ks * 32);
                     const uint32_t vb = smem_u32(sm + OFF_VT + ks * 32);
                     mma_bf16(dU, smem_desc(ta, 16, 1024, kSwizzle128B),
                              smem_desc(vb, 16, 1024, kSwizzle128B), id_u, ks > 0);
@@ -655,15 +683,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         const int ptid = tid - 128, pw = warp & 3;
         const bool lead = (ptid == 0);
         const uint32_t lb = lane_base(warp);
-        const int trow = ptid >> 1, thalf = ptid & 1;       // T row / half handled here
-        float4 tn[8];                                        // T row half, prefetched
-        auto load_t = [&](int cc) {
-            const float4 *src = reinterpret_cast<const float4 *>(rec_of(cc) + trow * C + thalf * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) tn[q] = src[q];
-        };
-        if (nch > 0) load_t(0);
-        uint32_t pre_mma_phase = 0, pre_u_phase = 0;
+        const int trow = ptid >> 1, thalf = ptid & 1;       // query row / half handled here
+        uint32_t pre_u_phase = 0;
         for (int cc = 0; cc < nch; ++cc) {
             const int st = cc & 1, u = cc >> 1;
             uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
@@ -676,24 +697,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                 if (thalf == 0) rq[trow] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
             }
-            // T' = T diag(c1), T'' = T diag(c2): hi/lo operand half rows
-            {
-                float x[32];
-                const float *c1 = F + SC_C1 * C + thalf * 32, *c2 = F + SC_C2 * C + thalf * 32;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    x[4 * q] = tn[q].x * c1[4 * q]; x[4 * q + 1] = tn[q].y * c1[4 * q + 1];
-                    x[4 * q + 2] = tn[q].z * c1[4 * q + 2]; x[4 * q + 3] = tn[q].w * c1[4 * q + 3];
-                }
-                store_half_row_hilo(sm + OFF_T1, sm + OFF_T1 + 8192, trow, thalf * 4, x);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    x[4 * q] = tn[q].x * c2[4 * q]; x[4 * q + 1] = tn[q].y * c2[4 * q + 1];
-                    x[4 * q + 2] = tn[q].z * c2[4 * q + 2]; x[4 * q + 3] = tn[q].w * c2[4 * q + 3];
-                }
-                store_half_row_hilo(sm + OFF_T2, sm + OFF_T2 + 8192, trow, thalf * 4, x);
-            }
-            if (cc + 1 < nch) load_t(cc + 1);               // prefetch the next chunk's T
             // V^T: [32 value rows][64 tokens] from the staged [64 tokens][32 values]
             {
                 const __nv_bfloat16 *vsrc = reinterpret_cast<const __nv_bfloat16 *>(stg + kStageV);
@@ -709,20 +712,19 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 }
             }
             fence_async_smem();
-            mbar_arrive(&bars[B_TIMG]);            // T', T'' and V^T operands written
+            mbar_arrive(&bars[B_TIMG]);            // V^T operand written
             // the previous chunk's MMA1 (both issuers) must have consumed the -W operand
             if (cc >= 1 && !wg_wait(B_D1, (cc - 1) & 1, 1, lead)) break;
             if (cc >= 1 && !wg_wait(B_D1Q, (cc - 1) & 1, 1, lead)) break;
             // W^T from TMEM (lane = key i) -> -W hi/lo: row i of the MN-major A operand
-            if (!wg_wait(B_PRE_MMA, pre_mma_phase & 1, 1, lead)) break;
-            ++pre_mma_phase;
+            if (!wg_wait(B_PRE_MMA0 + st, u & 1, 1, lead)) break;
             tc_fence_after();
             {
                 const int i = ptid;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float wv[32];
-                    tmem_ld32(tmem + lb + TM_W + half * 32, wv);
+                    tmem_ld32(tmem + lb + tm_w(st) + half * 32, wv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
