@@ -12,22 +12,18 @@
 // products accumulated in fp32 in TMEM: x*y ~ hi(x)hi(y) + hi(x)lo(y) + lo(x)hi(y).
 //
 // Two kernels:
-//  prep  -- one CTA per (chunk, value head), all independent: TMA the key tile, Gram
-//           K K^T on the tensor core, norms, decay prefix, A, then T = (I + A)^{-1} by a
-//           blocked forward substitution in fp32 (16 x 16 diagonal blocks, then block
-//           rows).  Writes T' = T diag(beta gamma rk) and T'' = T diag(beta) as hi/lo
-//           bf16 operand images, ready for the tensor core, and the per-token factors
-//           (34 KiB per record).
+//  prep  -- one CTA per (chunk, value head), all independent: TMA the key and query
+//           tiles, Gram K K^T and Q K^T on the tensor core, norms, decay prefix, A, then
+//           T = (I + A)^{-1} by a blocked forward substitution in fp32 (16 x 16 diagonal
+//           blocks, then block rows), W^T = K^T T'^T on the tensor core, P; writes -W
+//           (hi/lo), T'' (hi/lo) and P as operand images, and the per-token factors.
 //  chain -- one CTA per (sequence, value head, 32-wide value slice), the sequential
-//           chunk loop, warp-specialised:
+//           chunk loop, warp-specialised (256 threads):
 //             warp 0       TMA producer (key, query tiles, value slice, the chunk's
 //                          record; 2-stage ring)
-//             warp 1       MMA issuer of the state-dependent products
-//             warp 2       MMA issuer of Q S and of the -W_lo S term
-//             warp 3       MMA issuer of Q K^T, W^T = K^T T'^T and Ut = T'' V
-//             warps 4-7    "pre" warpgroup, one chunk ahead: query norms, V^T operand,
-//                          W -> -W hi/lo operand, Q K^T -> P
-//             warps 8-11   epilogue warpgroup: holds the fp32 state slice in registers
+//             warps 1-3    MMA issuers: the three terms of -W S (one each), T'' V,
+//                          K^T Z, P U and Q S
+//             warps 4-7    epilogue warpgroup: holds the fp32 state slice in registers
 //                          (thread i = key row i), forms U, Z = kd U, O, the new state,
 //                          writes outputs (and the per-token states when asked).
 // All waits are bounded; a timeout sets GDN_ERR_TIMEOUT in the status word and the CTA
@@ -48,14 +44,16 @@ constexpr int C = 64;          // chunk
 constexpr int D = 128;         // key_dim = value_dim
 constexpr int NV = 32;         // value columns per chain CTA
 // Record of one (chunk, value head), written by the prep kernel and bulk-copied as is
-// into the chain kernel's stage: T' = T diag(beta gamma rk) and T'' = T diag(beta) as
-// bf16 hi and lo MMA operand images (K-major, 128B swizzle, 8 KiB each), then 8 rows
-// of per-token factors.
-constexpr int kRecImgBytes = 4 * 8192;
-constexpr int kRecFactorOff = kRecImgBytes / 4;           // in floats
-constexpr int kRecFloats = kRecFactorOff + 8 * C;
-constexpr int kRecBytes = kRecFloats * 4;                  // 34 KiB
-enum { SC_C1 = 0, SC_C2, SC_KD, SC_G, SC_RK, SC_ALPHA, SC_GAMMA, SC_MISC };
+// into the chain kernel's stage.  Operand images are bf16, 128B-swizzled, ready for the
+// tensor core:
+//   -W hi, -W lo  [128 keys][64 tokens]   MN-major A operand of (-W) S      16 KiB each
+//   T'' hi, lo    [64 tokens][64 tokens]  K-major A operand of T'' V        8 KiB each
+//   P             [64 tokens][64 tokens]  K-major A operand of P U          8 KiB
+//   factors       8 rows of 64 floats (qd, kd, rk, alpha, misc, 3 unused)  2 KiB
+constexpr int REC_WHI = 0, REC_WLO = 16384, REC_T2HI = 32768, REC_T2LO = 40960, REC_P = 49152,
+              REC_F = 57344;
+constexpr int kRecBytes = REC_F + 8 * C * 4;                // 58 KiB
+enum { SC_QD = 0, SC_KD, SC_RK, SC_ALPHA, SC_MISC };
 
 struct Params {
     const float *g, *beta, *s0;
@@ -68,7 +66,7 @@ struct Params {
     int l2norm;
     int max_chunks;
     int32_t *status, *chunk_seq, *chunk_first;
-    float *rec;                  // [chunks][HV][kRecFloats]
+    float *rec;                  // [chunks][HV] records of kRecBytes
 };
 
 // ------------------------------------------------------------------ shared helpers
@@ -150,53 +148,47 @@ __device__ __forceinline__ void store_half_row_bf16(uint8_t *img, int row, int c
     }
 }
 
-// sum of squares of 64 bf16 (8 swizzled 16-byte chunks: chunk order does not matter)
-__device__ __forceinline__ float sumsq_row64(const uint8_t *row128) {
-    float ss = 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const uint4 w4 = *reinterpret_cast<const uint4 *>(row128 + q * 16);
-        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(b2[e]);
-            ss += f.x * f.x + f.y * f.y;
-        }
-    }
-    return ss;
-}
-
 // ================================================================== prep kernel
-// smem: key tile (2 x 8 KB, 128B swizzle; reused as the X scratch of the solve once the
-// Gram is done) | A [64][65] | T [64][65] | per-token factors
+// One CTA per (chunk, value head).  smem (from a 1024-aligned base):
+//   key tile   [2][64][128 B], 128B swizzle (TMA)
+//   query tile [2][64][128 B], 128B swizzle (TMA); once Q K^T is done it holds the X
+//              scratch of the solve, then the T' hi/lo operand images
+//   A [64][65] | T [64][65] fp32 | per-token vectors | barriers
 constexpr int kPrepThreads = 128;
 constexpr int LDA = C + 1;
-constexpr size_t kPrepSmem = 1024 /*align*/ + 16384 + 2 * C * LDA * 4 + 8 * C * 4 + 64;
+constexpr int kPrepVec = 7;                                  // per-token vectors of C floats
+constexpr size_t kPrepSmem = 1024 /*align*/ + 32768 + 2 * C * LDA * 4 + kPrepVec * C * 4 + 64;
+constexpr uint32_t kPrepTmemCols = 128;                      // Gram / W^T (0-63), Q K^T (64-127)
 
-// 2^x on the MUFU unit (relative error ~2^-22); x <= 0 here, underflows to 0.
+// 2^x on the MUFU unit (relative error ~2^-22); underflows to 0.
 __device__ __forceinline__ float ex2_fast(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-constexpr float kLog2eP = 1.4426950408889634f;
+constexpr float kLog2e = 1.4426950408889634f;
 
-__global__ void __launch_bounds__(kPrepThreads)
-prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
+__global__ void __launch_bounds__(kPrepThreads, 3)
+prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
+            Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t su = smem_u32(smem_raw);
     uint8_t *sm = smem_raw + (((su + 1023u) & ~1023u) - su);
     uint8_t *sK = sm;                                   // [2][64][128 B]
-    float *sX = reinterpret_cast<float *>(sm);          // [16][65], after the Gram
-    float *sA = reinterpret_cast<float *>(sm + 16384);  // [64][65]
+    uint8_t *sQ = sm + 16384;                           // [2][64][128 B]
+    float *sX = reinterpret_cast<float *>(sQ);          // [16][65], during the solve
+    uint8_t *sT1 = sQ;                                  // T' hi | lo images, after the solve
+    float *sA = reinterpret_cast<float *>(sm + 32768);  // [64][65]
     float *sT = sA + C * LDA;                           // [64][65]
     float *sG = sT + C * LDA;                           // decay prefix (natural log)
     float *sG2 = sG + C;                                // decay prefix * log2(e)
     float *sB = sG2 + C;                                // beta
     float *sRk = sB + C;                                // key normaliser
-    float *sg = sRk + C;                                // g
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sg + 3 * C);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
+    float *sRq = sRk + C;                               // query normaliser (with the scale)
+    float *sg = sRq + C;                                // g
+    float *sC1 = sg + C;                                // beta gamma rk (0 past the chunk end)
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sC1 + C);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
 
     const int c = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -216,22 +208,28 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
         len = min(C, p.T_seq - local * C);
     }
     const int j = h / (p.HV / p.HK);
+    uint8_t *rec = reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h) * kRecBytes;
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
         fence_mbar_init();
         prefetch_tensormap(&mapK);
+        prefetch_tensormap(&mapQ);
     }
-    if (warp == 0) { tmem_alloc(tslot, 64); tmem_relinquish(); }
+    if (warp == 0) { tmem_alloc(tslot, kPrepTmemCols); tmem_relinquish(); }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;    // this warp's TMEM lanes
 
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bar[0], 16384);
+        mbar_arrive_expect_tx(&bar[0], 32768);
         tma_load_3d(sK, &mapK, &bar[0], 0, j, (int)t0);
         tma_load_3d(sK + 8192, &mapK, &bar[0], 64, j, (int)t0);
+        tma_load_3d(sQ, &mapQ, &bar[0], 0, j, (int)t0);
+        tma_load_3d(sQ + 8192, &mapQ, &bar[0], 64, j, (int)t0);
     }
     // gates of the chunk and the decay prefix (two warps, shuffle scan)
     if (tid < C) {
@@ -251,65 +249,80 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
     // T starts as zero (its upper part stays zero)
     for (int e = tid; e < C * LDA; e += kPrepThreads) sT[e] = 0.f;
     bool ok = mbar_wait(&bar[0], 0);
-    __syncthreads();
+    if (__syncthreads_or(!ok)) goto teardown;
     if (tid >= 32 && tid < C) sG[tid] += sG[31];
     tc_fence_after();
-    if (tid == 0 && ok) {
+    if (tid == 0) {
+        // Gram K K^T into columns 0-63, Q K^T into columns 64-127 (M = N = 64, K = 128)
         const uint32_t idesc = instr_desc(64, 64, kFmtBF16, 0, 0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t a = smem_u32(sK + (ks >> 2) * 8192 + (ks & 3) * 32);
-            mma_bf16(tmem, smem_desc(a, 16, 1024, kSwizzle128B), smem_desc(a, 16, 1024, kSwizzle128B),
-                     idesc, ks > 0);
+            const uint32_t o = (ks >> 2) * 8192 + (ks & 3) * 32;
+            const uint64_t kd = smem_desc(smem_u32(sK + o), 16, 1024, kSwizzle128B);
+            mma_bf16(tmem, kd, kd, idesc, ks > 0);
+            mma_bf16(tmem + 64, smem_desc(smem_u32(sQ + o), 16, 1024, kSwizzle128B), kd, idesc,
+                     ks > 0);
         }
         mma_commit(&bar[1]);
     }
-    __syncthreads();
-    if (tid < C) sG2[tid] = sG[tid] * kLog2eP;
-    ok = ok && mbar_wait(&bar[1], 0);
-    __syncthreads();
-    tc_fence_after();
-    if (!ok) {
-        if (tid == 0) set_error(p, GDN_ERR_TIMEOUT);
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, 64);
-        return;
-    }
-    // Gram rows: M = 64 layout, row t in lane 16 * warp + (lane < 16)
-    float kk[64];
+    // query normalisers: two threads per row; the 16-byte chunks are visited in an order
+    // that keeps the eight lanes of a quarter-warp on distinct banks
     {
-        float v[32];
-        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
-        tmem_ld32(ta, v);
-        tmem_ld_wait();
+        const int row = tid >> 1, half = tid & 1;
+        const uint8_t *src = sQ + half * 8192 + row * 128;
+        float ss = 0.f;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) kk[q] = v[q];
-        tmem_ld32(ta + 32, v);
-        tmem_ld_wait();
+        for (int q = 0; q < 8; ++q) {
+            const int pc = q ^ (row & 7) ^ (half * 4);
+            const uint4 w4 = *reinterpret_cast<const uint4 *>(src + pc * 16);
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) kk[32 + q] = v[q];
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(b2[e]);
+                ss += f.x * f.x + f.y * f.y;
+            }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (half == 0) sRq[row] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
     }
-    const int t = warp * 16 + lane;          // valid for lane < 16
-    if (lane < 16) {
-        float diag = 0.f;
+    if (tid < C) sG2[tid] = sG[tid] * kLog2e;
+    ok = mbar_wait(&bar[1], 0);
+    if (__syncthreads_or(!ok)) goto teardown;
+    tc_fence_after();
+    {
+        // Gram rows: M = 64 layout, row t in lane 16 * warp + (lane < 16)
+        float kk[64];
+        {
+            float v[32];
+            tmem_ld32(tmem + lb, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 64; ++q) diag = (q == t) ? kk[q] : diag;
-        sRk[t] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
-    if (lane < 16) {
-        const float bt = sB[t], G2t = sG2[t], rt = sRk[t];
-        const bool live = t < len;
+            for (int q = 0; q < 32; ++q) kk[q] = v[q];
+            tmem_ld32(tmem + lb + 32, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 64; ++q) {
-            float a = 0.f;
-            if (live && q < t) a = bt * ex2_fast(G2t - sG2[q]) * rt * sRk[q] * kk[q];
-            sA[t * LDA + q] = a;
+            for (int q = 0; q < 32; ++q) kk[32 + q] = v[q];
+        }
+        const int t = warp * 16 + lane;          // valid for lane < 16
+        if (lane < 16) {
+            float diag = 0.f;
+#pragma unroll
+            for (int q = 0; q < 64; ++q) diag = (q == t) ? kk[q] : diag;
+            sRk[t] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
+        }
+        __syncthreads();
+        if (lane < 16) {
+            const float bt = sB[t], G2t = sG2[t], rt = sRk[t];
+            const bool live = t < len;
+#pragma unroll
+            for (int q = 0; q < 64; ++q) {
+                float a = 0.f;
+                if (live && q < t) a = bt * ex2_fast(G2t - sG2[q]) * rt * sRk[q] * kk[q];
+                sA[t * LDA + q] = a;
+            }
         }
     }
+    if (tid < C) sC1[tid] = tid < len ? sB[tid] * expf(sG[tid]) * sRk[tid] : 0.f;
     __syncthreads();
 
     // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution
@@ -359,77 +372,122 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, Params p) {
         __syncthreads();
     }
 
-    // ---- record: T' = T diag(c1) and T'' = T diag(c2) as hi/lo operand images (two
-    // threads per row, 32 columns each), then the per-token factors
-    float *rec = p.rec + ((size_t)c * p.HV + h) * kRecFloats;
-    float *sC1 = reinterpret_cast<float *>(sm);      // the key tile is free by now
-    float *sC2 = sC1 + C;
-    if (tid < C) {
-        const bool in = tid < len;
-        sC1[tid] = in ? sB[tid] * expf(sG[tid]) * sRk[tid] : 0.f;
-        sC2[tid] = in ? sB[tid] : 0.f;
-    }
-    __syncthreads();
+    // ---- T' = T diag(beta gamma rk) as hi/lo operand images in shared memory (for W),
+    // T'' = T diag(beta) straight into the record (two threads per row, 32 columns each)
     {
         const int t = tid >> 1, hh = tid & 1;
         float x[32];
-        uint8_t *img = reinterpret_cast<uint8_t *>(rec);
 #pragma unroll
         for (int q = 0; q < 32; ++q) x[q] = sT[t * LDA + hh * 32 + q] * sC1[hh * 32 + q];
-        store_half_row_hilo(img, img + 8192, t, hh * 4, x);
+        store_half_row_hilo(sT1, sT1 + 8192, t, hh * 4, x);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) x[q] = sT[t * LDA + hh * 32 + q] * sC2[hh * 32 + q];
-        store_half_row_hilo(img + 16384, img + 24576, t, hh * 4, x);
+        for (int q = 0; q < 32; ++q) {
+            const int col = hh * 32 + q;
+            x[q] = sT[t * LDA + col] * sB[col];            // beta is 0 past the chunk end
+        }
+        store_half_row_hilo(rec + REC_T2HI, rec + REC_T2LO, t, hh * 4, x);
     }
-    float *sc = rec + kRecFactorOff;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens) into columns 0-63;
+        // A is the key tile read MN-major
+        const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ka = smem_desc(smem_u32(sK + ks * 2048), 8192, 1024, kSwizzle128B);
+            const uint32_t th = smem_u32(sT1 + ks * 32);
+            mma_bf16(tmem, ka, smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
+            mma_bf16(tmem, ka, smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
+        }
+        mma_commit(&bar[2]);
+    }
+    // ---- P from Q K^T while W runs: D_QK rows sit in lanes 0-15 (M = 64 layout), lanes
+    // 16-31 take the upper 32 columns of the same rows through a shuffle
+    {
+        float v1[32], v2[32], x[32];
+        tmem_ld32(tmem + lb + 64, v1);
+        tmem_ld32(tmem + lb + 96, v2);
+        tmem_ld_wait();
+        const int src = lane & 15, cb = lane >> 4;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const float r2 = __shfl_sync(0xffffffffu, v2[q], src);
+            x[q] = cb ? r2 : v1[q];
+        }
+        const int t = warp * 16 + src;
+        const float G2t = sG2[t], rqt = sRq[t];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const int jj = cb * 32 + q;
+            x[q] = (jj <= t && jj < len) ? ex2_fast(G2t - sG2[jj]) * rqt * sRk[jj] * x[q] : 0.f;
+        }
+        store_half_row_bf16(rec + REC_P, t, cb * 4, x);
+    }
+    // ---- per-token factors
     if (tid < C) {
+        float *sc = reinterpret_cast<float *>(rec + REC_F);
         const bool in = tid < len;
-        const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid], b = sB[tid];
-        const float gam = expf(G);
-        sc[SC_C1 * C + tid] = in ? b * gam * rk : 0.f;
-        sc[SC_C2 * C + tid] = in ? b : 0.f;
+        const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid];
+        sc[SC_QD * C + tid] = in ? sRq[tid] * expf(G) : 0.f;
         sc[SC_KD * C + tid] = in ? rk * expf(Gl - G) : 0.f;
-        sc[SC_G * C + tid] = G;
         sc[SC_RK * C + tid] = in ? rk : 0.f;
         sc[SC_ALPHA * C + tid] = in ? expf(sg[tid]) : 0.f;
-        sc[SC_GAMMA * C + tid] = in ? gam : 0.f;
         sc[SC_MISC * C + tid] = tid == 0 ? expf(Gl) : (tid == 1 ? (float)len : 0.f);
     }
+    // ---- -W hi/lo: thread i holds row i (key i) of W^T, i.e. row i of the MN-major
+    // operand of the chain's first product
+    ok = mbar_wait(&bar[2], 0);
+    if (__syncthreads_or(!ok)) goto teardown;
+    tc_fence_after();
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float wv[32];
+        tmem_ld32(tmem + lb + half * 32, wv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
+        store_half_row_hilo(rec + REC_WHI, rec + REC_WLO, tid, half * 4, wv);
+    }
+teardown:
+    if (!ok && tid == 0) set_error(p, GDN_ERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
 // ================================================================== chain kernel
-constexpr int kChainThreads = 384;
-// stage: key tile | query tile | value slice | the chunk's record (T', T'' operand
-// images, then the per-token factor rows)
-constexpr int kStageK = 0, kStageQ = 16384, kStageV = 32768, kStageT1 = 36864,
-              kStageT2 = kStageT1 + 16384, kStageF = kStageT1 + kRecImgBytes;
-constexpr int kStageBytes = kStageT1 + kRecBytes;           // 70 KiB
+constexpr int kChainThreads = 256;
+// stage: key tile | query tile | value slice (64B swizzle: the MN-major B operand of
+// Ut = T'' V as loaded) | the chunk's record
+constexpr int kStageK = 0, kStageQ = 16384, kStageV = 32768, kStageRec = 36864;
+constexpr int kStageBytes = kStageRec + kRecBytes;          // 94 KiB
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int OFF_STAGE = 0;                               // [2]
-constexpr int OFF_W = OFF_STAGE + 2 * kStageBytes;         // -W hi | lo   [128 keys][128B] MN-major
-constexpr int OFF_P = OFF_W + 2 * 16384;                   // P hi        [64][128B] K-major
-constexpr int OFF_VT = OFF_P + 8192;                       // V^T [32][128B]
-constexpr int OFF_S = OFF_VT + 4096;                       // S hi | lo   [128 keys][64B] MN-major
+constexpr int OFF_S = OFF_STAGE + 2 * kStageBytes;         // S hi | lo   [128 keys][64B] MN-major
 constexpr int OFF_Z = OFF_S + 2 * 8192;                    // Z hi | lo   [64 tokens][64B] MN-major
 constexpr int OFF_U = OFF_Z + 2 * 4096;                    // U hi        [64 tokens][64B] MN-major
 constexpr int OFF_UF = OFF_U + 4096;                       // U fp32 [64][32] (states)
-constexpr int OFF_RQ = OFF_UF + C * NV * 4;                // query normalisers [2][64] (pre)
-constexpr int OFF_BAR = OFF_RQ + 2 * C * 4;
+constexpr int OFF_BAR = OFF_UF + C * NV * 4;
 constexpr int kChainSmem = OFF_BAR + 256 + 1024;
-constexpr float kLog2e = 1.4426950408889634f;
+static_assert(kStageBytes % 1024 == 0 && kStageRec % 1024 == 0, "swizzled operands need 1 KiB alignment");
+static_assert(kChainSmem <= 232448, "shared memory");
 
-// TMEM columns
-constexpr uint32_t TM_QK = 0, TM_W = 64, TM_U0 = 128, TM_QS = 192, TM_S = 224, TM_O = 256,
-                   TM_U2 = 288, TM_QK1 = 320, TM_W1 = 384;
-// D_QK and D_W are double-buffered: chunk cc uses the first (cc even) or second copy
-__device__ __forceinline__ uint32_t tm_qk(int st) { return st ? TM_QK1 : TM_QK; }
-__device__ __forceinline__ uint32_t tm_w(int st) { return st ? TM_W1 : TM_W; }
-constexpr uint32_t kTmemCols = 512;
+// TMEM columns (M = 64 accumulators of N = 32 take 32 columns; D_S is M = 128)
+constexpr uint32_t TM_U0 = 0,     // D_U[2]: Ut + (-W_hi) S_hi, double-buffered
+                   TM_U2 = 64,    // (-W_lo) S_hi
+                   TM_U3 = 96,    // (-W_hi) S_lo
+                   TM_QS = 128,   // D_QS[2] = Q S_hi, double-buffered
+                   TM_S = 192,    // D_S = K^T Z
+                   TM_O = 224;    // D_O = P U_hi
+constexpr uint32_t kTmemCols = 256;
 
 // barriers
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_PRE_MMA0, B_PRE_MMA1, B_PRE_U, B_PRE_DONE, B_S_READY,
-    B_D1, B_D1Q, B_E1, B_D2, B_DO, B_TIMG, B_DRAIN, B_DRAIN2, B_DRAIN3, B_COUNT
+    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_PRE_U, B_S_READY, B_D1, B_D1Q, B_D1R, B_QS,
+    B_E1, B_D2, B_DO, B_DRAIN1, B_DRAIN2, B_DRAIN3, B_COUNT
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
@@ -452,29 +510,24 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     if (!p.cu_seqlens && vs == 0 && h == 0 && s == 0 && tid == 0) p.status[kStatusWord] = GDN_OK;
     const int j = h / (p.HV / p.HK);
     const int nch = sr.count;
-    auto rec_of = [&](int cc) -> const float * {
-        return p.rec + ((size_t)(sr.first + cc) * p.HV + h) * kRecFloats;
-    };
 
     if (tid == 0) {
         mbar_init(&bars[B_FULL0], 1);
         mbar_init(&bars[B_FULL1], 1);
-        mbar_init(&bars[B_EMPTY0], 2);      // MMA2 commit + epilogue warpgroup
+        mbar_init(&bars[B_EMPTY0], 2);      // last MMA commit + epilogue warpgroup
         mbar_init(&bars[B_EMPTY1], 2);
-        mbar_init(&bars[B_PRE_MMA0], 1);
-        mbar_init(&bars[B_PRE_MMA1], 1);
         mbar_init(&bars[B_PRE_U], 1);
-        mbar_init(&bars[B_PRE_DONE], 128);
         mbar_init(&bars[B_S_READY], 128);
         mbar_init(&bars[B_D1], 1);
         mbar_init(&bars[B_D1Q], 1);
+        mbar_init(&bars[B_D1R], 1);
+        mbar_init(&bars[B_QS], 1);
         mbar_init(&bars[B_E1], 128);
         mbar_init(&bars[B_D2], 1);
         mbar_init(&bars[B_DO], 1);
-        mbar_init(&bars[B_DRAIN], 1);
+        mbar_init(&bars[B_DRAIN1], 1);
         mbar_init(&bars[B_DRAIN2], 1);
         mbar_init(&bars[B_DRAIN3], 1);
-        mbar_init(&bars[B_TIMG], 128);
         *s_err = 0;
         fence_mbar_init();
         if (nch > 0) {
@@ -499,10 +552,20 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     };
     // Warpgroup-uniform wait: one elected thread polls, the warpgroup meets at a
     // named barrier, and every thread takes the same decision from the error flag.
-    auto wg_wait = [&](int b, uint32_t parity, int bar_id, bool elected) -> bool {
+    auto wg_wait = [&](int b, uint32_t parity, bool elected) -> bool {
         if (elected && !*s_err && !mbar_wait(&bars[b], parity)) fail();
-        named_sync(bar_id, 128);
+        named_sync(1, 128);
         return *s_err == 0;
+    };
+    // operand images of the state-dependent products
+    auto w_hi = [&](uint8_t *stg, int ks) { return smem_u32(stg + kStageRec + REC_WHI + ks * 2048); };
+    auto w_lo = [&](uint8_t *stg, int ks) { return smem_u32(stg + kStageRec + REC_WLO + ks * 2048); };
+    auto s_hi = [&](int ks) { return smem_u32(sm + OFF_S + ks * 1024); };
+    auto s_lo = [&](int ks) { return smem_u32(sm + OFF_S + 8192 + ks * 1024); };
+    // -W (A, M = 64 tokens, MN-major 128B swizzle) times S (B, N = 32, MN-major 64B swizzle)
+    constexpr uint32_t id_ws = instr_desc(64, NV, kFmtBF16, 1, 1);
+    auto mma_ws = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
+        mma_bf16(d, smem_desc(a, 16, 1024, kSwizzle128B), smem_desc(b, 16, 512, kSwizzle64B), id_ws, acc);
     };
 
     if (warp == 0) {
@@ -520,41 +583,34 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 tma_load_3d(stg + kStageQ, &mapQ, fb, 0, j, tok);
                 tma_load_3d(stg + kStageQ + 8192, &mapQ, fb, 64, j, tok);
                 tma_load_3d(stg + kStageV, &mapV, fb, vs * NV, h, tok);
-                bulk_load(stg + kStageT1, rec_of(cc), kRecBytes, fb);
+                bulk_load(stg + kStageRec,
+                          reinterpret_cast<const uint8_t *>(p.rec) +
+                              ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes,
+                          kRecBytes, fb);
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer 1
+        // (-W_hi) S_hi on top of Ut, then D_S = K^T Z and D_O = P U_hi
         if (lane == 0) {
-            // operands: -W (A, MN-major 128B swizzle), S / Z / U (B, MN-major 64B swizzle),
-            // key tile (A of MMA2, MN-major), P (A of MMA_O, K-major)
-            const uint32_t id_mma1 = instr_desc(64, NV, kFmtBF16, 1, 1);
             const uint32_t id_mma2 = instr_desc(128, NV, kFmtBF16, 1, 1);
             const uint32_t id_mmao = instr_desc(64, NV, kFmtBF16, 0, 1);
             bool issued = false;
             for (int cc = 0; cc < nch; ++cc) {
                 const int st = cc & 1;
                 uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-                if (!wait(B_FULL0 + st, (cc >> 1) & 1) || !wait(B_PRE_DONE, cc & 1) ||
+                if (!wait(B_FULL0 + st, (cc >> 1) & 1) || !wait(B_PRE_U, cc & 1) ||
                     !wait(B_S_READY, cc & 1))
                     break;
                 tc_fence_after();
-                // MMA1: D_U += (-W_hi) S_hi + (-W_hi) S_lo on top of Ut = T'' V; the third
-                // term (-W_lo) S_hi goes to D_U2 from the second issuer
                 const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
 #pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t wh = smem_u32(sm + OFF_W + ks * 2048);
-                    const uint32_t sh = smem_u32(sm + OFF_S + ks * 1024);
-                    const uint32_t sl = sh + 8192;
-                    mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 512, kSwizzle64B), id_mma1, 1);
-                    mma_bf16(dU, smem_desc(wh, 16, 1024, kSwizzle128B), smem_desc(sl, 16, 512, kSwizzle64B), id_mma1, 1);
-                }
+                for (int ks = 0; ks < 8; ++ks) mma_ws(dU, w_hi(stg, ks), s_hi(ks), true);
                 mma_commit(&bars[B_D1]);
                 issued = true;
                 if (!wait(B_E1, cc & 1)) break;
                 tc_fence_after();
-                // MMA2: D_S = K^T (Z hi + Z lo)   (A = key tile, MN-major)
+                // D_S = K^T (Z hi + Z lo)   (A = key tile, MN-major)
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t ka = smem_u32(stg + kStageK + ks * 2048);
@@ -563,30 +619,27 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh + 4096, 16, 512, kSwizzle64B), id_mma2, 1);
                 }
                 mma_commit(&bars[B_D2]);
-                mma_commit(&bars[B_EMPTY0 + st]);
-                // MMA_O: D_O = P_hi U_hi (outputs only: one bf16 term)
+                // D_O = P U_hi (outputs only: one bf16 term)
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ph = smem_u32(sm + OFF_P + ks * 32);
+                    const uint32_t ph = smem_u32(stg + kStageRec + REC_P + ks * 32);
                     const uint32_t uh = smem_u32(sm + OFF_U + ks * 1024);
                     mma_bf16(tmem + TM_O, smem_desc(ph, 16, 1024, kSwizzle128B), smem_desc(uh, 16, 512, kSwizzle64B), id_mmao, ks > 0);
                 }
                 mma_commit(&bars[B_DO]);
+                mma_commit(&bars[B_EMPTY0 + st]);
             }
             if (issued) {   // let every MMA of this thread finish before teardown
-                mma_commit(&bars[B_DRAIN]);
-                mbar_wait(&bars[B_DRAIN], 0);
+                mma_commit(&bars[B_DRAIN1]);
+                mbar_wait(&bars[B_DRAIN1], 0);
             }
         }
     } else if (warp == 2) {
-        // ------------------------------------------------------------ second MMA issuer
-        // D_QS = Q S_hi: needs only the staged queries and the state, so it runs while the
-        // first issuer still waits for the pre warpgroup.  Q S and P U only feed the
-        // outputs: one bf16 term each keeps them ~20x inside the output tolerance
-        // (measured 1e-3 max-abs at zero decay against the 2e-2 bound).
+        // ------------------------------------------------------------ MMA issuer 2
+        // (-W_lo) S_hi, then D_QS = Q S_hi (outputs only: one bf16 term, ~20x inside the
+        // output tolerance), which no step of the chain waits for
         if (lane == 0) {
             const uint32_t id_qs = instr_desc(64, NV, kFmtBF16, 0, 1);
-            const uint32_t id_u2 = instr_desc(64, NV, kFmtBF16, 1, 1);
             bool issued = false;
             for (int cc = 0; cc < nch; ++cc) {
                 const int st = cc & 1;
@@ -594,177 +647,62 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 if (!wait(B_FULL0 + st, (cc >> 1) & 1) || !wait(B_S_READY, cc & 1)) break;
                 tc_fence_after();
 #pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int kb = ks >> 2, ko = (ks & 3) * 32;
-                    const uint32_t sh = smem_u32(sm + OFF_S + ks * 1024);
-                    const uint32_t qa = smem_u32(stg + kStageQ + kb * 8192 + ko);
-                    mma_bf16(tmem + TM_QS, smem_desc(qa, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 512, kSwizzle64B), id_qs, ks > 0);
-                }
-                issued = true;
-                if (!wait(B_PRE_DONE, cc & 1)) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t wl = smem_u32(sm + OFF_W + 16384 + ks * 2048);
-                    const uint32_t sh = smem_u32(sm + OFF_S + ks * 1024);
-                    mma_bf16(tmem + TM_U2, smem_desc(wl, 16, 1024, kSwizzle128B), smem_desc(sh, 16, 512, kSwizzle64B), id_u2, ks > 0);
-                }
+                for (int ks = 0; ks < 8; ++ks) mma_ws(tmem + TM_U2, w_lo(stg, ks), s_hi(ks), ks > 0);
                 mma_commit(&bars[B_D1Q]);
-                // the next chunk's D_QS overwrites this one: the epilogue reads it before
-                // it arrives on s_ready, which the next iteration waits for
-            }
-            if (issued) {
-                mma_commit(&bars[B_DRAIN3]);
-                mbar_wait(&bars[B_DRAIN3], 0);
-            }
-        }
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ pre-stage MMA issuer
-        // Q K^T as soon as the tiles land; W^T = K^T T'^T and Ut = T'' V once the pre
-        // warpgroup has written the T', T'' and V^T operands.
-        if (lane == 0) {
-            const uint32_t id_qk = instr_desc(64, 64, kFmtBF16, 0, 0);
-            const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
-            const uint32_t id_u = instr_desc(64, NV, kFmtBF16, 0, 0);
-            bool issued = false;
-            for (int cc = 0; cc < nch; ++cc) {
-                const int st = cc & 1;
-                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-                if (!wait(B_FULL0 + st, (cc >> 1) & 1)) break;
-                tc_fence_after();
-                // Q K^T (M = 64, N = 64, K = 128) into D_QK[cc % 2]; its previous reader (the
-                // P step of chunk cc - 2) finished before the T-operand handshake of cc - 1
+                issued = true;
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
                     const int kb = ks >> 2, ko = (ks & 3) * 32;
                     const uint32_t qa = smem_u32(stg + kStageQ + kb * 8192 + ko);
-                    const uint32_t ka = smem_u32(stg + kStageK + kb * 8192 + ko);
-                    mma_bf16(tmem + tm_qk(st), smem_desc(qa, 16, 1024, kSwizzle128B),
-                             smem_desc(ka, 16, 1024, kSwizzle128B), id_qk, ks > 0);
+                    mma_bf16(tmem + TM_QS + (uint32_t)(st * NV), smem_desc(qa, 16, 1024, kSwizzle128B),
+                             smem_desc(s_hi(ks), 16, 512, kSwizzle64B), id_qs, ks > 0);
                 }
-                issued = true;
-                // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens), A MN-major,
-                // T' from the staged record; D_W[cc % 2] was last read by the W
-                // conversion of chunk cc - 2, done before the T-operand handshake of cc - 1
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ka = smem_u32(stg + kStageK + ks * 2048);
-                    const uint32_t th = smem_u32(stg + kStageT1 + ks * 32);
-                    mma_bf16(tmem + tm_w(st), smem_desc(ka, 8192, 1024, kSwizzle128B),
-                             smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
-                    mma_bf16(tmem + tm_w(st), smem_desc(ka, 8192, 1024, kSwizzle128B),
-                             smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
-                }
-                mma_commit(&bars[B_PRE_MMA0 + st]);
-                if (!wait(B_TIMG, cc & 1)) break;
-                // D_U[cc % 2] was last read by the epilogue for chunk cc - 2, which is done
-                // once MMA1 of chunk cc - 1 has run (s_ready handshake)
-                if (cc >= 1 && !wait(B_D1, (cc - 1) & 1)) break;
-                tc_fence_after();
-                const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ta = smem_u32(stg + kStageT2 + ks * 32);
-                    const uint32_t vb = smem_u32(sm + OFF_VT + ks * 32);
-                    mma_bf16(dU, smem_desc(ta, 16, 1024, kSwizzle128B),
-                             smem_desc(vb, 16, 1024, kSwizzle128B), id_u, ks > 0);
-                    mma_bf16(dU, smem_desc(ta + 8192, 16, 1024, kSwizzle128B),
-                             smem_desc(vb, 16, 1024, kSwizzle128B), id_u, 1);
-                }
-                mma_commit(&bars[B_PRE_U]);
+                mma_commit(&bars[B_QS]);
             }
             if (issued) {
                 mma_commit(&bars[B_DRAIN2]);
                 mbar_wait(&bars[B_DRAIN2], 0);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ pre warpgroup
-        const int ptid = tid - 128, pw = warp & 3;
-        const bool lead = (ptid == 0);
-        const uint32_t lb = lane_base(warp);
-        const int trow = ptid >> 1, thalf = ptid & 1;       // query row / half handled here
-        uint32_t pre_u_phase = 0;
-        for (int cc = 0; cc < nch; ++cc) {
-            const int st = cc & 1, u = cc >> 1;
-            uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-            const float *F = reinterpret_cast<const float *>(stg + kStageF);
-            float *rq = reinterpret_cast<float *>(sm + OFF_RQ) + st * C;
-            if (!wg_wait(B_FULL0 + st, u & 1, 1, lead)) break;
-            // query normalisers (for P): two threads per row
-            {
-                float ss = sumsq_row64(stg + kStageQ + thalf * 8192 + trow * 128);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                if (thalf == 0) rq[trow] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
-            }
-            // V^T: [32 value rows][64 tokens] from the staged [64 tokens][32 values]
-            {
-                const __nv_bfloat16 *vsrc = reinterpret_cast<const __nv_bfloat16 *>(stg + kStageV);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int e = ptid + 128 * r, cv = e >> 3, q = e & 7;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int ee = 0; ee < 4; ++ee)
-                        w[ee] = pack2(vsrc[(q * 8 + 2 * ee) * NV + cv], vsrc[(q * 8 + 2 * ee + 1) * NV + cv]);
-                    *reinterpret_cast<uint4 *>(sm + OFF_VT + sw128_offset(cv, q * 16)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ MMA issuer 3
+        // Ut = T'' V into D_U[cc % 2] once the previous chunk's D_S is done (so that it
+        // does not delay that product), then (-W_hi) S_lo
+        if (lane == 0) {
+            const uint32_t id_u = instr_desc(64, NV, kFmtBF16, 0, 1);
+            bool issued = false;
+            for (int cc = 0; cc < nch; ++cc) {
+                const int st = cc & 1;
+                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
+                if (!wait(B_FULL0 + st, (cc >> 1) & 1)) break;
+                // D_U[cc % 2] was last read by the epilogue in chunk cc - 2, before it let
+                // the products of chunk cc - 1 start
+                if (cc >= 1 && !wait(B_D2, (cc - 1) & 1)) break;
+                tc_fence_after();
+                const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
+#pragma unroll 1
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t ta = smem_u32(stg + kStageRec + REC_T2HI + ks * 32);
+                    const uint64_t vb = smem_desc(smem_u32(stg + kStageV + ks * 1024), 16, 512, kSwizzle64B);
+                    mma_bf16(dU, smem_desc(ta, 16, 1024, kSwizzle128B), vb, id_u, ks > 0);
+                    mma_bf16(dU, smem_desc(ta + 8192, 16, 1024, kSwizzle128B), vb, id_u, 1);
                 }
+                mma_commit(&bars[B_PRE_U]);
+                issued = true;
+                if (!wait(B_S_READY, cc & 1)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks) mma_ws(tmem + TM_U3, w_hi(stg, ks), s_lo(ks), ks > 0);
+                mma_commit(&bars[B_D1R]);
             }
-            fence_async_smem();
-            mbar_arrive(&bars[B_TIMG]);            // V^T operand written
-            // the previous chunk's MMA1 (both issuers) must have consumed the -W operand
-            if (cc >= 1 && !wg_wait(B_D1, (cc - 1) & 1, 1, lead)) break;
-            if (cc >= 1 && !wg_wait(B_D1Q, (cc - 1) & 1, 1, lead)) break;
-            // W^T from TMEM (lane = key i) -> -W hi/lo: row i of the MN-major A operand
-            if (!wg_wait(B_PRE_MMA0 + st, u & 1, 1, lead)) break;
-            tc_fence_after();
-            {
-                const int i = ptid;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float wv[32];
-                    tmem_ld32(tmem + lb + tm_w(st) + half * 32, wv);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
-                    store_half_row_hilo(sm + OFF_W, sm + OFF_W + 16384, i, half * 4, wv);
-                }
+            if (issued) {
+                mma_commit(&bars[B_DRAIN3]);
+                mbar_wait(&bars[B_DRAIN3], 0);
             }
-            // P from Q K^T once the previous chunk's MMA_O has consumed the P operand.
-            // D_QK rows sit in lanes 0-15 (M = 64 layout): lanes 16-31 take their upper
-            // 32 columns through a shuffle.
-            if (cc >= 1 && !wg_wait(B_DO, (cc - 1) & 1, 1, lead)) break;
-            tc_fence_after();
-            {
-                float v1[32], v2[32], x[32];
-                tmem_ld32(tmem + lb + tm_qk(st), v1);
-                tmem_ld32(tmem + lb + tm_qk(st) + 32, v2);
-                tmem_ld_wait();
-                const int src = lane & 15, cb = lane >> 4;
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const float r2 = __shfl_sync(0xffffffffu, v2[q], src);
-                    x[q] = cb ? r2 : v1[q];
-                }
-                const int t = pw * 16 + src;
-                const float Gt = F[SC_G * C + t] * kLog2e, rqt = rq[t];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int jj = cb * 32 + q;
-                    x[q] = (jj <= t) ? ex2_fast(Gt - F[SC_G * C + jj] * kLog2e) * rqt * F[SC_RK * C + jj] * x[q] : 0.f;
-                }
-                store_half_row_bf16(sm + OFF_P, t, cb * 4, x);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            if (!wg_wait(B_PRE_U, pre_u_phase & 1, 1, lead)) break;
-            ++pre_u_phase;
-            mbar_arrive(&bars[B_PRE_DONE]);
         }
-    } else if (warp >= 8) {
+    } else {
         // ------------------------------------------------------------ epilogue warpgroup
-        const int i = tid - 256;            // key row of the state slice
+        const int i = tid - 128;            // key row of the state slice
         const bool lead = (i == 0);
         const uint32_t lb = lane_base(warp);
         const int ew = warp & 3;
@@ -784,12 +722,12 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         auto write_state_operand = [&]() {
 #pragma unroll
             for (int q = 0; q < NV / 8; ++q) {
-                uint32_t h[4], l[4];
+                uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) split2_bf16(S[8 * q + 2 * e], S[8 * q + 2 * e + 1], h[e], l[e]);
+                for (int e = 0; e < 4; ++e) split2_bf16(S[8 * q + 2 * e], S[8 * q + 2 * e + 1], hw[e], lw[e]);
                 const uint32_t off = sw64_offset(i, q * 16);
-                *reinterpret_cast<uint4 *>(sm + OFF_S + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_S + 8192 + off) = make_uint4(l[0], l[1], l[2], l[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_S + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_S + 8192 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
         };
         write_state_operand();
@@ -799,37 +737,26 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         const int tq = ew * 16 + (lane & 15);      // token row of the M = 64 results
         for (int cc = 0; cc < nch; ++cc) {
             const int st = cc & 1, u = cc >> 1;
-            const uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-            const float *F = reinterpret_cast<const float *>(stg + kStageF);
+            uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
+            const float *F = reinterpret_cast<const float *>(stg + kStageRec + REC_F);
             const int64_t tok0 = sr.t0 + (int64_t)cc * C;
             const int len = (int)min((int64_t)C, sr.t_end - tok0);
-            // the stage (query rows, key rows, factors) of this chunk is loaded
-            if (!wg_wait(B_FULL0 + st, u & 1, 2, lead)) break;
-            // query normaliser of row tq: two lanes per row, overlapping MMA1
-            float qd, kd;
-            {
-                float ss = sumsq_row64(stg + kStageQ + (lane >> 4) * 8192 + tq * 128);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-                const float rqt = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
-                qd = rqt * F[SC_GAMMA * C + tq];
-                kd = F[SC_KD * C + tq];
-            }
-            if (!wg_wait(B_D1, cc & 1, 2, lead)) break;
-            if (!wg_wait(B_D1Q, cc & 1, 2, lead)) break;
+            if (!wg_wait(B_FULL0 + st, u & 1, lead)) break;
+            const float qd = F[SC_QD * C + tq], kd = F[SC_KD * C + tq];
+            if (!wg_wait(B_D1, cc & 1, lead) || !wg_wait(B_D1Q, cc & 1, lead) ||
+                !wg_wait(B_D1R, cc & 1, lead))
+                break;
             tc_fence_after();
-            // E1: U rows and Q S rows (M = 64 layout: row tq in lanes 0-15)
-            float op[NV];
+            // E1: U = D_U + D_U2 + D_U3 (M = 64 layout: row tq in lanes 0-15)
             {
-                float uu[NV], qs[NV], u2[NV];
+                float uu[NV], u2[NV], u3[NV];
                 tmem_ld32(tmem + lb + TM_U0 + (uint32_t)(st * NV), uu);
                 tmem_ld32(tmem + lb + TM_U2, u2);
-                tmem_ld32(tmem + lb + TM_QS, qs);
+                tmem_ld32(tmem + lb + TM_U3, u3);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) uu[c] += u2[c];
+                for (int c = 0; c < NV; ++c) uu[c] += u2[c] + u3[c];
                 if (lane < 16) {
-#pragma unroll
-                    for (int c = 0; c < NV; ++c) op[c] = qd * qs[c];
                     // row tq of the MN-major 64B-swizzled Z (hi, lo) and U (hi) operands
 #pragma unroll
                     for (int q = 0; q < NV / 8; ++q) {
@@ -857,8 +784,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(&bars[B_E1]);
-            // E2: new state (thread i = key row i)
-            if (!wg_wait(B_D2, cc & 1, 2, lead)) break;
+            // E2: new state (thread i = key row i); Q S_hi must have read the old state
+            if (!wg_wait(B_D2, cc & 1, lead) || !wg_wait(B_QS, cc & 1, lead)) break;
             tc_fence_after();
             float ds[NV];
             tmem_ld32(tmem + lb + TM_S, ds);
@@ -896,15 +823,14 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             write_state_operand();
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars[B_S_READY]);   // the next chunk's MMA1 may start now
-            named_sync(2, 128);              // every reader of the stage and of uf is done
-            if (lead) mbar_arrive(&bars[B_EMPTY0 + st]);
-            // outputs, off the chain's critical path
-            if (!wg_wait(B_DO, cc & 1, 2, lead)) break;
+            mbar_arrive(&bars[B_S_READY]);   // the next chunk's products may start now
+            // outputs, off the chain's critical path: O = qd * (Q S_hi) + P U_hi
+            if (!wg_wait(B_DO, cc & 1, lead)) break;
             tc_fence_after();
             {
-                float dov[NV];
+                float dov[NV], qs[NV];
                 tmem_ld32(tmem + lb + TM_O, dov);
+                tmem_ld32(tmem + lb + TM_QS + (uint32_t)(st * NV), qs);
                 tmem_ld_wait();
                 if (lane < 16 && tq < len) {
                     __nv_bfloat16 *dst = p.out + ((size_t)(tok0 + tq) * p.HV + h) * D + (size_t)vs * NV;
@@ -913,13 +839,15 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                         uint32_t w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            w[e] = pack2(__float2bfloat16_rn(op[c + 2 * e] + dov[c + 2 * e]),
-                                         __float2bfloat16_rn(op[c + 2 * e + 1] + dov[c + 2 * e + 1]));
+                            w[e] = pack2(__float2bfloat16_rn(qd * qs[c + 2 * e] + dov[c + 2 * e]),
+                                         __float2bfloat16_rn(qd * qs[c + 2 * e + 1] + dov[c + 2 * e + 1]));
                         *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
             tc_fence_before();
+            named_sync(1, 128);              // every reader of the stage and of uf is done
+            if (lead) mbar_arrive(&bars[B_EMPTY0 + st]);
         }
         // final state slice
         if (!*s_err) {
@@ -950,7 +878,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [T_total][heads][128] bf16 viewed as 3-D (element, head, token), box {box_x, 1, 64}
 static bool make_map(CUtensorMap *m, const void *base, int heads, int64_t T_total, int box_x,
-                     bool swizzle) {
+                     CUtensorMapSwizzle swizzle) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)T_total};
@@ -959,14 +887,14 @@ static bool make_map(CUtensorMap *m, const void *base, int heads, int64_t T_tota
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 }  // namespace tc
 
-size_t tc_record_bytes() { return (size_t)tc::kRecFloats * sizeof(float); }
+size_t tc_record_bytes() { return (size_t)tc::kRecBytes; }
 
 bool tc_supported(int Dk, int Dv, gdn_dtype dtype) {
     return Dk == tc::D && Dv == tc::D && dtype == GDN_BF16;
@@ -975,6 +903,8 @@ bool tc_supported(int Dk, int Dv, gdn_dtype dtype) {
 cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     using namespace tc;
     cudaError_t e;
+    // the caller sized the workspace for records of rec_floats floats
+    if ((size_t)pp.rec_floats * sizeof(float) < (size_t)kRecBytes) return cudaErrorInvalidValue;
     if (pp.cu_seqlens) {
         if ((e = launch_chunk_table(pp, st)) != cudaSuccess) return e;
     }
@@ -988,9 +918,9 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     p.chunk_first = pp.chunk_first; p.rec = pp.rec;
     CUtensorMap mk, mq, mv;
     if (pp.T_total > 0) {
-        if (!make_map(&mk, pp.k, pp.HK, pp.T_total, 64, true) ||
-            !make_map(&mq, pp.q, pp.HK, pp.T_total, 64, true) ||
-            !make_map(&mv, pp.v, pp.HV, pp.T_total, NV, false))
+        if (!make_map(&mk, pp.k, pp.HK, pp.T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&mq, pp.q, pp.HK, pp.T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&mv, pp.v, pp.HV, pp.T_total, NV, CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     } else {
         memset(&mk, 0, sizeof mk); memset(&mq, 0, sizeof mq); memset(&mv, 0, sizeof mv);
@@ -999,7 +929,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kPrepSmem)) != cudaSuccess)
             return e;
-        prep_kernel<<<dim3(pp.max_chunks, pp.HV), kPrepThreads, kPrepSmem, st>>>(mk, p);
+        prep_kernel<<<dim3(pp.max_chunks, pp.HV), kPrepThreads, kPrepSmem, st>>>(mk, mq, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (pp.N > 0) {
