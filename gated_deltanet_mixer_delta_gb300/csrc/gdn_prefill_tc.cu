@@ -18,14 +18,12 @@
 //           blocks, then block rows), W^T = K^T T'^T on the tensor core, P; writes -W
 //           (hi/lo), T'' (hi/lo) and P as operand images, and the per-token factors.
 //  chain -- one CTA per (sequence, value head, 32-wide value slice), the sequential
-//           chunk loop, warp-specialised (256 threads):
-//             warp 0       TMA producer (key, query tiles, value slice, the chunk's
-//                          record; 2-stage ring)
-//             warps 1-3    MMA issuers: the three terms of -W S (one each), T'' V,
-//                          K^T Z, P U and Q S
-//             warps 4-7    epilogue warpgroup: holds the fp32 state slice in registers
-//                          (thread i = key row i), forms U, Z = kd U, O, the new state,
-//                          writes outputs (and the per-token states when asked).
+//           chunk loop, warp-specialised (192 threads): a TMA producer warp, a warp that
+//           issues T'' V one chunk ahead, and an epilogue warpgroup that holds the fp32
+//           state slice in registers (thread i = key row i), forms U, Z = kd U, the new
+//           state and the outputs (and the per-token states when asked), and issues the
+//           tensor-core products that follow each of its steps itself.  Hi/lo operand
+//           pairs are stacked along M or N so that one instruction covers several terms.
 // All waits are bounded; a timeout sets GDN_ERR_TIMEOUT in the status word and the CTA
 // drains and exits.
 #include <string.h>
@@ -44,16 +42,20 @@ constexpr int C = 64;          // chunk
 constexpr int D = 128;         // key_dim = value_dim
 constexpr int NV = 32;         // value columns per chain CTA
 // Record of one (chunk, value head), written by the prep kernel and bulk-copied as is
-// into the chain kernel's stage.  Operand images are bf16, 128B-swizzled, ready for the
-// tensor core:
-//   -W hi, -W lo  [128 keys][64 tokens]   MN-major A operand of (-W) S      16 KiB each
-//   T'' hi, lo    [64 tokens][64 tokens]  K-major A operand of T'' V        8 KiB each
+// into the chain kernel's shared memory.  Operand images are bf16, 128B-swizzled, ready
+// for the tensor core:
+//   -W hi, -W lo  [128 keys][64 tokens]   MN-major; stacked along M they are the A
+//                                          operand [-W_hi; -W_lo] of (-W) S   16 KiB each
+//   T'' hi, lo    [64 tokens][64 tokens]  K-major; stacked, the A operand of T'' V
+//                                                                            8 KiB each
 //   P             [64 tokens][64 tokens]  K-major A operand of P U          8 KiB
-//   factors       8 rows of 64 floats (qd, kd, rk, alpha, misc, 3 unused)  2 KiB
+//   Q'            [64 tokens][128 keys]   Q' = diag(rq gamma) Q, K-major A operand of Q' S
+//                                                                            16 KiB
+//   factors       8 rows of 64 floats (kd, rk, alpha, misc, 4 unused)      2 KiB
 constexpr int REC_WHI = 0, REC_WLO = 16384, REC_T2HI = 32768, REC_T2LO = 40960, REC_P = 49152,
-              REC_F = 57344;
-constexpr int kRecBytes = REC_F + 8 * C * 4;                // 58 KiB
-enum { SC_QD = 0, SC_KD, SC_RK, SC_ALPHA, SC_MISC };
+              REC_QP = 57344, REC_F = 73728;
+constexpr int kRecBytes = REC_F + 8 * C * 4;                // 74 KiB
+enum { SC_KD = 0, SC_RK, SC_ALPHA, SC_MISC };
 
 struct Params {
     const float *g, *beta, *s0;
@@ -153,9 +155,9 @@ __device__ __forceinline__ void store_half_row_bf16(uint8_t *img, int row, int c
 //   key tile   [2][64][128 B], 128B swizzle (TMA)
 //   query tile [2][64][128 B], 128B swizzle (TMA); once Q K^T is done it holds the X
 //              scratch of the solve, then the T' hi/lo operand images
-//   A [64][65] | T [64][65] fp32 | per-token vectors | barriers
+//   A [64][68] | T [64][68] fp32 (rows 16-byte aligned) | per-token vectors | barriers
 constexpr int kPrepThreads = 128;
-constexpr int LDA = C + 1;
+constexpr int LDA = C + 4;
 constexpr int kPrepVec = 7;                                  // per-token vectors of C floats
 constexpr size_t kPrepSmem = 1024 /*align*/ + 32768 + 2 * C * LDA * 4 + kPrepVec * C * 4 + 64;
 constexpr uint32_t kPrepTmemCols = 128;                      // Gram / W^T (0-63), Q K^T (64-127)
@@ -168,6 +170,76 @@ __device__ __forceinline__ float ex2_fast(float x) {
 }
 constexpr float kLog2e = 1.4426950408889634f;
 
+__device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void sts4(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+
+// One row of an M = 64 accumulator pair (columns c0 .. c0+63) spread over a warp: the
+// rows sit in lanes 0-15 (row 16 * (warp % 4) + lane); lane l < 16 keeps columns 0-31
+// of its row, lane l + 16 receives columns 32-63 of the same row.
+__device__ __forceinline__ void tmem_row_split(uint32_t taddr, float (&x)[32]) {
+    float v1[32], v2[32];
+    tmem_ld32(taddr, v1);
+    tmem_ld32(taddr + 32, v2);
+    tmem_ld_wait();
+    const int lane = threadIdx.x & 31, src = lane & 15, cb = lane >> 4;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+        const float r2 = __shfl_sync(0xffffffffu, v2[q], src);
+        x[q] = cb ? r2 : v1[q];
+    }
+}
+
+// Off-diagonal block of T = (I + A)^{-1} from two diagonal blocks already in T:
+//   X = A[rows, cols] T[cols, cols];  T[rows, cols] = -T[rows, rows] X
+// for an n x n block (n = 16 or 32) at row offset r0 and column offset c0; thread
+// (r, cg) computes a 1 x 4*NQ strip.  Full-length loops: T and A are zero above their
+// diagonals, so no bounds are needed.
+template <int N, int NQ>
+__device__ __forceinline__ void solve_block(float *sA, float *sT, float *sX, int r0, int c0, int r,
+                                            int cg) {
+    const int cx = cg * 4 * NQ;
+    float acc[4 * NQ];
+#pragma unroll
+    for (int e = 0; e < 4 * NQ; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int m = 0; m < N; ++m) {
+        const float a = sA[(r0 + r) * LDA + c0 + m];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const float4 t4 = lds4(sT + (c0 + m) * LDA + c0 + cx + 4 * q);
+            acc[4 * q] += a * t4.x; acc[4 * q + 1] += a * t4.y;
+            acc[4 * q + 2] += a * t4.z; acc[4 * q + 3] += a * t4.w;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+        sts4(sX + r * LDA + cx + 4 * q, acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+}
+template <int N, int NQ>
+__device__ __forceinline__ void apply_block(float *sT, const float *sX, int r0, int c0, int r,
+                                            int cg) {
+    const int cx = cg * 4 * NQ;
+    float acc[4 * NQ];
+#pragma unroll
+    for (int e = 0; e < 4 * NQ; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int m = 0; m < N; ++m) {
+        const float t = sT[(r0 + r) * LDA + r0 + m];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const float4 x4 = lds4(sX + m * LDA + cx + 4 * q);
+            acc[4 * q] += t * x4.x; acc[4 * q + 1] += t * x4.y;
+            acc[4 * q + 2] += t * x4.z; acc[4 * q + 3] += t * x4.w;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+        sts4(sT + (r0 + r) * LDA + c0 + cx + 4 * q, -acc[4 * q], -acc[4 * q + 1], -acc[4 * q + 2],
+             -acc[4 * q + 3]);
+}
+
 __global__ void __launch_bounds__(kPrepThreads, 3)
 prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
             Params p) {
@@ -176,10 +248,10 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     uint8_t *sm = smem_raw + (((su + 1023u) & ~1023u) - su);
     uint8_t *sK = sm;                                   // [2][64][128 B]
     uint8_t *sQ = sm + 16384;                           // [2][64][128 B]
-    float *sX = reinterpret_cast<float *>(sQ);          // [16][65], during the solve
+    float *sX = reinterpret_cast<float *>(sQ);          // [32][68], during the solve
     uint8_t *sT1 = sQ;                                  // T' hi | lo images, after the solve
-    float *sA = reinterpret_cast<float *>(sm + 32768);  // [64][65]
-    float *sT = sA + C * LDA;                           // [64][65]
+    float *sA = reinterpret_cast<float *>(sm + 32768);  // [64][68]
+    float *sT = sA + C * LDA;                           // [64][68]
     float *sG = sT + C * LDA;                           // decay prefix (natural log)
     float *sG2 = sG + C;                                // decay prefix * log2(e)
     float *sB = sG2 + C;                                // beta
@@ -188,7 +260,7 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     float *sg = sRq + C;                                // g
     float *sC1 = sg + C;                                // beta gamma rk (0 past the chunk end)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sC1 + C);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
     const int c = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -211,9 +283,7 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     uint8_t *rec = reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h) * kRecBytes;
 
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        mbar_init(&bar[2], 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
         prefetch_tensormap(&mapK);
         prefetch_tensormap(&mapQ);
@@ -223,6 +293,8 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lb = (uint32_t)(warp * 32) << 16;    // this warp's TMEM lanes
+    const int trow = warp * 16 + (lane & 15), tcb = lane >> 4;   // row / column half of
+                                                                  // the M = 64 results
 
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar[0], 32768);
@@ -247,23 +319,23 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         sG[tid] = x;   // inclusive within the warp
     }
     // T starts as zero (its upper part stays zero)
-    for (int e = tid; e < C * LDA; e += kPrepThreads) sT[e] = 0.f;
+    for (int e = tid; e < C * LDA / 4; e += kPrepThreads) sts4(sT + 4 * e, 0.f, 0.f, 0.f, 0.f);
     bool ok = mbar_wait(&bar[0], 0);
     if (__syncthreads_or(!ok)) goto teardown;
     if (tid >= 32 && tid < C) sG[tid] += sG[31];
     tc_fence_after();
-    if (tid == 0) {
-        // Gram K K^T into columns 0-63, Q K^T into columns 64-127 (M = N = 64, K = 128)
+    if (lane == 0 && warp < 2) {
+        // Gram K K^T into columns 0-63 (thread 0), Q K^T into columns 64-127 (thread 32);
+        // M = N = 64, K = 128
         const uint32_t idesc = instr_desc(64, 64, kFmtBF16, 0, 0);
+        const uint8_t *aop = warp ? sQ : sK;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t o = (ks >> 2) * 8192 + (ks & 3) * 32;
-            const uint64_t kd = smem_desc(smem_u32(sK + o), 16, 1024, kSwizzle128B);
-            mma_bf16(tmem, kd, kd, idesc, ks > 0);
-            mma_bf16(tmem + 64, smem_desc(smem_u32(sQ + o), 16, 1024, kSwizzle128B), kd, idesc,
-                     ks > 0);
+            mma_bf16(tmem + warp * 64, smem_desc(smem_u32(aop + o), 16, 1024, kSwizzle128B),
+                     smem_desc(smem_u32(sK + o), 16, 1024, kSwizzle128B), idesc, ks > 0);
         }
-        mma_commit(&bar[1]);
+        mma_commit(&bar[1 + 2 * warp]);
     }
     // query normalisers: two threads per row; the 16-byte chunks are visited in an order
     // that keeps the eight lanes of a quarter-warp on distinct banks
@@ -286,46 +358,60 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         if (half == 0) sRq[row] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
     }
     if (tid < C) sG2[tid] = sG[tid] * kLog2e;
-    ok = mbar_wait(&bar[1], 0);
+    ok = mbar_wait(&bar[1], 0) && mbar_wait(&bar[3], 0);
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
-    {
-        // Gram rows: M = 64 layout, row t in lane 16 * warp + (lane < 16)
-        float kk[64];
-        {
-            float v[32];
-            tmem_ld32(tmem + lb, v);
-            tmem_ld_wait();
+    // Q' = diag(rq gamma) Q (0 past the chunk end) in the query tile's own swizzled
+    // layout: every 16-byte chunk of row r is scaled by the row's factor
 #pragma unroll
-            for (int q = 0; q < 32; ++q) kk[q] = v[q];
-            tmem_ld32(tmem + lb + 32, v);
-            tmem_ld_wait();
+    for (int k = 0; k < 8; ++k) {
+        const int e = tid + kPrepThreads * k, r = (e >> 3) & 63;
+        const int off = (e >> 9) * 8192 + r * 128 + (e & 7) * 16;
+        const float f = r < len ? sRq[r] * expf(sG[r]) : 0.f;
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(sQ + off);
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
+        uint32_t o[4];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) kk[32 + q] = v[q];
+        for (int q = 0; q < 4; ++q) {
+            const float2 v = __bfloat1622float2(b2[q]);
+            const __nv_bfloat162 sv = __floats2bfloat162_rn(v.x * f, v.y * f);
+            o[q] = *reinterpret_cast<const uint32_t *>(&sv);
         }
-        const int t = warp * 16 + lane;          // valid for lane < 16
-        if (lane < 16) {
+        *reinterpret_cast<uint4 *>(rec + REC_QP + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    {
+        // Gram row trow, columns tcb*32 .. +31; the key normaliser from its diagonal
+        float gr[32];
+        tmem_row_split(tmem + lb, gr);
+        {
             float diag = 0.f;
 #pragma unroll
-            for (int q = 0; q < 64; ++q) diag = (q == t) ? kk[q] : diag;
-            sRk[t] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
+            for (int q = 0; q < 32; ++q) diag = (tcb * 32 + q == trow) ? gr[q] : diag;
+            if ((trow >> 5) == tcb) sRk[trow] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
         }
         __syncthreads();
-        if (lane < 16) {
-            const float bt = sB[t], G2t = sG2[t], rt = sRk[t];
-            const bool live = t < len;
+        // A_tj = beta_t e^{G_t-G_j} rk_t rk_j k_t.k_j (j < t) into smem and
+        // P_tj = e^{G_t-G_j} rq_t rk_j q_t.k_j (j <= t) into the record, one exponential
+        float qk[32];
+        tmem_row_split(tmem + lb + 64, qk);
+        const bool live = trow < len;
+        const float G2t = sG2[trow], at = sB[trow] * sRk[trow], pt = sRq[trow];
 #pragma unroll
-            for (int q = 0; q < 64; ++q) {
-                float a = 0.f;
-                if (live && q < t) a = bt * ex2_fast(G2t - sG2[q]) * rt * sRk[q] * kk[q];
-                sA[t * LDA + q] = a;
-            }
+        for (int q = 0; q < 32; ++q) {
+            const int jj = tcb * 32 + q;
+            const float e = (jj <= trow && jj < len) ? ex2_fast(G2t - sG2[jj]) * sRk[jj] : 0.f;
+            gr[q] = (live && jj < trow) ? at * e * gr[q] : 0.f;
+            qk[q] = pt * e * qk[q];
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            sts4(sA + trow * LDA + tcb * 32 + 4 * q, gr[4 * q], gr[4 * q + 1], gr[4 * q + 2], gr[4 * q + 3]);
+        store_half_row_bf16(rec + REC_P, trow, tcb * 4, qk);
     }
     if (tid < C) sC1[tid] = tid < len ? sB[tid] * expf(sG[tid]) * sRk[tid] : 0.f;
     __syncthreads();
 
-    // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution
+    // ---- T = (I + A)^{-1}: the four 16 x 16 diagonal blocks by forward substitution
     if (tid < C) {
         const int b = tid >> 4, cc = tid & 15, base = b * 16;
         float x[16];
@@ -340,35 +426,20 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         for (int r = 0; r < 16; ++r) sT[(base + r) * LDA + base + cc] = x[r];
     }
     __syncthreads();
-    // ---- block rows i = 1..3: X = A[i-block, 0:16i] T[0:16i, 0:16i]; T[i, 0:16i] = -T_ii X
-    // (2 x 2 register tiles; T is lower triangular so column c only needs rows m >= c)
-    for (int i = 1; i < 4; ++i) {
-        const int ncol = 16 * i, tpr = ncol / 2, ntile = 8 * tpr;
-        for (int e = tid; e < ntile; e += kPrepThreads) {
-            const int r0 = 2 * (e / tpr), c0 = 2 * (e % tpr);
-            const float *a0 = sA + (16 * i + r0) * LDA, *a1 = a0 + LDA;
-            float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-            for (int m = c0; m < ncol; ++m) {
-                const float t0v = sT[m * LDA + c0], t1v = sT[m * LDA + c0 + 1];
-                const float av = a0[m], bv = a1[m];
-                x00 += av * t0v; x01 += av * t1v; x10 += bv * t0v; x11 += bv * t1v;
-            }
-            sX[r0 * LDA + c0] = x00; sX[r0 * LDA + c0 + 1] = x01;
-            sX[(r0 + 1) * LDA + c0] = x10; sX[(r0 + 1) * LDA + c0 + 1] = x11;
-        }
+    // ---- then by doubling: blocks (1,0) and (3,2) of 16 x 16 (64 threads each), then
+    // block (1,0) of 32 x 32 (all threads): T_ij = -T_ii A_ij T_jj
+    {
+        const int pb = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
+        solve_block<16, 1>(sA, sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
         __syncthreads();
-        for (int e = tid; e < ntile; e += kPrepThreads) {
-            const int r0 = 2 * (e / tpr), c0 = 2 * (e % tpr);
-            const float *t0r = sT + (16 * i + r0) * LDA + 16 * i, *t1r = t0r + LDA;
-            float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-            for (int m = 0; m <= r0 + 1; ++m) {
-                const float x0 = sX[m * LDA + c0], x1 = sX[m * LDA + c0 + 1];
-                const float ta = t0r[m], tb = t1r[m];
-                y00 += ta * x0; y01 += ta * x1; y10 += tb * x0; y11 += tb * x1;
-            }
-            float *o0 = sT + (16 * i + r0) * LDA;
-            o0[c0] = -y00; o0[c0 + 1] = -y01; o0[LDA + c0] = -y10; o0[LDA + c0 + 1] = -y11;
-        }
+        apply_block<16, 1>(sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
+        __syncthreads();
+    }
+    {
+        const int r = tid >> 2, cg = tid & 3;
+        solve_block<32, 2>(sA, sT, sX, 32, 0, r, cg);
+        __syncthreads();
+        apply_block<32, 2>(sT, sX, 32, 0, r, cg);
         __syncthreads();
     }
 
@@ -376,15 +447,17 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     // T'' = T diag(beta) straight into the record (two threads per row, 32 columns each)
     {
         const int t = tid >> 1, hh = tid & 1;
-        float x[32];
+        float tv[32], x[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) x[q] = sT[t * LDA + hh * 32 + q] * sC1[hh * 32 + q];
+        for (int q = 0; q < 8; ++q) {
+            const float4 t4 = lds4(sT + t * LDA + hh * 32 + 4 * q);
+            tv[4 * q] = t4.x; tv[4 * q + 1] = t4.y; tv[4 * q + 2] = t4.z; tv[4 * q + 3] = t4.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) x[q] = tv[q] * sC1[hh * 32 + q];
         store_half_row_hilo(sT1, sT1 + 8192, t, hh * 4, x);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const int col = hh * 32 + q;
-            x[q] = sT[t * LDA + col] * sB[col];            // beta is 0 past the chunk end
-        }
+        for (int q = 0; q < 32; ++q) x[q] = tv[q] * sB[hh * 32 + q];   // beta is 0 past the end
         store_half_row_hilo(rec + REC_T2HI, rec + REC_T2LO, t, hh * 4, x);
     }
     fence_async_smem();
@@ -404,34 +477,11 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         }
         mma_commit(&bar[2]);
     }
-    // ---- P from Q K^T while W runs: D_QK rows sit in lanes 0-15 (M = 64 layout), lanes
-    // 16-31 take the upper 32 columns of the same rows through a shuffle
-    {
-        float v1[32], v2[32], x[32];
-        tmem_ld32(tmem + lb + 64, v1);
-        tmem_ld32(tmem + lb + 96, v2);
-        tmem_ld_wait();
-        const int src = lane & 15, cb = lane >> 4;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const float r2 = __shfl_sync(0xffffffffu, v2[q], src);
-            x[q] = cb ? r2 : v1[q];
-        }
-        const int t = warp * 16 + src;
-        const float G2t = sG2[t], rqt = sRq[t];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const int jj = cb * 32 + q;
-            x[q] = (jj <= t && jj < len) ? ex2_fast(G2t - sG2[jj]) * rqt * sRk[jj] * x[q] : 0.f;
-        }
-        store_half_row_bf16(rec + REC_P, t, cb * 4, x);
-    }
     // ---- per-token factors
     if (tid < C) {
         float *sc = reinterpret_cast<float *>(rec + REC_F);
         const bool in = tid < len;
         const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid];
-        sc[SC_QD * C + tid] = in ? sRq[tid] * expf(G) : 0.f;
         sc[SC_KD * C + tid] = in ? rk * expf(Gl - G) : 0.f;
         sc[SC_RK * C + tid] = in ? rk : 0.f;
         sc[SC_ALPHA * C + tid] = in ? expf(sg[tid]) : 0.f;
@@ -459,43 +509,112 @@ teardown:
 }
 
 // ================================================================== chain kernel
-constexpr int kChainThreads = 256;
-// stage: key tile | query tile | value slice (64B swizzle: the MN-major B operand of
-// Ut = T'' V as loaded) | the chunk's record
-constexpr int kStageK = 0, kStageQ = 16384, kStageV = 32768, kStageRec = 36864;
-constexpr int kStageBytes = kStageRec + kRecBytes;          // 94 KiB
+// Operand shapes: hi/lo pairs are stacked so that one instruction covers several terms.
+//   -W S      A = [-W_hi; -W_lo] (M = 128: two 64-token halves), B = [S_hi | S_lo]
+//             (N = 64): rows 0-63 hold -W_hi S_hi and -W_hi S_lo, rows 64-127 -W_lo S_hi
+//             (and the negligible -W_lo S_lo); two issuers take k-steps 0-3 and 4-7
+//   T'' V     A = [T''_hi; T''_lo] (M = 128), B = V slice (N = 32)
+//   K^T Z     A = key tile (M = 128 keys), B = [Z_hi | Z_lo] (N = 64)
+//   Q' S      A = Q' (M = 64), B = [S_hi | S_lo]; P U_hi accumulates on top of its first
+//             32 columns, so the output is the sum of the two column halves
+// Warp roles (192 threads):
+//   warps 0-3  epilogue warpgroup: thread i holds key row i of the fp32 state slice in
+//              registers; forms U (rows 64-127 of the stacked products are folded into
+//              rows 0-63 through shared memory), Z = kd U, the new state and the
+//              outputs; lane 0 of warps 1-3 issues the products on the chain's critical
+//              path right after the step that enables them (no hand-off):
+//                after the state update: warps 1, 2 the k-step halves of -W S of the
+//                next chunk;  after U: warps 2, 3 the k-step halves of K^T Z.
+//   warp 4     TMEM owner; issues the products off the critical path: T'' V of the next
+//              chunk once -W S is done, P U_hi once U is formed, Q' S of the next chunk
+//              once the new state is written (Q' S and P U share an accumulator, so
+//              one thread issues both)
+//   warp 5     TMA producer
+// A chunk's inputs come through two 2-deep rings that are released at different points:
+//   ring A  -W hi/lo, T'' hi/lo (the first 48 KiB of the record) and the value slice
+//           (64B swizzle: the MN-major B operand of T'' V as loaded); free once -W S and
+//           T'' V of the chunk are done, so the next loads start early in the chunk
+//   ring B  key tile, P, Q' and the factor rows; free after the state update and P U
+constexpr int kChainThreads = 192;
+constexpr int kAW = 0, kAV = REC_P, kStageA = kAV + C * NV * 2;              // 52 KiB
+constexpr int kBK = 0, kBP = 16384, kBQ = kBP + (REC_QP - REC_P), kBF = kBP + (REC_F - REC_P),
+              kStageB = kBF + 8 * C * 4;                                     // 42 KiB
+static_assert(REC_WHI == 0 && REC_P == REC_T2LO + 8192 && REC_QP == REC_P + 8192 &&
+                  REC_F == REC_QP + 16384, "record layout");
 // shared memory map (bytes from a 1024-aligned base)
-constexpr int OFF_STAGE = 0;                               // [2]
-constexpr int OFF_S = OFF_STAGE + 2 * kStageBytes;         // S hi | lo   [128 keys][64B] MN-major
-constexpr int OFF_Z = OFF_S + 2 * 8192;                    // Z hi | lo   [64 tokens][64B] MN-major
-constexpr int OFF_U = OFF_Z + 2 * 4096;                    // U hi        [64 tokens][64B] MN-major
-constexpr int OFF_UF = OFF_U + 4096;                       // U fp32 [64][32] (states)
-constexpr int OFF_BAR = OFF_UF + C * NV * 4;
+constexpr int OFF_A = 0;                                   // [2] ring A
+constexpr int OFF_B = OFF_A + 2 * kStageA;                 // [2] ring B
+constexpr int OFF_S = OFF_B + 2 * kStageB;                 // [S_hi | S_lo] [128 keys][128B] MN-major
+constexpr int OFF_Z = OFF_S + 16384;                       // [Z_hi | Z_lo] [64 tokens][128B] MN-major
+constexpr int OFF_U = OFF_Z + 8192;                        // U_hi [64 tokens][64B] MN-major
+constexpr int LDX = NV + 4;                                // padded row: conflict-free float4
+constexpr int OFF_X = OFF_U + 4096;                        // fp32 [64][LDX]: rows 64-127 of the
+                                                           // stacked products, then U (states)
+constexpr int OFF_BAR = OFF_X + C * LDX * 4;
 constexpr int kChainSmem = OFF_BAR + 256 + 1024;
-static_assert(kStageBytes % 1024 == 0 && kStageRec % 1024 == 0, "swizzled operands need 1 KiB alignment");
+static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0 && kAV % 1024 == 0 && kBQ % 1024 == 0,
+              "swizzled operands need 1 KiB alignment");
 static_assert(kChainSmem <= 232448, "shared memory");
 
-// TMEM columns (M = 64 accumulators of N = 32 take 32 columns; D_S is M = 128)
-constexpr uint32_t TM_U0 = 0,     // D_U[2]: Ut + (-W_hi) S_hi, double-buffered
-                   TM_U2 = 64,    // (-W_lo) S_hi
-                   TM_U3 = 96,    // (-W_hi) S_lo
-                   TM_QS = 128,   // D_QS[2] = Q S_hi, double-buffered
-                   TM_S = 192,    // D_S = K^T Z
-                   TM_O = 224;    // D_O = P U_hi
-constexpr uint32_t kTmemCols = 256;
+// TMEM columns; M = 128 accumulators have row m in lane m, M = 64 ones row m in lane
+// 32 (m / 16) + m % 16
+constexpr uint32_t TM_WA = 0,     // -W S, k-steps 0-3   (M = 128, N = 64)
+                   TM_WB = 64,    // -W S, k-steps 4-7   (M = 128, N = 64)
+                   TM_UT = 128,   // T'' V [2]           (M = 128, N = 32 each)
+                   TM_S = 192,    // K^T Z, k-steps 0-1  (M = 128, N = 64)
+                   TM_S2 = 256,   // K^T Z, k-steps 2-3  (M = 128, N = 64)
+                   TM_O = 320;    // Q' S + P U_hi [2]   (M = 64, N = 64 each)
+constexpr uint32_t kTmemCols = 512;
 
-// barriers
+// barriers (arrival counts in brackets)
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_PRE_U, B_S_READY, B_D1, B_D1Q, B_D1R, B_QS,
-    B_E1, B_D2, B_DO, B_DRAIN1, B_DRAIN2, B_DRAIN3, B_COUNT
+    B_FULLA0 = 0, B_FULLA1,    // [1 + tx] ring A stage loaded
+    B_EMPTYA0, B_EMPTYA1,      // [1] ring A stage released
+    B_FULLB0, B_FULLB1,        // [1 + tx] ring B stage loaded
+    B_EMPTYB0, B_EMPTYB1,      // [2] ring B stage released (state update, P U done)
+    B_D1,                      // [3] both halves of -W S and T'' V of the chunk are done
+    B_D2,                      // [3] both halves of K^T Z and Q' S of the chunk are done
+    B_DO0, B_DO1,              // [1] P U_hi of a chunk using D_O[0] / D_O[1] is done (the
+                               // outputs of chunk c are read after P U of chunk c + 1 may
+                               // have finished, so each buffer has its own barrier)
+    B_E1DONE,                  // [1] Z and U_hi of the chunk are written
+    B_SREADY,                  // [1] the state operand for the next chunk is written
+    B_DRAIN,                   // [4] every MMA of every issuer is done (teardown)
+    B_COUNT
 };
 
 __device__ __forceinline__ uint32_t lane_base(int warp) { return (uint32_t)((warp & 3) * 32) << 16; }
 
+// AND of a predicate over the 128 threads of the epilogue warpgroup (named barrier 1)
+__device__ __forceinline__ bool wg_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// 32 fp32 values -> one 128-byte row [hi | lo] of a 128B-swizzled bf16 image
+__device__ __forceinline__ void store_row_hilo128(uint8_t *img, int row, const float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2_bf16(x[q * 8 + 2 * e], x[q * 8 + 2 * e + 1], h[e], l[e]);
+        *reinterpret_cast<uint4 *>(img + sw128_offset(row, q * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(img + sw128_offset(row, 64 + q * 16)) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
 template <bool STATES>
 __global__ void __launch_bounds__(kChainThreads, 1)
-chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
-             const __grid_constant__ CUtensorMap mapV, Params p) {
+chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+             Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t su = smem_u32(smem_raw);
     uint8_t *sm = smem_raw + (((su + 1023u) & ~1023u) - su);
@@ -512,31 +631,27 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     const int nch = sr.count;
 
     if (tid == 0) {
-        mbar_init(&bars[B_FULL0], 1);
-        mbar_init(&bars[B_FULL1], 1);
-        mbar_init(&bars[B_EMPTY0], 2);      // last MMA commit + epilogue warpgroup
-        mbar_init(&bars[B_EMPTY1], 2);
-        mbar_init(&bars[B_PRE_U], 1);
-        mbar_init(&bars[B_S_READY], 128);
-        mbar_init(&bars[B_D1], 1);
-        mbar_init(&bars[B_D1Q], 1);
-        mbar_init(&bars[B_D1R], 1);
-        mbar_init(&bars[B_QS], 1);
-        mbar_init(&bars[B_E1], 128);
-        mbar_init(&bars[B_D2], 1);
-        mbar_init(&bars[B_DO], 1);
-        mbar_init(&bars[B_DRAIN1], 1);
-        mbar_init(&bars[B_DRAIN2], 1);
-        mbar_init(&bars[B_DRAIN3], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[B_FULLA0 + b], 1);
+            mbar_init(&bars[B_EMPTYA0 + b], 1);
+            mbar_init(&bars[B_FULLB0 + b], 1);
+            mbar_init(&bars[B_EMPTYB0 + b], 2);
+        }
+        mbar_init(&bars[B_D1], 3);
+        mbar_init(&bars[B_D2], 3);
+        mbar_init(&bars[B_DO0], 1);
+        mbar_init(&bars[B_DO1], 1);
+        mbar_init(&bars[B_E1DONE], 1);
+        mbar_init(&bars[B_SREADY], 1);
+        mbar_init(&bars[B_DRAIN], 4);
         *s_err = 0;
         fence_mbar_init();
         if (nch > 0) {
             prefetch_tensormap(&mapK);
-            prefetch_tensormap(&mapQ);
             prefetch_tensormap(&mapV);
         }
     }
-    if (warp == 2) { tmem_alloc(tslot, kTmemCols); tmem_relinquish(); }
+    if (warp == 4) { tmem_alloc(tslot, kTmemCols); tmem_relinquish(); }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
@@ -545,167 +660,126 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         *s_err = 1;
         set_error(p, GDN_ERR_TIMEOUT);
     };
+    // single-thread wait (issuing lanes, producer)
     auto wait = [&](int b, uint32_t parity) -> bool {
         if (*s_err) return false;
         if (!mbar_wait(&bars[b], parity)) { fail(); return false; }
         return true;
     };
-    // Warpgroup-uniform wait: one elected thread polls, the warpgroup meets at a
-    // named barrier, and every thread takes the same decision from the error flag.
-    auto wg_wait = [&](int b, uint32_t parity, bool elected) -> bool {
-        if (elected && !*s_err && !mbar_wait(&bars[b], parity)) fail();
-        named_sync(1, 128);
-        return *s_err == 0;
+    // Epilogue-warpgroup wait: every thread polls the barrier itself, then one barrier
+    // reduction makes the outcome uniform (a timeout anywhere stops every thread).
+    auto wg_wait = [&](int b, uint32_t parity) -> bool {
+        bool ok = !*s_err;
+        if (ok && !mbar_wait(&bars[b], parity)) { fail(); ok = false; }
+        return wg_and(ok);
     };
-    // operand images of the state-dependent products
-    auto w_hi = [&](uint8_t *stg, int ks) { return smem_u32(stg + kStageRec + REC_WHI + ks * 2048); };
-    auto w_lo = [&](uint8_t *stg, int ks) { return smem_u32(stg + kStageRec + REC_WLO + ks * 2048); };
-    auto s_hi = [&](int ks) { return smem_u32(sm + OFF_S + ks * 1024); };
-    auto s_lo = [&](int ks) { return smem_u32(sm + OFF_S + 8192 + ks * 1024); };
-    // -W (A, M = 64 tokens, MN-major 128B swizzle) times S (B, N = 32, MN-major 64B swizzle)
-    constexpr uint32_t id_ws = instr_desc(64, NV, kFmtBF16, 1, 1);
-    auto mma_ws = [&](uint32_t d, uint32_t a, uint32_t b, bool acc) {
-        mma_bf16(d, smem_desc(a, 16, 1024, kSwizzle128B), smem_desc(b, 16, 512, kSwizzle64B), id_ws, acc);
+    auto ring_a = [&](int cc) { return sm + OFF_A + (cc & 1) * kStageA; };
+    auto ring_b = [&](int cc) { return sm + OFF_B + (cc & 1) * kStageB; };
+    const uint32_t s_img = smem_u32(sm + OFF_S), z_img = smem_u32(sm + OFF_Z);
+
+    // -W S of chunk cc from the state of chunk cc - 1, issued by lane 0 of epilogue warp
+    // w = 1 (k-steps 0-3) or 2 (k-steps 4-7); commit D1.
+    auto issue_ws = [&](int w, int cc) -> bool {
+        if (!wait(B_FULLA0 + (cc & 1), (cc >> 1) & 1)) return false;
+        tc_fence_after();
+        constexpr uint32_t id_ws = instr_desc(128, 64, kFmtBF16, 1, 1);
+        const uint32_t wa = smem_u32(ring_a(cc) + kAW + REC_WHI);
+        const uint32_t d = tmem + (w == 1 ? TM_WA : TM_WB);
+        const int k0 = (w - 1) * 4;
+#pragma unroll 1
+        for (int ks = k0; ks < k0 + 4; ++ks)
+            mma_bf16(d, smem_desc(wa + ks * 2048, REC_WLO - REC_WHI, 1024, kSwizzle128B),
+                     smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_ws, ks > k0);
+        mma_commit(&bars[B_D1]);
+        return true;
     };
 
-    if (warp == 0) {
+    if (warp == 5) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             for (int cc = 0; cc < nch; ++cc) {
                 const int st = cc & 1, u = cc >> 1;
-                if (u >= 1 && !wait(B_EMPTY0 + st, (u - 1) & 1)) break;
-                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
                 const int tok = (int)(sr.t0 + (int64_t)cc * C);
-                uint64_t *fb = &bars[B_FULL0 + st];
-                mbar_arrive_expect_tx(fb, kStageBytes);
-                tma_load_3d(stg + kStageK, &mapK, fb, 0, j, tok);
-                tma_load_3d(stg + kStageK + 8192, &mapK, fb, 64, j, tok);
-                tma_load_3d(stg + kStageQ, &mapQ, fb, 0, j, tok);
-                tma_load_3d(stg + kStageQ + 8192, &mapQ, fb, 64, j, tok);
-                tma_load_3d(stg + kStageV, &mapV, fb, vs * NV, h, tok);
-                bulk_load(stg + kStageRec,
-                          reinterpret_cast<const uint8_t *>(p.rec) +
-                              ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes,
-                          kRecBytes, fb);
+                const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.rec) +
+                                     ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes;
+                if (u >= 1 && !wait(B_EMPTYA0 + st, (u - 1) & 1)) break;
+                uint8_t *sa = ring_a(cc);
+                uint64_t *fa = &bars[B_FULLA0 + st];
+                mbar_arrive_expect_tx(fa, kStageA);
+                bulk_load(sa + kAW, rec, REC_P, fa);
+                tma_load_3d(sa + kAV, &mapV, fa, vs * NV, h, tok);
+                if (u >= 1 && !wait(B_EMPTYB0 + st, (u - 1) & 1)) break;
+                uint8_t *sb = ring_b(cc);
+                uint64_t *fb = &bars[B_FULLB0 + st];
+                mbar_arrive_expect_tx(fb, kStageB);
+                tma_load_3d(sb + kBK, &mapK, fb, 0, j, tok);
+                tma_load_3d(sb + kBK + 8192, &mapK, fb, 64, j, tok);
+                bulk_load(sb + kBP, rec + REC_P, kStageB - kBP, fb);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer 1
-        // (-W_hi) S_hi on top of Ut, then D_S = K^T Z and D_O = P U_hi
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ off-path products
         if (lane == 0) {
-            const uint32_t id_mma2 = instr_desc(128, NV, kFmtBF16, 1, 1);
-            const uint32_t id_mmao = instr_desc(64, NV, kFmtBF16, 0, 1);
-            bool issued = false;
-            for (int cc = 0; cc < nch; ++cc) {
-                const int st = cc & 1;
-                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-                if (!wait(B_FULL0 + st, (cc >> 1) & 1) || !wait(B_PRE_U, cc & 1) ||
-                    !wait(B_S_READY, cc & 1))
-                    break;
+            constexpr uint32_t id_u = instr_desc(128, NV, kFmtBF16, 0, 1);
+            constexpr uint32_t id_qs = instr_desc(64, 64, kFmtBF16, 0, 1);
+            constexpr uint32_t id_o = instr_desc(64, NV, kFmtBF16, 0, 1);
+            // T'' V of chunk c into D_UT[c % 2] (last read by the epilogue in chunk c - 2)
+            auto issue_tv = [&](int c) -> bool {
+                if (!wait(B_FULLA0 + (c & 1), (c >> 1) & 1)) return false;
                 tc_fence_after();
-                const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
+                uint8_t *sa = ring_a(c);
+                const uint32_t ta = smem_u32(sa + kAW + REC_T2HI), va = smem_u32(sa + kAV);
 #pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks) mma_ws(dU, w_hi(stg, ks), s_hi(ks), true);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + TM_UT + (uint32_t)((c & 1) * NV),
+                             smem_desc(ta + ks * 32, 16, 1024, kSwizzle128B),
+                             smem_desc(va + ks * 1024, 16, 512, kSwizzle64B), id_u, ks > 0);
                 mma_commit(&bars[B_D1]);
-                issued = true;
-                if (!wait(B_E1, cc & 1)) break;
+                return true;
+            };
+            // Q' S of chunk c into D_O[c % 2] (last read by the epilogue's output of chunk
+            // c - 2, done before the state of chunk c - 1 was written)
+            auto issue_qs = [&](int c) -> bool {
+                if (!wait(B_SREADY, c & 1) || !wait(B_FULLB0 + (c & 1), (c >> 1) & 1)) return false;
                 tc_fence_after();
-                // D_S = K^T (Z hi + Z lo)   (A = key tile, MN-major)
+                const uint32_t qa = smem_u32(ring_b(c) + kBQ);
+                const uint32_t d = tmem + TM_O + (uint32_t)((c & 1) * 64);
 #pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ka = smem_u32(stg + kStageK + ks * 2048);
-                    const uint32_t zh = smem_u32(sm + OFF_Z + ks * 1024);
-                    mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh, 16, 512, kSwizzle64B), id_mma2, ks > 0);
-                    mma_bf16(tmem + TM_S, smem_desc(ka, 8192, 1024, kSwizzle128B), smem_desc(zh + 4096, 16, 512, kSwizzle64B), id_mma2, 1);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(d, smem_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
+                             smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_qs, ks > 0);
                 mma_commit(&bars[B_D2]);
-                // D_O = P U_hi (outputs only: one bf16 term)
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ph = smem_u32(stg + kStageRec + REC_P + ks * 32);
-                    const uint32_t uh = smem_u32(sm + OFF_U + ks * 1024);
-                    mma_bf16(tmem + TM_O, smem_desc(ph, 16, 1024, kSwizzle128B), smem_desc(uh, 16, 512, kSwizzle64B), id_mmao, ks > 0);
-                }
-                mma_commit(&bars[B_DO]);
-                mma_commit(&bars[B_EMPTY0 + st]);
-            }
-            if (issued) {   // let every MMA of this thread finish before teardown
-                mma_commit(&bars[B_DRAIN1]);
-                mbar_wait(&bars[B_DRAIN1], 0);
-            }
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ MMA issuer 2
-        // (-W_lo) S_hi, then D_QS = Q S_hi (outputs only: one bf16 term, ~20x inside the
-        // output tolerance), which no step of the chain waits for
-        if (lane == 0) {
-            const uint32_t id_qs = instr_desc(64, NV, kFmtBF16, 0, 1);
+                return true;
+            };
             bool issued = false;
             for (int cc = 0; cc < nch; ++cc) {
-                const int st = cc & 1;
-                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-                if (!wait(B_FULL0 + st, (cc >> 1) & 1) || !wait(B_S_READY, cc & 1)) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks) mma_ws(tmem + TM_U2, w_lo(stg, ks), s_hi(ks), ks > 0);
-                mma_commit(&bars[B_D1Q]);
+                if (cc == 0 && (!issue_tv(0) || !issue_qs(0))) break;
                 issued = true;
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int kb = ks >> 2, ko = (ks & 3) * 32;
-                    const uint32_t qa = smem_u32(stg + kStageQ + kb * 8192 + ko);
-                    mma_bf16(tmem + TM_QS + (uint32_t)(st * NV), smem_desc(qa, 16, 1024, kSwizzle128B),
-                             smem_desc(s_hi(ks), 16, 512, kSwizzle64B), id_qs, ks > 0);
-                }
-                mma_commit(&bars[B_QS]);
-            }
-            if (issued) {
-                mma_commit(&bars[B_DRAIN2]);
-                mbar_wait(&bars[B_DRAIN2], 0);
-            }
-        }
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ MMA issuer 3
-        // Ut = T'' V into D_U[cc % 2] once the previous chunk's D_S is done (so that it
-        // does not delay that product), then (-W_hi) S_lo
-        if (lane == 0) {
-            const uint32_t id_u = instr_desc(64, NV, kFmtBF16, 0, 1);
-            bool issued = false;
-            for (int cc = 0; cc < nch; ++cc) {
-                const int st = cc & 1;
-                uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-                if (!wait(B_FULL0 + st, (cc >> 1) & 1)) break;
-                // D_U[cc % 2] was last read by the epilogue in chunk cc - 2, before it let
-                // the products of chunk cc - 1 start
-                if (cc >= 1 && !wait(B_D2, (cc - 1) & 1)) break;
+                if (cc + 1 < nch && (!wait(B_D1, cc & 1) || !issue_tv(cc + 1))) break;
+                // P U_hi on top of Q' S (outputs only: one bf16 term)
+                if (!wait(B_E1DONE, cc & 1)) break;
                 tc_fence_after();
-                const uint32_t dU = tmem + TM_U0 + (uint32_t)(st * NV);
+                {
+                    const uint32_t pa = smem_u32(ring_b(cc) + kBP), ub = smem_u32(sm + OFF_U);
 #pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t ta = smem_u32(stg + kStageRec + REC_T2HI + ks * 32);
-                    const uint64_t vb = smem_desc(smem_u32(stg + kStageV + ks * 1024), 16, 512, kSwizzle64B);
-                    mma_bf16(dU, smem_desc(ta, 16, 1024, kSwizzle128B), vb, id_u, ks > 0);
-                    mma_bf16(dU, smem_desc(ta + 8192, 16, 1024, kSwizzle128B), vb, id_u, 1);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem + TM_O + (uint32_t)((cc & 1) * 64), smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B),
+                                 smem_desc(ub + ks * 1024, 16, 512, kSwizzle64B), id_o, 1);
+                    mma_commit(&bars[B_DO0 + (cc & 1)]);
+                    mma_commit(&bars[B_EMPTYB0 + (cc & 1)]);
                 }
-                mma_commit(&bars[B_PRE_U]);
-                issued = true;
-                if (!wait(B_S_READY, cc & 1)) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks) mma_ws(tmem + TM_U3, w_hi(stg, ks), s_lo(ks), ks > 0);
-                mma_commit(&bars[B_D1R]);
+                if (cc + 1 < nch && !issue_qs(cc + 1)) break;
             }
-            if (issued) {
-                mma_commit(&bars[B_DRAIN3]);
-                mbar_wait(&bars[B_DRAIN3], 0);
-            }
+            if (issued) mma_commit(&bars[B_DRAIN]);
+            else mbar_arrive(&bars[B_DRAIN]);
         }
     } else {
         // ------------------------------------------------------------ epilogue warpgroup
-        const int i = tid - 128;            // key row of the state slice
+        const int i = tid;                  // key row of the state slice / row of the
+                                            // M = 128 results
         const bool lead = (i == 0);
         const uint32_t lb = lane_base(warp);
-        const int ew = warp & 3;
+        const int tq = warp * 16 + (lane & 15);    // token row of the M = 64 results
         float S[NV];
         const size_t sbase = (((size_t)s * p.HV + h) * D + i) * D + (size_t)vs * NV;
         if (p.s0) {
@@ -718,85 +792,159 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll
             for (int q = 0; q < NV; ++q) S[q] = 0.f;
         }
-        // S hi/lo operands: row i (this thread's key) of the MN-major 64B-swizzled images
-        auto write_state_operand = [&]() {
-#pragma unroll
-            for (int q = 0; q < NV / 8; ++q) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) split2_bf16(S[8 * q + 2 * e], S[8 * q + 2 * e + 1], hw[e], lw[e]);
-                const uint32_t off = sw64_offset(i, q * 16);
-                *reinterpret_cast<uint4 *>(sm + OFF_S + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_S + 8192 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
+        float *xf = reinterpret_cast<float *>(sm + OFF_X);
+        float kd = 0.f, gl = 0.f;           // factors of the current chunk
+        auto load_factors = [&](int cc) -> bool {
+            if (!wg_wait(B_FULLB0 + (cc & 1), (cc >> 1) & 1)) return false;
+            const float *F = reinterpret_cast<const float *>(ring_b(cc) + kBF);
+            kd = F[SC_KD * C + (i & 63)];
+            gl = F[SC_MISC * C + 0];
+            return true;
         };
-        write_state_operand();
+        // outputs of chunk c: O = D_O[:, 0:32] + D_O[:, 32:64] (M = 64 layout)
+        auto output = [&](int c) -> bool {
+            if (!wg_wait(B_DO0 + (c & 1), (c >> 1) & 1)) return false;
+            tc_fence_after();
+            float o1[NV], o2[NV];
+            tmem_ld32(tmem + lb + TM_O + (uint32_t)((c & 1) * 64), o1);
+            tmem_ld32(tmem + lb + TM_O + (uint32_t)((c & 1) * 64) + 32, o2);
+            tmem_ld_wait();
+            const int64_t t0c = sr.t0 + (int64_t)c * C;
+            if (lane < 16 && t0c + tq < sr.t_end) {
+                __nv_bfloat16 *dst = p.out + ((size_t)(t0c + tq) * p.HV + h) * D + (size_t)vs * NV;
+#pragma unroll
+                for (int q = 0; q < NV; q += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack2(__float2bfloat16_rn(o1[q + 2 * e] + o2[q + 2 * e]),
+                                     __float2bfloat16_rn(o1[q + 2 * e + 1] + o2[q + 2 * e + 1]));
+                    *reinterpret_cast<uint4 *>(dst + q) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            tc_fence_before();
+            return true;
+        };
+        store_row_hilo128(sm + OFF_S, i, S);
         fence_async_smem();
-        mbar_arrive(&bars[B_S_READY]);
-        float *uf = reinterpret_cast<float *>(sm + OFF_UF);
-        const int tq = ew * 16 + (lane & 15);      // token row of the M = 64 results
-        for (int cc = 0; cc < nch; ++cc) {
-            const int st = cc & 1, u = cc >> 1;
-            uint8_t *stg = sm + OFF_STAGE + st * kStageBytes;
-            const float *F = reinterpret_cast<const float *>(stg + kStageRec + REC_F);
+        named_sync(1, 128);
+        if (lead) mbar_arrive(&bars[B_SREADY]);
+        bool issued = false;                // this lane has issued tensor-core work
+        bool run = nch > 0 && load_factors(0);
+        if (run && lane == 0 && (warp == 1 || warp == 2)) {
+            if (!issue_ws(warp, 0)) fail();
+            issued = true;
+        }
+        __syncwarp();
+        int done = 0;                       // chunks whose outputs are written
+        for (int cc = 0; cc < nch && run; ++cc) {
+            const int st = cc & 1;
+            uint8_t *sb = ring_b(cc);
             const int64_t tok0 = sr.t0 + (int64_t)cc * C;
             const int len = (int)min((int64_t)C, sr.t_end - tok0);
-            if (!wg_wait(B_FULL0 + st, u & 1, lead)) break;
-            const float qd = F[SC_QD * C + tq], kd = F[SC_KD * C + tq];
-            if (!wg_wait(B_D1, cc & 1, lead) || !wg_wait(B_D1Q, cc & 1, lead) ||
-                !wg_wait(B_D1R, cc & 1, lead))
-                break;
+            // ---- E1: U = rows 0-63 + rows 64-127 of (-W S + T'' V), Z = kd U
+            if (!wg_wait(B_D1, cc & 1)) break;
+            if (lead) mbar_arrive(&bars[B_EMPTYA0 + st]);   // ring A of chunk cc is consumed
             tc_fence_after();
-            // E1: U = D_U + D_U2 + D_U3 (M = 64 layout: row tq in lanes 0-15)
+            float uu[NV];
             {
-                float uu[NV], u2[NV], u3[NV];
-                tmem_ld32(tmem + lb + TM_U0 + (uint32_t)(st * NV), uu);
-                tmem_ld32(tmem + lb + TM_U2, u2);
-                tmem_ld32(tmem + lb + TM_U3, u3);
+                float a[NV], b[NV];
+                tmem_ld32(tmem + lb + TM_WA, uu);
+                tmem_ld32(tmem + lb + TM_WA + 32, a);
+                tmem_ld32(tmem + lb + TM_WB, b);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) uu[c] += u2[c] + u3[c];
-                if (lane < 16) {
-                    // row tq of the MN-major 64B-swizzled Z (hi, lo) and U (hi) operands
+                for (int c = 0; c < NV; ++c) uu[c] += a[c] + b[c];
+                tmem_ld32(tmem + lb + TM_WB + 32, a);
+                tmem_ld32(tmem + lb + TM_UT + (uint32_t)(st * NV), b);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < NV / 8; ++q) {
-                        uint32_t zh[4], zl[4], uh[4];
+                for (int c = 0; c < NV; ++c) uu[c] += a[c] + b[c];
+            }
+            if (i >= 64) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 8 * q + 2 * e;
-                            split2_bf16(kd * uu[c], kd * uu[c + 1], zh[e], zl[e]);
-                            const __nv_bfloat162 u2v = __floats2bfloat162_rn(uu[c], uu[c + 1]);
-                            uh[e] = *reinterpret_cast<const uint32_t *>(&u2v);
-                        }
-                        const uint32_t off = sw64_offset(tq, q * 16);
-                        *reinterpret_cast<uint4 *>(sm + OFF_Z + off) = make_uint4(zh[0], zh[1], zh[2], zh[3]);
-                        *reinterpret_cast<uint4 *>(sm + OFF_Z + 4096 + off) = make_uint4(zl[0], zl[1], zl[2], zl[3]);
-                        *reinterpret_cast<uint4 *>(sm + OFF_U + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+                for (int c = 0; c < NV; c += 4)
+                    *reinterpret_cast<float4 *>(xf + (i - 64) * LDX + c) = make_float4(uu[c], uu[c + 1], uu[c + 2], uu[c + 3]);
+            }
+            named_sync(1, 128);
+            if (i < 64) {
+                // token i: its U row, Z = kd U as [Z_hi | Z_lo], U_hi for P U
+#pragma unroll
+                for (int c = 0; c < NV; c += 4) {
+                    const float4 x4 = *reinterpret_cast<const float4 *>(xf + i * LDX + c);
+                    uu[c] += x4.x; uu[c + 1] += x4.y; uu[c + 2] += x4.z; uu[c + 3] += x4.w;
+                }
+                if (STATES) {
+#pragma unroll
+                    for (int c = 0; c < NV; c += 4)
+                        *reinterpret_cast<float4 *>(xf + i * LDX + c) = make_float4(uu[c], uu[c + 1], uu[c + 2], uu[c + 3]);
+                }
+                float z[NV];
+#pragma unroll
+                for (int c = 0; c < NV; ++c) z[c] = kd * uu[c];
+                store_row_hilo128(sm + OFF_Z, i, z);
+#pragma unroll
+                for (int q = 0; q < NV / 8; ++q) {
+                    uint32_t uh[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 u2v = __floats2bfloat162_rn(uu[8 * q + 2 * e], uu[8 * q + 2 * e + 1]);
+                        uh[e] = *reinterpret_cast<const uint32_t *>(&u2v);
                     }
-                    if (STATES) {
-#pragma unroll
-                        for (int c = 0; c < NV; c += 4)
-                            *reinterpret_cast<float4 *>(uf + tq * NV + c) =
-                                make_float4(uu[c], uu[c + 1], uu[c + 2], uu[c + 3]);
-                    }
+                    *reinterpret_cast<uint4 *>(sm + OFF_U + sw64_offset(i, q * 16)) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
                 }
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars[B_E1]);
-            // E2: new state (thread i = key row i); Q S_hi must have read the old state
-            if (!wg_wait(B_D2, cc & 1, lead) || !wg_wait(B_QS, cc & 1, lead)) break;
+            named_sync(1, 128);                 // Z, U (and the U rows for the states) complete
+            if (lead) mbar_arrive(&bars[B_E1DONE]);
+            if (lane == 0 && (warp == 2 || warp == 3)) {
+                // K^T [Z_hi | Z_lo]: A = key tile read MN-major; k-steps 0-1 / 2-3
+                tc_fence_after();
+                constexpr uint32_t id_kz = instr_desc(128, 64, kFmtBF16, 1, 1);
+                const uint32_t ka = smem_u32(sb + kBK);
+                const int k0 = (warp - 2) * 2;
+                const uint32_t d = tmem + (warp == 2 ? TM_S : TM_S2);
+#pragma unroll 1
+                for (int ks = k0; ks < k0 + 2; ++ks)
+                    mma_bf16(d, smem_desc(ka + ks * 2048, 8192, 1024, kSwizzle128B),
+                             smem_desc(z_img + ks * 2048, 16, 1024, kSwizzle128B), id_kz, ks > k0);
+                mma_commit(&bars[B_D2]);
+                issued = true;
+            }
+            __syncwarp();
+            // the previous chunk's outputs while K^T Z runs
+            if (cc >= 1) {
+                if (!output(cc - 1)) break;
+                done = cc;
+            }
+            // ---- E2: new state (thread i = key row i)
+            if (!wg_wait(B_D2, cc & 1)) break;
             tc_fence_after();
             float ds[NV];
-            tmem_ld32(tmem + lb + TM_S, ds);
-            tmem_ld_wait();
-            const float gl = F[SC_MISC * C + 0];
-            if (STATES) {
-                const uint8_t *ktile = stg + kStageK + (i >> 6) * 8192;
-                const uint32_t kbyte = (uint32_t)(i & 63) * 2;
-                float run[NV];
+            {
+                float d2[NV];
+                tmem_ld32(tmem + lb + TM_S, ds);
+                tmem_ld32(tmem + lb + TM_S + 32, d2);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) run[c] = S[c];
+                for (int c = 0; c < NV; ++c) ds[c] += d2[c];
+                tmem_ld32(tmem + lb + TM_S2, d2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < NV; ++c) ds[c] += d2[c];
+                tmem_ld32(tmem + lb + TM_S2 + 32, d2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < NV; ++c) ds[c] += d2[c];
+            }
+            if (STATES) {
+                const float *F = reinterpret_cast<const float *>(sb + kBF);
+                const uint8_t *ktile = sb + kBK + (i >> 6) * 8192;
+                const uint32_t kbyte = (uint32_t)(i & 63) * 2;
+                float rs[NV];
+#pragma unroll
+                for (int c = 0; c < NV; ++c) rs[c] = S[c];
                 for (int t = 0; t < len; ++t) {
                     const float kt = __bfloat162float(
                         *reinterpret_cast<const __nv_bfloat16 *>(ktile + sw128_offset(t, kbyte)));
@@ -805,49 +953,44 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     const bool last = (t == len - 1);
 #pragma unroll
                     for (int c = 0; c < NV; c += 4) {
-                        const float4 u4 = *reinterpret_cast<const float4 *>(uf + t * NV + c);
-                        run[c] = al * run[c] + f * u4.x;
-                        run[c + 1] = al * run[c + 1] + f * u4.y;
-                        run[c + 2] = al * run[c + 2] + f * u4.z;
-                        run[c + 3] = al * run[c + 3] + f * u4.w;
+                        const float4 u4 = *reinterpret_cast<const float4 *>(xf + t * LDX + c);
+                        rs[c] = al * rs[c] + f * u4.x;
+                        rs[c + 1] = al * rs[c + 1] + f * u4.y;
+                        rs[c + 2] = al * rs[c + 2] + f * u4.z;
+                        rs[c + 3] = al * rs[c + 3] + f * u4.w;
                         const float4 o4 = last
                             ? make_float4(gl * S[c] + ds[c], gl * S[c + 1] + ds[c + 1],
                                           gl * S[c + 2] + ds[c + 2], gl * S[c + 3] + ds[c + 3])
-                            : make_float4(run[c], run[c + 1], run[c + 2], run[c + 3]);
+                            : make_float4(rs[c], rs[c + 1], rs[c + 2], rs[c + 3]);
                         __stcs(reinterpret_cast<float4 *>(dst + c), o4);
                     }
                 }
             }
 #pragma unroll
             for (int c = 0; c < NV; ++c) S[c] = gl * S[c] + ds[c];
-            write_state_operand();
+            store_row_hilo128(sm + OFF_S, i, S);
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars[B_S_READY]);   // the next chunk's products may start now
-            // outputs, off the chain's critical path: O = qd * (Q S_hi) + P U_hi
-            if (!wg_wait(B_DO, cc & 1, lead)) break;
-            tc_fence_after();
-            {
-                float dov[NV], qs[NV];
-                tmem_ld32(tmem + lb + TM_O, dov);
-                tmem_ld32(tmem + lb + TM_QS + (uint32_t)(st * NV), qs);
-                tmem_ld_wait();
-                if (lane < 16 && tq < len) {
-                    __nv_bfloat16 *dst = p.out + ((size_t)(tok0 + tq) * p.HV + h) * D + (size_t)vs * NV;
-#pragma unroll
-                    for (int c = 0; c < NV; c += 8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack2(__float2bfloat16_rn(qd * qs[c + 2 * e] + dov[c + 2 * e]),
-                                         __float2bfloat16_rn(qd * qs[c + 2 * e + 1] + dov[c + 2 * e + 1]));
-                        *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
+            named_sync(1, 128);                 // the new state operand is complete
+            if (lead) {
+                mbar_arrive(&bars[B_EMPTYB0 + st]);   // (with the P U commit)
+                mbar_arrive(&bars[B_SREADY]);
             }
-            tc_fence_before();
-            named_sync(1, 128);              // every reader of the stage and of uf is done
-            if (lead) mbar_arrive(&bars[B_EMPTY0 + st]);
+            if (cc + 1 < nch && lane == 0 && (warp == 1 || warp == 2)) {
+                if (!issue_ws(warp, cc + 1)) fail();
+                issued = true;
+            }
+            __syncwarp();
+            if (cc + 1 < nch && !load_factors(cc + 1)) break;
+            if (cc + 1 == nch) {
+                if (!output(cc)) break;
+                done = nch;
+            }
+        }
+        (void)done;
+        if (lane == 0 && warp >= 1) {
+            if (issued) mma_commit(&bars[B_DRAIN]);
+            else mbar_arrive(&bars[B_DRAIN]);
         }
         // final state slice
         if (!*s_err) {
@@ -856,10 +999,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 reinterpret_cast<float4 *>(p.s_final + sbase)[q] =
                     make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
         }
+        if (lead) mbar_wait(&bars[B_DRAIN], 0);   // every MMA of the CTA has finished
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 4) tmem_dealloc(tmem, kTmemCols);
 }
 // ================================================================== host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -937,7 +1081,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kChainSmem)) != cudaSuccess)
             return e;
-        kern<<<dim3(D / NV, pp.HV, pp.N), kChainThreads, kChainSmem, st>>>(mk, mq, mv, p);
+        kern<<<dim3(D / NV, pp.HV, pp.N), kChainThreads, kChainSmem, st>>>(mk, mv, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
