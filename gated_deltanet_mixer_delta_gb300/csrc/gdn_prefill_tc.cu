@@ -18,12 +18,13 @@
 //           blocks, then block rows), W^T = K^T T'^T on the tensor core, P; writes -W
 //           (hi/lo), T'' (hi/lo) and P as operand images, and the per-token factors.
 //  chain -- one CTA per (sequence, value head, 32-wide value slice), the sequential
-//           chunk loop, warp-specialised (192 threads): a TMA producer warp, a warp that
-//           issues T'' V one chunk ahead, and an epilogue warpgroup that holds the fp32
-//           state slice in registers (thread i = key row i), forms U, Z = kd U, the new
-//           state and the outputs (and the per-token states when asked), and issues the
-//           tensor-core products that follow each of its steps itself.  Hi/lo operand
-//           pairs are stacked along M or N so that one instruction covers several terms.
+//           chunk loop, warp-specialised (256 threads): a TMA producer warp, a warp that
+//           issues the products off the chain's critical path, two output warps, and an
+//           epilogue warpgroup that holds the fp32 state slice in registers (thread i =
+//           key row i), forms U, Z = kd U and the new state (and the per-token states
+//           when asked), and issues the products on the critical path itself.  Hi/lo
+//           operand pairs are stacked along M or N so that one instruction covers several
+//           terms.
 // All waits are bounded; a timeout sets GDN_ERR_TIMEOUT in the status word and the CTA
 // drains and exits.
 #include <string.h>
@@ -514,56 +515,61 @@ teardown:
 //             (N = 64): rows 0-63 hold -W_hi S_hi and -W_hi S_lo, rows 64-127 -W_lo S_hi
 //             (and the negligible -W_lo S_lo); two issuers take k-steps 0-3 and 4-7
 //   T'' V     A = [T''_hi; T''_lo] (M = 128), B = V slice (N = 32)
-//   K^T Z     A = key tile (M = 128 keys), B = [Z_hi | Z_lo] (N = 64)
-//   Q' S      A = Q' (M = 64), B = [S_hi | S_lo]; P U_hi accumulates on top of its first
-//             32 columns, so the output is the sum of the two column halves
-// Warp roles (192 threads):
+//   K^T Z     A = key tile (M = 128 keys), B = [Z_hi | Z_lo] (N = 64); two issuers take
+//             k-steps 0-1 and 2-3
+//   Q' S      A = [any; Q'] (M = 128, the operand read from 8 KiB before Q', so that the
+//             64 live rows land in TMEM lanes 64-127), B = [S_hi | S_lo]; P U_hi (A read
+//             the same way) accumulates on top of its first 32 columns, so an output row
+//             is the sum of the two column halves
+// Warp roles (256 threads):
 //   warps 0-3  epilogue warpgroup: thread i holds key row i of the fp32 state slice in
-//              registers; forms U (rows 64-127 of the stacked products are folded into
-//              rows 0-63 through shared memory), Z = kd U, the new state and the
-//              outputs; lane 0 of warps 1-3 issues the products on the chain's critical
-//              path right after the step that enables them (no hand-off):
-//                after the state update: warps 1, 2 the k-step halves of -W S of the
-//                next chunk;  after U: warps 2, 3 the k-step halves of K^T Z.
-//   warp 4     TMEM owner; issues the products off the critical path: T'' V of the next
-//              chunk once -W S is done, P U_hi once U is formed, Q' S of the next chunk
-//              once the new state is written (Q' S and P U share an accumulator, so
-//              one thread issues both)
+//              registers; forms U (the two token halves of the stacked products are
+//              combined through shared memory, each thread finishing 16 columns of one
+//              token), Z = kd U and the new state; lane 0 of warps 1-3 issues the
+//              products on the chain's critical path right after the step that enables
+//              them (no hand-off): after the state update warps 1, 2 the k-step halves
+//              of -W S of the next chunk, after U warps 2, 3 the k-step halves of K^T Z.
+//   warp 4     TMEM owner; issues the products off the critical path: once U of chunk
+//              cc is formed, P U_hi of chunk cc and T'' V of chunk cc + 1; once the new
+//              state is written, Q' S of chunk cc + 1 (Q' S and P U share an accumulator,
+//              so one thread issues both)
 //   warp 5     TMA producer
+//   warps 6-7  output warps: read rows 64-127 of D_O (TMEM lanes 64-127, one token per
+//              thread) and write the outputs
 // A chunk's inputs come through two 2-deep rings that are released at different points:
 //   ring A  -W hi/lo, T'' hi/lo (the first 48 KiB of the record) and the value slice
 //           (64B swizzle: the MN-major B operand of T'' V as loaded); free once -W S and
 //           T'' V of the chunk are done, so the next loads start early in the chunk
 //   ring B  key tile, P, Q' and the factor rows; free after the state update and P U
-constexpr int kChainThreads = 192;
+constexpr int kChainThreads = 256;
 constexpr int kAW = 0, kAV = REC_P, kStageA = kAV + C * NV * 2;              // 52 KiB
 constexpr int kBK = 0, kBP = 16384, kBQ = kBP + (REC_QP - REC_P), kBF = kBP + (REC_F - REC_P),
               kStageB = kBF + 8 * C * 4;                                     // 42 KiB
 static_assert(REC_WHI == 0 && REC_P == REC_T2LO + 8192 && REC_QP == REC_P + 8192 &&
                   REC_F == REC_QP + 16384, "record layout");
+static_assert(kBP >= 8192 && kBQ >= 8192, "the stacked output operands read 8 KiB before P and Q'");
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int OFF_A = 0;                                   // [2] ring A
 constexpr int OFF_B = OFF_A + 2 * kStageA;                 // [2] ring B
 constexpr int OFF_S = OFF_B + 2 * kStageB;                 // [S_hi | S_lo] [128 keys][128B] MN-major
 constexpr int OFF_Z = OFF_S + 16384;                       // [Z_hi | Z_lo] [64 tokens][128B] MN-major
 constexpr int OFF_U = OFF_Z + 8192;                        // U_hi [64 tokens][64B] MN-major
-constexpr int LDX = NV + 4;                                // padded row: conflict-free float4
-constexpr int OFF_X = OFF_U + 4096;                        // fp32 [64][LDX]: rows 64-127 of the
-                                                           // stacked products, then U (states)
-constexpr int OFF_BAR = OFF_X + C * LDX * 4;
+constexpr int OFF_X = OFF_U + 4096;                        // fp32 [2][64][16] half-row exchange
+                                                           // (16-byte chunks XOR-swizzled), then
+                                                           // U rows [64][32] for the states
+constexpr int OFF_BAR = OFF_X + C * NV * 4;
 constexpr int kChainSmem = OFF_BAR + 256 + 1024;
 static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0 && kAV % 1024 == 0 && kBQ % 1024 == 0,
               "swizzled operands need 1 KiB alignment");
 static_assert(kChainSmem <= 232448, "shared memory");
 
-// TMEM columns; M = 128 accumulators have row m in lane m, M = 64 ones row m in lane
-// 32 (m / 16) + m % 16
-constexpr uint32_t TM_WA = 0,     // -W S, k-steps 0-3   (M = 128, N = 64)
-                   TM_WB = 64,    // -W S, k-steps 4-7   (M = 128, N = 64)
-                   TM_UT = 128,   // T'' V [2]           (M = 128, N = 32 each)
-                   TM_S = 192,    // K^T Z, k-steps 0-1  (M = 128, N = 64)
-                   TM_S2 = 256,   // K^T Z, k-steps 2-3  (M = 128, N = 64)
-                   TM_O = 320;    // Q' S + P U_hi [2]   (M = 64, N = 64 each)
+// TMEM columns; M = 128 accumulators have row m in lane m
+constexpr uint32_t TM_WA = 0,     // -W S, k-steps 0-3   (N = 64)
+                   TM_WB = 64,    // -W S, k-steps 4-7   (N = 64)
+                   TM_UT = 128,   // T'' V [2]           (N = 32 each)
+                   TM_S = 192,    // K^T Z, k-steps 0-1  (N = 64)
+                   TM_S2 = 256,   // K^T Z, k-steps 2-3  (N = 64)
+                   TM_O = 320;    // Q' S + P U_hi [2]   (N = 64 each; rows 64-127 live)
 constexpr uint32_t kTmemCols = 512;
 
 // barriers (arrival counts in brackets)
@@ -574,9 +580,8 @@ enum {
     B_EMPTYB0, B_EMPTYB1,      // [2] ring B stage released (state update, P U done)
     B_D1,                      // [3] both halves of -W S and T'' V of the chunk are done
     B_D2,                      // [3] both halves of K^T Z and Q' S of the chunk are done
-    B_DO0, B_DO1,              // [1] P U_hi of a chunk using D_O[0] / D_O[1] is done (the
-                               // outputs of chunk c are read after P U of chunk c + 1 may
-                               // have finished, so each buffer has its own barrier)
+    B_DO0, B_DO1,              // [1] P U_hi into D_O[0] / D_O[1] is done
+    B_OUT0, B_OUT1,            // [2] the output warps have read D_O[0] / D_O[1]
     B_E1DONE,                  // [1] Z and U_hi of the chunk are written
     B_SREADY,                  // [1] the state operand for the next chunk is written
     B_DRAIN,                   // [4] every MMA of every issuer is done (teardown)
@@ -611,6 +616,10 @@ __device__ __forceinline__ void store_row_hilo128(uint8_t *img, int row, const f
     }
 }
 
+// float offset of 16-byte chunk c (0-3) of row t in a [64][16] fp32 block whose chunks
+// are XOR-swizzled so that eight consecutive rows hit eight different bank groups
+__device__ __forceinline__ int xchg_off(int t, int c) { return t * 16 + ((c ^ ((t >> 1) & 3)) << 2); }
+
 template <bool STATES>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -636,11 +645,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             mbar_init(&bars[B_EMPTYA0 + b], 1);
             mbar_init(&bars[B_FULLB0 + b], 1);
             mbar_init(&bars[B_EMPTYB0 + b], 2);
+            mbar_init(&bars[B_DO0 + b], 1);
+            mbar_init(&bars[B_OUT0 + b], 2);
         }
         mbar_init(&bars[B_D1], 3);
         mbar_init(&bars[B_D2], 3);
-        mbar_init(&bars[B_DO0], 1);
-        mbar_init(&bars[B_DO1], 1);
         mbar_init(&bars[B_E1DONE], 1);
         mbar_init(&bars[B_SREADY], 1);
         mbar_init(&bars[B_DRAIN], 4);
@@ -665,13 +674,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         if (*s_err) return false;
         if (!mbar_wait(&bars[b], parity)) { fail(); return false; }
         return true;
-    };
-    // Epilogue-warpgroup wait: every thread polls the barrier itself, then one barrier
-    // reduction makes the outcome uniform (a timeout anywhere stops every thread).
-    auto wg_wait = [&](int b, uint32_t parity) -> bool {
-        bool ok = !*s_err;
-        if (ok && !mbar_wait(&bars[b], parity)) { fail(); ok = false; }
-        return wg_and(ok);
     };
     auto ring_a = [&](int cc) { return sm + OFF_A + (cc & 1) * kStageA; };
     auto ring_b = [&](int cc) { return sm + OFF_B + (cc & 1) * kStageB; };
@@ -721,8 +723,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         // ------------------------------------------------------------ off-path products
         if (lane == 0) {
             constexpr uint32_t id_u = instr_desc(128, NV, kFmtBF16, 0, 1);
-            constexpr uint32_t id_qs = instr_desc(64, 64, kFmtBF16, 0, 1);
-            constexpr uint32_t id_o = instr_desc(64, NV, kFmtBF16, 0, 1);
+            constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
+            constexpr uint32_t id_o = instr_desc(128, NV, kFmtBF16, 0, 1);
             // T'' V of chunk c into D_UT[c % 2] (last read by the epilogue in chunk c - 2)
             auto issue_tv = [&](int c) -> bool {
                 if (!wait(B_FULLA0 + (c & 1), (c >> 1) & 1)) return false;
@@ -737,12 +739,13 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 mma_commit(&bars[B_D1]);
                 return true;
             };
-            // Q' S of chunk c into D_O[c % 2] (last read by the epilogue's output of chunk
-            // c - 2, done before the state of chunk c - 1 was written)
+            // Q' S of chunk c into D_O[c % 2] once the state operand of chunk c - 1 is
+            // written and the output warps have read the outputs of chunk c - 2
             auto issue_qs = [&](int c) -> bool {
                 if (!wait(B_SREADY, c & 1) || !wait(B_FULLB0 + (c & 1), (c >> 1) & 1)) return false;
+                if (c >= 2 && !wait(B_OUT0 + (c & 1), ((c - 2) >> 1) & 1)) return false;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(ring_b(c) + kBQ);
+                const uint32_t qa = smem_u32(ring_b(c) + kBQ - 8192);
                 const uint32_t d = tmem + TM_O + (uint32_t)((c & 1) * 64);
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
@@ -755,12 +758,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             for (int cc = 0; cc < nch; ++cc) {
                 if (cc == 0 && (!issue_tv(0) || !issue_qs(0))) break;
                 issued = true;
-                if (cc + 1 < nch && (!wait(B_D1, cc & 1) || !issue_tv(cc + 1))) break;
                 // P U_hi on top of Q' S (outputs only: one bf16 term)
                 if (!wait(B_E1DONE, cc & 1)) break;
                 tc_fence_after();
                 {
-                    const uint32_t pa = smem_u32(ring_b(cc) + kBP), ub = smem_u32(sm + OFF_U);
+                    const uint32_t pa = smem_u32(ring_b(cc) + kBP - 8192), ub = smem_u32(sm + OFF_U);
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16(tmem + TM_O + (uint32_t)((cc & 1) * 64), smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B),
@@ -768,10 +770,43 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     mma_commit(&bars[B_DO0 + (cc & 1)]);
                     mma_commit(&bars[B_EMPTYB0 + (cc & 1)]);
                 }
-                if (cc + 1 < nch && !issue_qs(cc + 1)) break;
+                // the next chunk's T'' V (its accumulator was last read in chunk cc - 1,
+                // before U of chunk cc was formed) and Q' S
+                if (cc + 1 < nch && (!issue_tv(cc + 1) || !issue_qs(cc + 1))) break;
             }
             if (issued) mma_commit(&bars[B_DRAIN]);
             else mbar_arrive(&bars[B_DRAIN]);
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ output warps
+        // thread = token t (TMEM lane 64 + t of the stacked output accumulator)
+        const int t = tid - 192;
+        const uint32_t lb = lane_base(warp);
+        for (int cc = 0; cc < nch; ++cc) {
+            bool ok = !*s_err && mbar_wait(&bars[B_DO0 + (cc & 1)], (cc >> 1) & 1);
+            if (!ok) fail();
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            float o1[NV], o2[NV];
+            tmem_ld32(tmem + lb + TM_O + (uint32_t)((cc & 1) * 64), o1);
+            tmem_ld32(tmem + lb + TM_O + (uint32_t)((cc & 1) * 64) + 32, o2);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_OUT0 + (cc & 1)]);
+            const int64_t tok = sr.t0 + (int64_t)cc * C + t;
+            if (tok < sr.t_end) {
+                __nv_bfloat16 *dst = p.out + ((size_t)tok * p.HV + h) * D + (size_t)vs * NV;
+#pragma unroll
+                for (int q = 0; q < NV; q += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack2(__float2bfloat16_rn(o1[q + 2 * e] + o2[q + 2 * e]),
+                                     __float2bfloat16_rn(o1[q + 2 * e + 1] + o2[q + 2 * e + 1]));
+                    *reinterpret_cast<uint4 *>(dst + q) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue warpgroup
@@ -779,7 +814,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                                             // M = 128 results
         const bool lead = (i == 0);
         const uint32_t lb = lane_base(warp);
-        const int tq = warp * 16 + (lane & 15);    // token row of the M = 64 results
+        const int tk = i & 63, hf = i >> 6;        // token, column half handled in E1
         float S[NV];
         const size_t sbase = (((size_t)s * p.HV + h) * D + i) * D + (size_t)vs * NV;
         if (p.s0) {
@@ -793,59 +828,39 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             for (int q = 0; q < NV; ++q) S[q] = 0.f;
         }
         float *xf = reinterpret_cast<float *>(sm + OFF_X);
-        float kd = 0.f, gl = 0.f;           // factors of the current chunk
-        auto load_factors = [&](int cc) -> bool {
-            if (!wg_wait(B_FULLB0 + (cc & 1), (cc >> 1) & 1)) return false;
-            const float *F = reinterpret_cast<const float *>(ring_b(cc) + kBF);
-            kd = F[SC_KD * C + (i & 63)];
-            gl = F[SC_MISC * C + 0];
-            return true;
-        };
-        // outputs of chunk c: O = D_O[:, 0:32] + D_O[:, 32:64] (M = 64 layout)
-        auto output = [&](int c) -> bool {
-            if (!wg_wait(B_DO0 + (c & 1), (c >> 1) & 1)) return false;
-            tc_fence_after();
-            float o1[NV], o2[NV];
-            tmem_ld32(tmem + lb + TM_O + (uint32_t)((c & 1) * 64), o1);
-            tmem_ld32(tmem + lb + TM_O + (uint32_t)((c & 1) * 64) + 32, o2);
-            tmem_ld_wait();
-            const int64_t t0c = sr.t0 + (int64_t)c * C;
-            if (lane < 16 && t0c + tq < sr.t_end) {
-                __nv_bfloat16 *dst = p.out + ((size_t)(t0c + tq) * p.HV + h) * D + (size_t)vs * NV;
-#pragma unroll
-                for (int q = 0; q < NV; q += 8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack2(__float2bfloat16_rn(o1[q + 2 * e] + o2[q + 2 * e]),
-                                     __float2bfloat16_rn(o1[q + 2 * e + 1] + o2[q + 2 * e + 1]));
-                    *reinterpret_cast<uint4 *>(dst + q) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            tc_fence_before();
-            return true;
+        // every thread polls the barriers itself, then one barrier reduction makes the
+        // outcome uniform (a timeout anywhere stops every thread)
+        auto wg_wait3 = [&](int b1, uint32_t p1, int b2, uint32_t p2, int b3, uint32_t p3) -> bool {
+            bool ok = !*s_err;
+            if (ok && !mbar_wait(&bars[b1], p1)) { fail(); ok = false; }
+            if (ok && b2 >= 0 && !mbar_wait(&bars[b2], p2)) { fail(); ok = false; }
+            if (ok && b3 >= 0 && !mbar_wait(&bars[b3], p3)) { fail(); ok = false; }
+            return wg_and(ok);
         };
         store_row_hilo128(sm + OFF_S, i, S);
         fence_async_smem();
         named_sync(1, 128);
         if (lead) mbar_arrive(&bars[B_SREADY]);
         bool issued = false;                // this lane has issued tensor-core work
-        bool run = nch > 0 && load_factors(0);
-        if (run && lane == 0 && (warp == 1 || warp == 2)) {
+        if (nch > 0 && lane == 0 && (warp == 1 || warp == 2)) {
             if (!issue_ws(warp, 0)) fail();
             issued = true;
         }
         __syncwarp();
-        int done = 0;                       // chunks whose outputs are written
-        for (int cc = 0; cc < nch && run; ++cc) {
+        for (int cc = 0; cc < nch; ++cc) {
             const int st = cc & 1;
             uint8_t *sb = ring_b(cc);
+            const float *F = reinterpret_cast<const float *>(sb + kBF);
             const int64_t tok0 = sr.t0 + (int64_t)cc * C;
             const int len = (int)min((int64_t)C, sr.t_end - tok0);
-            // ---- E1: U = rows 0-63 + rows 64-127 of (-W S + T'' V), Z = kd U
-            if (!wg_wait(B_D1, cc & 1)) break;
+            // ---- E1: U = rows 0-63 + rows 64-127 of (-W S + T'' V), Z = kd U; the previous
+            // chunk's P U_hi must have read the U_hi image
+            if (!wg_wait3(B_D1, cc & 1, B_FULLB0 + st, (cc >> 1) & 1,
+                          cc >= 1 ? B_DO0 + (st ^ 1) : -1, ((cc - 1) >> 1) & 1))
+                break;
             if (lead) mbar_arrive(&bars[B_EMPTYA0 + st]);   // ring A of chunk cc is consumed
             tc_fence_after();
+            const float kd = F[SC_KD * C + tk], gl = F[SC_MISC * C + 0];
             float uu[NV];
             {
                 float a[NV], b[NV];
@@ -861,38 +876,56 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll
                 for (int c = 0; c < NV; ++c) uu[c] += a[c] + b[c];
             }
-            if (i >= 64) {
+            // keep this thread's 16 columns, send the other 16 to the partner row (tk, 1 - hf)
+            float u16[16], o16[16];
 #pragma unroll
-                for (int c = 0; c < NV; c += 4)
-                    *reinterpret_cast<float4 *>(xf + (i - 64) * LDX + c) = make_float4(uu[c], uu[c + 1], uu[c + 2], uu[c + 3]);
+            for (int k = 0; k < 16; ++k) {
+                u16[k] = hf ? uu[16 + k] : uu[k];
+                o16[k] = hf ? uu[k] : uu[16 + k];
+            }
+            {
+                float *dst = xf + (1 - hf) * (C * 16);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<float4 *>(dst + xchg_off(tk, c)) =
+                        make_float4(o16[4 * c], o16[4 * c + 1], o16[4 * c + 2], o16[4 * c + 3]);
             }
             named_sync(1, 128);
-            if (i < 64) {
-                // token i: its U row, Z = kd U as [Z_hi | Z_lo], U_hi for P U
+            {
+                const float *src = xf + hf * (C * 16);
 #pragma unroll
-                for (int c = 0; c < NV; c += 4) {
-                    const float4 x4 = *reinterpret_cast<const float4 *>(xf + i * LDX + c);
-                    uu[c] += x4.x; uu[c + 1] += x4.y; uu[c + 2] += x4.z; uu[c + 3] += x4.w;
+                for (int c = 0; c < 4; ++c) {
+                    const float4 x4 = *reinterpret_cast<const float4 *>(src + xchg_off(tk, c));
+                    u16[4 * c] += x4.x;
+                    u16[4 * c + 1] += x4.y;
+                    u16[4 * c + 2] += x4.z;
+                    u16[4 * c + 3] += x4.w;
                 }
-                if (STATES) {
+            }
+            // columns 16 hf .. 16 hf + 15 of token tk: Z_hi, Z_lo (chunks 2 hf, 2 hf + 1 of
+            // each half of the 128-byte row) and U_hi (chunks 2 hf, 2 hf + 1 of the 64-byte row)
 #pragma unroll
-                    for (int c = 0; c < NV; c += 4)
-                        *reinterpret_cast<float4 *>(xf + i * LDX + c) = make_float4(uu[c], uu[c + 1], uu[c + 2], uu[c + 3]);
+            for (int q = 0; q < 2; ++q) {
+                uint32_t zh[4], zl[4], uh[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 8 * q + 2 * e;
+                    split2_bf16(kd * u16[c], kd * u16[c + 1], zh[e], zl[e]);
+                    const __nv_bfloat162 u2v = __floats2bfloat162_rn(u16[c], u16[c + 1]);
+                    uh[e] = *reinterpret_cast<const uint32_t *>(&u2v);
                 }
-                float z[NV];
+                const int ch = 2 * hf + q;
+                *reinterpret_cast<uint4 *>(sm + OFF_Z + sw128_offset(tk, ch * 16)) = make_uint4(zh[0], zh[1], zh[2], zh[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_Z + sw128_offset(tk, 64 + ch * 16)) = make_uint4(zl[0], zl[1], zl[2], zl[3]);
+                *reinterpret_cast<uint4 *>(sm + OFF_U + sw64_offset(tk, ch * 16)) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+            }
+            if (STATES) {
+                // U rows [64][32] for the per-token states, once every exchange read is done
+                named_sync(1, 128);
 #pragma unroll
-                for (int c = 0; c < NV; ++c) z[c] = kd * uu[c];
-                store_row_hilo128(sm + OFF_Z, i, z);
-#pragma unroll
-                for (int q = 0; q < NV / 8; ++q) {
-                    uint32_t uh[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __nv_bfloat162 u2v = __floats2bfloat162_rn(uu[8 * q + 2 * e], uu[8 * q + 2 * e + 1]);
-                        uh[e] = *reinterpret_cast<const uint32_t *>(&u2v);
-                    }
-                    *reinterpret_cast<uint4 *>(sm + OFF_U + sw64_offset(i, q * 16)) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-                }
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<float4 *>(xf + tk * NV + hf * 16 + 4 * c) =
+                        make_float4(u16[4 * c], u16[4 * c + 1], u16[4 * c + 2], u16[4 * c + 3]);
             }
             fence_async_smem();
             tc_fence_before();
@@ -913,13 +946,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 issued = true;
             }
             __syncwarp();
-            // the previous chunk's outputs while K^T Z runs
-            if (cc >= 1) {
-                if (!output(cc - 1)) break;
-                done = cc;
-            }
             // ---- E2: new state (thread i = key row i)
-            if (!wg_wait(B_D2, cc & 1)) break;
+            if (!wg_wait3(B_D2, cc & 1, -1, 0, -1, 0)) break;
             tc_fence_after();
             float ds[NV];
             {
@@ -939,7 +967,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 for (int c = 0; c < NV; ++c) ds[c] += d2[c];
             }
             if (STATES) {
-                const float *F = reinterpret_cast<const float *>(sb + kBF);
                 const uint8_t *ktile = sb + kBK + (i >> 6) * 8192;
                 const uint32_t kbyte = (uint32_t)(i & 63) * 2;
                 float rs[NV];
@@ -953,7 +980,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     const bool last = (t == len - 1);
 #pragma unroll
                     for (int c = 0; c < NV; c += 4) {
-                        const float4 u4 = *reinterpret_cast<const float4 *>(xf + t * LDX + c);
+                        const float4 u4 = *reinterpret_cast<const float4 *>(xf + t * NV + c);
                         rs[c] = al * rs[c] + f * u4.x;
                         rs[c + 1] = al * rs[c + 1] + f * u4.y;
                         rs[c + 2] = al * rs[c + 2] + f * u4.z;
@@ -981,13 +1008,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 issued = true;
             }
             __syncwarp();
-            if (cc + 1 < nch && !load_factors(cc + 1)) break;
-            if (cc + 1 == nch) {
-                if (!output(cc)) break;
-                done = nch;
-            }
         }
-        (void)done;
         if (lane == 0 && warp >= 1) {
             if (issued) mma_commit(&bars[B_DRAIN]);
             else mbar_arrive(&bars[B_DRAIN]);
