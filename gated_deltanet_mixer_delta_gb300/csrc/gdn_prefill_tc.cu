@@ -529,11 +529,11 @@ teardown:
 //              products on the chain's critical path right after the step that enables
 //              them (no hand-off): after the state update warps 1, 2 the k-step halves
 //              of -W S of the next chunk, after U warps 2, 3 the k-step halves of K^T Z.
-//   warp 4     TMEM owner; issues the products off the critical path: once U of chunk
-//              cc is formed, P U_hi of chunk cc and T'' V of chunk cc + 1; once the new
-//              state is written, Q' S of chunk cc + 1 (Q' S and P U share an accumulator,
-//              so one thread issues both)
-//   warp 5     TMA producer
+//   warp 4     TMEM owner; issues the output products: once U of chunk cc is formed,
+//              P U_hi of chunk cc; once the new state is written, Q' S of chunk cc + 1
+//              (Q' S and P U share an accumulator, so one thread issues both)
+//   warp 5     TMA producer; also issues T'' V of chunk cc + 1 as soon as it sees ring A
+//              of chunk cc - 1 released, i.e. once -W S of chunk cc is done
 //   warps 6-7  output warps: read rows 64-127 of D_O (TMEM lanes 64-127, one token per
 //              thread) and write the outputs
 // A chunk's inputs come through two 2-deep rings that are released at different points:
@@ -579,12 +579,13 @@ enum {
     B_FULLB0, B_FULLB1,        // [1 + tx] ring B stage loaded
     B_EMPTYB0, B_EMPTYB1,      // [2] ring B stage released (state update, P U done)
     B_D1,                      // [3] both halves of -W S and T'' V of the chunk are done
-    B_D2,                      // [3] both halves of K^T Z and Q' S of the chunk are done
+    B_D2,                      // [2] both halves of K^T Z of the chunk are done
+    B_QSD,                     // [1] Q' S of the chunk is done (it reads the state operand)
     B_DO0, B_DO1,              // [1] P U_hi into D_O[0] / D_O[1] is done
     B_OUT0, B_OUT1,            // [2] the output warps have read D_O[0] / D_O[1]
     B_E1DONE,                  // [1] Z and U_hi of the chunk are written
     B_SREADY,                  // [1] the state operand for the next chunk is written
-    B_DRAIN,                   // [4] every MMA of every issuer is done (teardown)
+    B_DRAIN,                   // [5] every MMA of every issuer is done (teardown)
     B_COUNT
 };
 
@@ -649,10 +650,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             mbar_init(&bars[B_OUT0 + b], 2);
         }
         mbar_init(&bars[B_D1], 3);
-        mbar_init(&bars[B_D2], 3);
+        mbar_init(&bars[B_D2], 2);
+        mbar_init(&bars[B_QSD], 1);
         mbar_init(&bars[B_E1DONE], 1);
         mbar_init(&bars[B_SREADY], 1);
-        mbar_init(&bars[B_DRAIN], 4);
+        mbar_init(&bars[B_DRAIN], 5);
         *s_err = 0;
         fence_mbar_init();
         if (nch > 0) {
@@ -697,35 +699,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     };
 
     if (warp == 5) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            for (int cc = 0; cc < nch; ++cc) {
-                const int st = cc & 1, u = cc >> 1;
-                const int tok = (int)(sr.t0 + (int64_t)cc * C);
-                const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.rec) +
-                                     ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes;
-                if (u >= 1 && !wait(B_EMPTYA0 + st, (u - 1) & 1)) break;
-                uint8_t *sa = ring_a(cc);
-                uint64_t *fa = &bars[B_FULLA0 + st];
-                mbar_arrive_expect_tx(fa, kStageA);
-                bulk_load(sa + kAW, rec, REC_P, fa);
-                tma_load_3d(sa + kAV, &mapV, fa, vs * NV, h, tok);
-                if (u >= 1 && !wait(B_EMPTYB0 + st, (u - 1) & 1)) break;
-                uint8_t *sb = ring_b(cc);
-                uint64_t *fb = &bars[B_FULLB0 + st];
-                mbar_arrive_expect_tx(fb, kStageB);
-                tma_load_3d(sb + kBK, &mapK, fb, 0, j, tok);
-                tma_load_3d(sb + kBK + 8192, &mapK, fb, 64, j, tok);
-                bulk_load(sb + kBP, rec + REC_P, kStageB - kBP, fb);
-            }
-        }
-    } else if (warp == 4) {
-        // ------------------------------------------------------------ off-path products
+        // ------------------------------------------------------------ TMA producer, T'' V
         if (lane == 0) {
             constexpr uint32_t id_u = instr_desc(128, NV, kFmtBF16, 0, 1);
-            constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
-            constexpr uint32_t id_o = instr_desc(128, NV, kFmtBF16, 0, 1);
-            // T'' V of chunk c into D_UT[c % 2] (last read by the epilogue in chunk c - 2)
+            // T'' V of chunk c into D_UT[c % 2] (last read by the epilogue in chunk c - 2,
+            // whose U was formed before -W S of chunk c - 1 was issued)
             auto issue_tv = [&](int c) -> bool {
                 if (!wait(B_FULLA0 + (c & 1), (c >> 1) & 1)) return false;
                 tc_fence_after();
@@ -739,6 +717,46 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 mma_commit(&bars[B_D1]);
                 return true;
             };
+            bool issued = false;
+            // iteration cc: (once -W S of chunk cc - 2 is done) T'' V of chunk cc - 1, then
+            // the loads of chunk cc; the last iteration only issues T'' V of chunk nch - 1.
+            // T'' V of chunk 0 waits for its inputs, so it follows the loads of chunk 1.
+            for (int cc = 0; cc <= nch; ++cc) {
+                const int st = cc & 1, u = cc >> 1;
+                if (cc >= 2 && !wait(B_EMPTYA0 + st, (u - 1) & 1)) break;
+                if (cc >= 2 || (cc == 1 && nch == 1)) {
+                    if (!issue_tv(cc - 1)) break;
+                    issued = true;
+                }
+                if (cc == nch) break;
+                const int tok = (int)(sr.t0 + (int64_t)cc * C);
+                const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.rec) +
+                                     ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes;
+                uint8_t *sa = ring_a(cc);
+                uint64_t *fa = &bars[B_FULLA0 + st];
+                mbar_arrive_expect_tx(fa, kStageA);
+                bulk_load(sa + kAW, rec, REC_P, fa);
+                tma_load_3d(sa + kAV, &mapV, fa, vs * NV, h, tok);
+                if (u >= 1 && !wait(B_EMPTYB0 + st, (u - 1) & 1)) break;
+                uint8_t *sb = ring_b(cc);
+                uint64_t *fb = &bars[B_FULLB0 + st];
+                mbar_arrive_expect_tx(fb, kStageB);
+                tma_load_3d(sb + kBK, &mapK, fb, 0, j, tok);
+                tma_load_3d(sb + kBK + 8192, &mapK, fb, 64, j, tok);
+                bulk_load(sb + kBP, rec + REC_P, kStageB - kBP, fb);
+                if (cc == 1) {
+                    if (!issue_tv(0)) break;
+                    issued = true;
+                }
+            }
+            if (issued) mma_commit(&bars[B_DRAIN]);
+            else mbar_arrive(&bars[B_DRAIN]);
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ off-path products
+        if (lane == 0) {
+            constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
+            constexpr uint32_t id_o = instr_desc(128, NV, kFmtBF16, 0, 1);
             // Q' S of chunk c into D_O[c % 2] once the state operand of chunk c - 1 is
             // written and the output warps have read the outputs of chunk c - 2
             auto issue_qs = [&](int c) -> bool {
@@ -751,12 +769,12 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(d, smem_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
                              smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_qs, ks > 0);
-                mma_commit(&bars[B_D2]);
+                mma_commit(&bars[B_QSD]);
                 return true;
             };
             bool issued = false;
             for (int cc = 0; cc < nch; ++cc) {
-                if (cc == 0 && (!issue_tv(0) || !issue_qs(0))) break;
+                if (cc == 0 && !issue_qs(0)) break;
                 issued = true;
                 // P U_hi on top of Q' S (outputs only: one bf16 term)
                 if (!wait(B_E1DONE, cc & 1)) break;
@@ -770,9 +788,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     mma_commit(&bars[B_DO0 + (cc & 1)]);
                     mma_commit(&bars[B_EMPTYB0 + (cc & 1)]);
                 }
-                // the next chunk's T'' V (its accumulator was last read in chunk cc - 1,
-                // before U of chunk cc was formed) and Q' S
-                if (cc + 1 < nch && (!issue_tv(cc + 1) || !issue_qs(cc + 1))) break;
+                if (cc + 1 < nch && !issue_qs(cc + 1)) break;
             }
             if (issued) mma_commit(&bars[B_DRAIN]);
             else mbar_arrive(&bars[B_DRAIN]);
@@ -995,6 +1011,9 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             }
 #pragma unroll
             for (int c = 0; c < NV; ++c) S[c] = gl * S[c] + ds[c];
+            // Q' S of this chunk reads the state operand that is rewritten now (a timeout
+            // here is caught by the next warpgroup wait)
+            if (!*s_err && !mbar_wait(&bars[B_QSD], cc & 1)) fail();
             store_row_hilo128(sm + OFF_S, i, S);
             fence_async_smem();
             tc_fence_before();
