@@ -564,12 +564,11 @@ static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0 && kAV % 1024 == 0 && k
 static_assert(kChainSmem <= 232448, "shared memory");
 
 // TMEM columns; M = 128 accumulators have row m in lane m
-constexpr uint32_t TM_WA = 0,     // -W S, k-steps 0-3   (N = 64)
-                   TM_WB = 64,    // -W S, k-steps 4-7   (N = 64)
-                   TM_UT = 128,   // T'' V [2]           (N = 32 each)
-                   TM_S = 192,    // K^T Z, k-steps 0-1  (N = 64)
-                   TM_S2 = 256,   // K^T Z, k-steps 2-3  (N = 64)
-                   TM_O = 320;    // Q' S + P U_hi [2]   (N = 64 each; rows 64-127 live)
+constexpr uint32_t TM_W = 0,      // -W S [2], k-steps 0-3 / 4-7 (N = 64 each)
+                   TM_UT = 256,   // T'' V [2]           (N = 32 each)
+                   TM_S = 320,    // K^T Z, k-steps 0-1  (N = 64)
+                   TM_S2 = 384,   // K^T Z, k-steps 2-3  (N = 64)
+                   TM_O = 448;    // Q' S + P U_hi       (N = 64; rows 64-127 live)
 constexpr uint32_t kTmemCols = 512;
 
 // barriers (arrival counts in brackets)
@@ -581,11 +580,11 @@ enum {
     B_D1,                      // [3] both halves of -W S and T'' V of the chunk are done
     B_D2,                      // [2] both halves of K^T Z of the chunk are done
     B_QSD,                     // [1] Q' S of the chunk is done (it reads the state operand)
-    B_DO0, B_DO1,              // [1] P U_hi into D_O[0] / D_O[1] is done
-    B_OUT0, B_OUT1,            // [2] the output warps have read D_O[0] / D_O[1]
+    B_DO,                      // [1] P U_hi (and Q' S before it) of the chunk is done
+    B_OUT,                     // [2] the output warps have read D_O
     B_E1DONE,                  // [1] Z and U_hi of the chunk are written
     B_SREADY,                  // [1] the state operand for the next chunk is written
-    B_DRAIN,                   // [5] every MMA of every issuer is done (teardown)
+    B_DRAIN,                   // [6] every MMA of every issuer is done (teardown)
     B_COUNT
 };
 
@@ -646,15 +645,15 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             mbar_init(&bars[B_EMPTYA0 + b], 1);
             mbar_init(&bars[B_FULLB0 + b], 1);
             mbar_init(&bars[B_EMPTYB0 + b], 2);
-            mbar_init(&bars[B_DO0 + b], 1);
-            mbar_init(&bars[B_OUT0 + b], 2);
         }
         mbar_init(&bars[B_D1], 3);
+        mbar_init(&bars[B_DO], 1);
+        mbar_init(&bars[B_OUT], 2);
         mbar_init(&bars[B_D2], 2);
         mbar_init(&bars[B_QSD], 1);
         mbar_init(&bars[B_E1DONE], 1);
         mbar_init(&bars[B_SREADY], 1);
-        mbar_init(&bars[B_DRAIN], 5);
+        mbar_init(&bars[B_DRAIN], 6);
         *s_err = 0;
         fence_mbar_init();
         if (nch > 0) {
@@ -681,21 +680,21 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     auto ring_b = [&](int cc) { return sm + OFF_B + (cc & 1) * kStageB; };
     const uint32_t s_img = smem_u32(sm + OFF_S), z_img = smem_u32(sm + OFF_Z);
 
-    // -W S of chunk cc from the state of chunk cc - 1, issued by lane 0 of epilogue warp
-    // w = 1 (k-steps 0-3) or 2 (k-steps 4-7); commit D1.
-    auto issue_ws = [&](int w, int cc) -> bool {
-        if (!wait(B_FULLA0 + (cc & 1), (cc >> 1) & 1)) return false;
+    // -W S of chunk cc from the state of chunk cc - 1, k-steps 4(w-1) .. 4(w-1)+3, issued
+    // by lane 0 of epilogue warp w = 1 or 2 into its own accumulator; commit D1.  The
+    // epilogue warpgroup has already seen ring A of chunk cc loaded.
+    auto issue_ws = [&](int w, int cc) {
         tc_fence_after();
         constexpr uint32_t id_ws = instr_desc(128, 64, kFmtBF16, 1, 1);
         const uint32_t wa = smem_u32(ring_a(cc) + kAW + REC_WHI);
-        const uint32_t d = tmem + (w == 1 ? TM_WA : TM_WB);
-        const int k0 = (w - 1) * 4;
+        const uint32_t d = tmem + TM_W + (uint32_t)((w - 1) * 64);
 #pragma unroll 1
-        for (int ks = k0; ks < k0 + 4; ++ks)
+        for (int q = 0; q < 4; ++q) {
+            const int ks = 4 * (w - 1) + q;
             mma_bf16(d, smem_desc(wa + ks * 2048, REC_WLO - REC_WHI, 1024, kSwizzle128B),
-                     smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_ws, ks > k0);
+                     smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_ws, q > 0);
+        }
         mma_commit(&bars[B_D1]);
-        return true;
     };
 
     if (warp == 5) {
@@ -757,14 +756,14 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         if (lane == 0) {
             constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
             constexpr uint32_t id_o = instr_desc(128, NV, kFmtBF16, 0, 1);
-            // Q' S of chunk c into D_O[c % 2] once the state operand of chunk c - 1 is
-            // written and the output warps have read the outputs of chunk c - 2
+            // Q' S of chunk c into D_O once the state operand of chunk c - 1 is written and
+            // the output warps have read the outputs of chunk c - 1
             auto issue_qs = [&](int c) -> bool {
                 if (!wait(B_SREADY, c & 1) || !wait(B_FULLB0 + (c & 1), (c >> 1) & 1)) return false;
-                if (c >= 2 && !wait(B_OUT0 + (c & 1), ((c - 2) >> 1) & 1)) return false;
+                if (c >= 1 && !wait(B_OUT, (c - 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t qa = smem_u32(ring_b(c) + kBQ - 8192);
-                const uint32_t d = tmem + TM_O + (uint32_t)((c & 1) * 64);
+                const uint32_t d = tmem + TM_O;
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(d, smem_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
@@ -783,9 +782,9 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     const uint32_t pa = smem_u32(ring_b(cc) + kBP - 8192), ub = smem_u32(sm + OFF_U);
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem + TM_O + (uint32_t)((cc & 1) * 64), smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B),
+                        mma_bf16(tmem + TM_O, smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B),
                                  smem_desc(ub + ks * 1024, 16, 512, kSwizzle64B), id_o, 1);
-                    mma_commit(&bars[B_DO0 + (cc & 1)]);
+                    mma_commit(&bars[B_DO]);
                     mma_commit(&bars[B_EMPTYB0 + (cc & 1)]);
                 }
                 if (cc + 1 < nch && !issue_qs(cc + 1)) break;
@@ -799,17 +798,17 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         const int t = tid - 192;
         const uint32_t lb = lane_base(warp);
         for (int cc = 0; cc < nch; ++cc) {
-            bool ok = !*s_err && mbar_wait(&bars[B_DO0 + (cc & 1)], (cc >> 1) & 1);
+            bool ok = !*s_err && mbar_wait(&bars[B_DO], cc & 1);
             if (!ok) fail();
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             float o1[NV], o2[NV];
-            tmem_ld32(tmem + lb + TM_O + (uint32_t)((cc & 1) * 64), o1);
-            tmem_ld32(tmem + lb + TM_O + (uint32_t)((cc & 1) * 64) + 32, o2);
+            tmem_ld32(tmem + lb + TM_O, o1);
+            tmem_ld32(tmem + lb + TM_O + 32, o2);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_OUT0 + (cc & 1)]);
+            if (lane == 0) mbar_arrive(&bars[B_OUT]);
             const int64_t tok = sr.t0 + (int64_t)cc * C + t;
             if (tok < sr.t_end) {
                 __nv_bfloat16 *dst = p.out + ((size_t)tok * p.HV + h) * D + (size_t)vs * NV;
@@ -846,51 +845,59 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         float *xf = reinterpret_cast<float *>(sm + OFF_X);
         // every thread polls the barriers itself, then one barrier reduction makes the
         // outcome uniform (a timeout anywhere stops every thread)
-        auto wg_wait3 = [&](int b1, uint32_t p1, int b2, uint32_t p2, int b3, uint32_t p3) -> bool {
+        // (barrier, parity) pairs; a negative barrier index is skipped
+        auto wg_wait4 = [&](int b1, uint32_t p1, int b2, uint32_t p2, int b3, uint32_t p3,
+                            int b4, uint32_t p4) -> bool {
             bool ok = !*s_err;
             if (ok && !mbar_wait(&bars[b1], p1)) { fail(); ok = false; }
             if (ok && b2 >= 0 && !mbar_wait(&bars[b2], p2)) { fail(); ok = false; }
             if (ok && b3 >= 0 && !mbar_wait(&bars[b3], p3)) { fail(); ok = false; }
+            if (ok && b4 >= 0 && !mbar_wait(&bars[b4], p4)) { fail(); ok = false; }
             return wg_and(ok);
         };
         store_row_hilo128(sm + OFF_S, i, S);
         fence_async_smem();
         named_sync(1, 128);
         if (lead) mbar_arrive(&bars[B_SREADY]);
+        int nch_run = nch;
         bool issued = false;                // this lane has issued tensor-core work
-        if (nch > 0 && lane == 0 && (warp == 1 || warp == 2)) {
-            if (!issue_ws(warp, 0)) fail();
-            issued = true;
+        if (nch > 0) {
+            if (!wg_wait4(B_FULLA0, 0, -1, 0, -1, 0, -1, 0)) nch_run = 0;
+            else if (lane == 0 && (warp == 1 || warp == 2)) {
+                issue_ws(warp, 0);
+                issued = true;
+            }
+            __syncwarp();
         }
-        __syncwarp();
-        for (int cc = 0; cc < nch; ++cc) {
+        for (int cc = 0; cc < nch_run; ++cc) {
             const int st = cc & 1;
             uint8_t *sb = ring_b(cc);
             const float *F = reinterpret_cast<const float *>(sb + kBF);
             const int64_t tok0 = sr.t0 + (int64_t)cc * C;
             const int len = (int)min((int64_t)C, sr.t_end - tok0);
             // ---- E1: U = rows 0-63 + rows 64-127 of (-W S + T'' V), Z = kd U; the previous
-            // chunk's P U_hi must have read the U_hi image
-            if (!wg_wait3(B_D1, cc & 1, B_FULLB0 + st, (cc >> 1) & 1,
-                          cc >= 1 ? B_DO0 + (st ^ 1) : -1, ((cc - 1) >> 1) & 1))
+            // chunk's P U_hi must have read the U_hi image.  Ring A of the next chunk is
+            // checked here too, for the -W S issued after the state update.
+            if (!wg_wait4(B_D1, cc & 1, B_FULLB0 + st, (cc >> 1) & 1, cc >= 1 ? B_DO : -1, (cc - 1) & 1,
+                          cc + 1 < nch ? B_FULLA0 + (st ^ 1) : -1, ((cc + 1) >> 1) & 1))
                 break;
             if (lead) mbar_arrive(&bars[B_EMPTYA0 + st]);   // ring A of chunk cc is consumed
             tc_fence_after();
             const float kd = F[SC_KD * C + tk], gl = F[SC_MISC * C + 0];
             float uu[NV];
             {
-                float a[NV], b[NV];
-                tmem_ld32(tmem + lb + TM_WA, uu);
-                tmem_ld32(tmem + lb + TM_WA + 32, a);
-                tmem_ld32(tmem + lb + TM_WB, b);
+                float a[NV], b[NV], c2[NV];
+                tmem_ld32(tmem + lb + TM_UT + (uint32_t)(st * NV), uu);
+                tmem_ld32(tmem + lb + TM_W, a);
+                tmem_ld32(tmem + lb + TM_W + 32, b);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < NV; ++c) uu[c] += a[c] + b[c];
-                tmem_ld32(tmem + lb + TM_WB + 32, a);
-                tmem_ld32(tmem + lb + TM_UT + (uint32_t)(st * NV), b);
+                tmem_ld32(tmem + lb + TM_W + 64, a);
+                tmem_ld32(tmem + lb + TM_W + 96, c2);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) uu[c] += a[c] + b[c];
+                for (int c = 0; c < NV; ++c) uu[c] += a[c] + c2[c];
             }
             // keep this thread's 16 columns, send the other 16 to the partner row (tk, 1 - hf)
             float u16[16], o16[16];
@@ -963,24 +970,18 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             }
             __syncwarp();
             // ---- E2: new state (thread i = key row i)
-            if (!wg_wait3(B_D2, cc & 1, -1, 0, -1, 0)) break;
+            if (!wg_wait4(B_D2, cc & 1, -1, 0, -1, 0, -1, 0)) break;
             tc_fence_after();
             float ds[NV];
             {
-                float d2[NV];
+                float d2[NV], d3[NV], d4[NV];
                 tmem_ld32(tmem + lb + TM_S, ds);
                 tmem_ld32(tmem + lb + TM_S + 32, d2);
+                tmem_ld32(tmem + lb + TM_S2, d3);
+                tmem_ld32(tmem + lb + TM_S2 + 32, d4);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) ds[c] += d2[c];
-                tmem_ld32(tmem + lb + TM_S2, d2);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < NV; ++c) ds[c] += d2[c];
-                tmem_ld32(tmem + lb + TM_S2 + 32, d2);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < NV; ++c) ds[c] += d2[c];
+                for (int c = 0; c < NV; ++c) ds[c] += d2[c] + d3[c] + d4[c];
             }
             if (STATES) {
                 const uint8_t *ktile = sb + kBK + (i >> 6) * 8192;
@@ -1023,12 +1024,12 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 mbar_arrive(&bars[B_SREADY]);
             }
             if (cc + 1 < nch && lane == 0 && (warp == 1 || warp == 2)) {
-                if (!issue_ws(warp, cc + 1)) fail();
+                issue_ws(warp, cc + 1);
                 issued = true;
             }
             __syncwarp();
         }
-        if (lane == 0 && warp >= 1) {
+        if (lane == 0) {
             if (issued) mma_commit(&bars[B_DRAIN]);
             else mbar_arrive(&bars[B_DRAIN]);
         }
