@@ -50,13 +50,11 @@ constexpr int NV = 32;         // value columns per chain CTA
 //   T'' hi, lo    [64 tokens][64 tokens]  K-major; stacked, the A operand of T'' V
 //                                                                            8 KiB each
 //   P             [64 tokens][64 tokens]  K-major A operand of P U          8 KiB
-//   Q'            [64 tokens][128 keys]   Q' = diag(rq gamma) Q, K-major A operand of Q' S
-//                                                                            16 KiB
-//   factors       8 rows of 64 floats (kd, rk, alpha, misc, 4 unused)      2 KiB
+//   factors       8 rows of 64 floats (qd, kd, rk, alpha, misc, 3 unused)  2 KiB
 constexpr int REC_WHI = 0, REC_WLO = 16384, REC_T2HI = 32768, REC_T2LO = 40960, REC_P = 49152,
-              REC_QP = 57344, REC_F = 73728;
-constexpr int kRecBytes = REC_F + 8 * C * 4;                // 74 KiB
-enum { SC_KD = 0, SC_RK, SC_ALPHA, SC_MISC };
+              REC_F = 57344;
+constexpr int kRecBytes = REC_F + 8 * C * 4;                // 58 KiB
+enum { SC_QD = 0, SC_KD, SC_RK, SC_ALPHA, SC_MISC };
 
 struct Params {
     const float *g, *beta, *s0;
@@ -362,24 +360,6 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     ok = mbar_wait(&bar[1], 0) && mbar_wait(&bar[3], 0);
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
-    // Q' = diag(rq gamma) Q (0 past the chunk end) in the query tile's own swizzled
-    // layout: every 16-byte chunk of row r is scaled by the row's factor
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int e = tid + kPrepThreads * k, r = (e >> 3) & 63;
-        const int off = (e >> 9) * 8192 + r * 128 + (e & 7) * 16;
-        const float f = r < len ? sRq[r] * expf(sG[r]) : 0.f;
-        const uint4 w4 = *reinterpret_cast<const uint4 *>(sQ + off);
-        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
-        uint32_t o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 v = __bfloat1622float2(b2[q]);
-            const __nv_bfloat162 sv = __floats2bfloat162_rn(v.x * f, v.y * f);
-            o[q] = *reinterpret_cast<const uint32_t *>(&sv);
-        }
-        *reinterpret_cast<uint4 *>(rec + REC_QP + off) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
     {
         // Gram row trow, columns tcb*32 .. +31; the key normaliser from its diagonal
         float gr[32];
@@ -483,6 +463,7 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         float *sc = reinterpret_cast<float *>(rec + REC_F);
         const bool in = tid < len;
         const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid];
+        sc[SC_QD * C + tid] = in ? sRq[tid] * expf(G) : 0.f;
         sc[SC_KD * C + tid] = in ? rk * expf(Gl - G) : 0.f;
         sc[SC_RK * C + tid] = in ? rk : 0.f;
         sc[SC_ALPHA * C + tid] = in ? expf(sg[tid]) : 0.f;
@@ -517,10 +498,10 @@ teardown:
 //   T'' V     A = [T''_hi; T''_lo] (M = 128), B = V slice (N = 32)
 //   K^T Z     A = key tile (M = 128 keys), B = [Z_hi | Z_lo] (N = 64); two issuers take
 //             k-steps 0-1 and 2-3
-//   Q' S      A = [any; Q'] (M = 128, the operand read from 8 KiB before Q', so that the
-//             64 live rows land in TMEM lanes 64-127), B = [S_hi | S_lo]; P U_hi (A read
-//             the same way) accumulates on top of its first 32 columns, so an output row
-//             is the sum of the two column halves
+//   Q S       A = [any; Q] (M = 128, the operand read from 8 KiB before the query tile,
+//             so that the 64 live rows land in TMEM lanes 64-127), B = [S_hi | S_lo]
+//   P U_hi    A = [any; P] the same way, B = U_hi (N = 32); an output row is
+//             qd (Q S[:, 0:32] + Q S[:, 32:64]) + P U_hi
 // Warp roles (256 threads):
 //   warps 0-3  epilogue warpgroup: thread i holds key row i of the fp32 state slice in
 //              registers; forms U (the two token halves of the stacked products are
@@ -530,24 +511,23 @@ teardown:
 //              them (no hand-off): after the state update warps 1, 2 the k-step halves
 //              of -W S of the next chunk, after U warps 2, 3 the k-step halves of K^T Z.
 //   warp 4     TMEM owner; issues the output products: once U of chunk cc is formed,
-//              P U_hi of chunk cc; once the new state is written, Q' S of chunk cc + 1
-//              (Q' S and P U share an accumulator, so one thread issues both)
+//              P U_hi of chunk cc; once the new state is written, Q S of chunk cc + 1
 //   warp 5     TMA producer; also issues T'' V of chunk cc + 1 as soon as it sees ring A
 //              of chunk cc - 1 released, i.e. once -W S of chunk cc is done
-//   warps 6-7  output warps: read rows 64-127 of D_O (TMEM lanes 64-127, one token per
-//              thread) and write the outputs
+//   warps 6-7  output warps: read rows 64-127 of Q S and P U (TMEM lanes 64-127, one
+//              token per thread) and write the outputs
 // A chunk's inputs come through two 2-deep rings that are released at different points:
 //   ring A  -W hi/lo, T'' hi/lo (the first 48 KiB of the record) and the value slice
 //           (64B swizzle: the MN-major B operand of T'' V as loaded); free once -W S and
 //           T'' V of the chunk are done, so the next loads start early in the chunk
-//   ring B  key tile, P, Q' and the factor rows; free after the state update and P U
+//   ring B  key and query tiles, P and the factor rows; free after the state update,
+//           P U and the output warps' read of the factors
 constexpr int kChainThreads = 256;
 constexpr int kAW = 0, kAV = REC_P, kStageA = kAV + C * NV * 2;              // 52 KiB
-constexpr int kBK = 0, kBP = 16384, kBQ = kBP + (REC_QP - REC_P), kBF = kBP + (REC_F - REC_P),
+constexpr int kBK = 0, kBQ = 16384, kBP = 32768, kBF = kBP + (REC_F - REC_P),
               kStageB = kBF + 8 * C * 4;                                     // 42 KiB
-static_assert(REC_WHI == 0 && REC_P == REC_T2LO + 8192 && REC_QP == REC_P + 8192 &&
-                  REC_F == REC_QP + 16384, "record layout");
-static_assert(kBP >= 8192 && kBQ >= 8192, "the stacked output operands read 8 KiB before P and Q'");
+static_assert(REC_WHI == 0 && REC_P == REC_T2LO + 8192 && REC_F == REC_P + 8192, "record layout");
+static_assert(kBP >= 8192 && kBQ >= 8192, "the stacked output operands read 8 KiB before P and Q");
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int OFF_A = 0;                                   // [2] ring A
 constexpr int OFF_B = OFF_A + 2 * kStageA;                 // [2] ring B
@@ -565,10 +545,11 @@ static_assert(kChainSmem <= 232448, "shared memory");
 
 // TMEM columns; M = 128 accumulators have row m in lane m
 constexpr uint32_t TM_W = 0,      // -W S [2], k-steps 0-3 / 4-7 (N = 64 each)
-                   TM_UT = 256,   // T'' V [2]           (N = 32 each)
-                   TM_S = 320,    // K^T Z, k-steps 0-1  (N = 64)
-                   TM_S2 = 384,   // K^T Z, k-steps 2-3  (N = 64)
-                   TM_O = 448;    // Q' S + P U_hi       (N = 64; rows 64-127 live)
+                   TM_UT = 128,   // T'' V [2]           (N = 32 each)
+                   TM_S = 192,    // K^T Z, k-steps 0-1  (N = 64)
+                   TM_S2 = 256,   // K^T Z, k-steps 2-3  (N = 64)
+                   TM_QS = 448,   // Q S                 (N = 64; rows 64-127 live)
+                   TM_PU = 416;   // P U_hi              (N = 32; rows 64-127 live)
 constexpr uint32_t kTmemCols = 512;
 
 // barriers (arrival counts in brackets)
@@ -576,12 +557,13 @@ enum {
     B_FULLA0 = 0, B_FULLA1,    // [1 + tx] ring A stage loaded
     B_EMPTYA0, B_EMPTYA1,      // [1] ring A stage released
     B_FULLB0, B_FULLB1,        // [1 + tx] ring B stage loaded
-    B_EMPTYB0, B_EMPTYB1,      // [2] ring B stage released (state update, P U done)
+    B_EMPTYB0, B_EMPTYB1,      // [4] ring B stage released (state update, P U done, both
+                               // output warps have read the factors)
     B_D1,                      // [3] both halves of -W S and T'' V of the chunk are done
     B_D2,                      // [2] both halves of K^T Z of the chunk are done
-    B_QSD,                     // [1] Q' S of the chunk is done (it reads the state operand)
-    B_DO,                      // [1] P U_hi (and Q' S before it) of the chunk is done
-    B_OUT,                     // [2] the output warps have read D_O
+    B_QSD,                     // [1] Q S of the chunk is done (it reads the state operand)
+    B_DO,                      // [1] P U_hi of the chunk is done
+    B_OUT,                     // [2] the output warps have read Q S and P U
     B_E1DONE,                  // [1] Z and U_hi of the chunk are written
     B_SREADY,                  // [1] the state operand for the next chunk is written
     B_DRAIN,                   // [6] every MMA of every issuer is done (teardown)
@@ -622,8 +604,8 @@ __device__ __forceinline__ int xchg_off(int t, int c) { return t * 16 + ((c ^ ((
 
 template <bool STATES>
 __global__ void __launch_bounds__(kChainThreads, 1)
-chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-             Params p) {
+chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
+             const __grid_constant__ CUtensorMap mapV, Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t su = smem_u32(smem_raw);
     uint8_t *sm = smem_raw + (((su + 1023u) & ~1023u) - su);
@@ -644,7 +626,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             mbar_init(&bars[B_FULLA0 + b], 1);
             mbar_init(&bars[B_EMPTYA0 + b], 1);
             mbar_init(&bars[B_FULLB0 + b], 1);
-            mbar_init(&bars[B_EMPTYB0 + b], 2);
+            mbar_init(&bars[B_EMPTYB0 + b], 4);
         }
         mbar_init(&bars[B_D1], 3);
         mbar_init(&bars[B_DO], 1);
@@ -658,6 +640,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         fence_mbar_init();
         if (nch > 0) {
             prefetch_tensormap(&mapK);
+            prefetch_tensormap(&mapQ);
             prefetch_tensormap(&mapV);
         }
     }
@@ -742,6 +725,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 mbar_arrive_expect_tx(fb, kStageB);
                 tma_load_3d(sb + kBK, &mapK, fb, 0, j, tok);
                 tma_load_3d(sb + kBK + 8192, &mapK, fb, 64, j, tok);
+                tma_load_3d(sb + kBQ, &mapQ, fb, 0, j, tok);
+                tma_load_3d(sb + kBQ + 8192, &mapQ, fb, 64, j, tok);
                 bulk_load(sb + kBP, rec + REC_P, kStageB - kBP, fb);
                 if (cc == 1) {
                     if (!issue_tv(0)) break;
@@ -756,14 +741,14 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         if (lane == 0) {
             constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
             constexpr uint32_t id_o = instr_desc(128, NV, kFmtBF16, 0, 1);
-            // Q' S of chunk c into D_O once the state operand of chunk c - 1 is written and
-            // the output warps have read the outputs of chunk c - 1
+            // Q S of chunk c once the state operand of chunk c - 1 is written and the output
+            // warps have read the outputs of chunk c - 1
             auto issue_qs = [&](int c) -> bool {
                 if (!wait(B_SREADY, c & 1) || !wait(B_FULLB0 + (c & 1), (c >> 1) & 1)) return false;
                 if (c >= 1 && !wait(B_OUT, (c - 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t qa = smem_u32(ring_b(c) + kBQ - 8192);
-                const uint32_t d = tmem + TM_O;
+                const uint32_t d = tmem + TM_QS;
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(d, smem_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
@@ -775,15 +760,15 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             for (int cc = 0; cc < nch; ++cc) {
                 if (cc == 0 && !issue_qs(0)) break;
                 issued = true;
-                // P U_hi on top of Q' S (outputs only: one bf16 term)
+                // P U_hi (outputs only: one bf16 term)
                 if (!wait(B_E1DONE, cc & 1)) break;
                 tc_fence_after();
                 {
                     const uint32_t pa = smem_u32(ring_b(cc) + kBP - 8192), ub = smem_u32(sm + OFF_U);
 #pragma unroll 1
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem + TM_O, smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B),
-                                 smem_desc(ub + ks * 1024, 16, 512, kSwizzle64B), id_o, 1);
+                        mma_bf16(tmem + TM_PU, smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B),
+                                 smem_desc(ub + ks * 1024, 16, 512, kSwizzle64B), id_o, ks > 0);
                     mma_commit(&bars[B_DO]);
                     mma_commit(&bars[B_EMPTYB0 + (cc & 1)]);
                 }
@@ -798,17 +783,27 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         const int t = tid - 192;
         const uint32_t lb = lane_base(warp);
         for (int cc = 0; cc < nch; ++cc) {
-            bool ok = !*s_err && mbar_wait(&bars[B_DO], cc & 1);
+            // the chunk's query factor, then release ring B's factor rows
+            bool ok = !*s_err && mbar_wait(&bars[B_FULLB0 + (cc & 1)], (cc >> 1) & 1);
+            if (!ok) fail();
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const float qd = reinterpret_cast<const float *>(ring_b(cc) + kBF)[SC_QD * C + t];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_EMPTYB0 + (cc & 1)]);
+            ok = !*s_err && mbar_wait(&bars[B_QSD], cc & 1) && mbar_wait(&bars[B_DO], cc & 1);
             if (!ok) fail();
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            float o1[NV], o2[NV];
-            tmem_ld32(tmem + lb + TM_O, o1);
-            tmem_ld32(tmem + lb + TM_O + 32, o2);
+            float o1[NV], o2[NV], o3[NV];
+            tmem_ld32(tmem + lb + TM_QS, o1);
+            tmem_ld32(tmem + lb + TM_QS + 32, o2);
+            tmem_ld32(tmem + lb + TM_PU, o3);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_OUT]);
+#pragma unroll
+            for (int q = 0; q < NV; ++q) o1[q] = qd * (o1[q] + o2[q]) + o3[q];
             const int64_t tok = sr.t0 + (int64_t)cc * C + t;
             if (tok < sr.t_end) {
                 __nv_bfloat16 *dst = p.out + ((size_t)tok * p.HV + h) * D + (size_t)vs * NV;
@@ -817,8 +812,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        w[e] = pack2(__float2bfloat16_rn(o1[q + 2 * e] + o2[q + 2 * e]),
-                                     __float2bfloat16_rn(o1[q + 2 * e + 1] + o2[q + 2 * e + 1]));
+                        w[e] = pack2(__float2bfloat16_rn(o1[q + 2 * e]), __float2bfloat16_rn(o1[q + 2 * e + 1]));
                     *reinterpret_cast<uint4 *>(dst + q) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
@@ -1122,7 +1116,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kChainSmem)) != cudaSuccess)
             return e;
-        kern<<<dim3(D / NV, pp.HV, pp.N), kChainThreads, kChainSmem, st>>>(mk, mv, p);
+        kern<<<dim3(D / NV, pp.HV, pp.N), kChainThreads, kChainSmem, st>>>(mk, mq, mv, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

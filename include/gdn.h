@@ -158,9 +158,9 @@ int gdn_decode_step(const void *queries, const void *keys, const void *values,
  *
  *   Arguments, layouts, results and error codes are those of gdn_prefill, minus the
  *   workspace.  Shapes whose scratch would exceed 64 MiB are rejected with
- *   GDN_ERR_WORKSPACE (for 128 x 128 bf16 heads a record is 74 KiB per 64-token chunk
- *   and value head: B * ceil(T / 64) * HV records must fit, at most 885 of them, e.g.
- *   T = 1728 tokens at 32 value heads uses 65.5 MB).
+ *   GDN_ERR_WORKSPACE (for 128 x 128 bf16 heads a record is 58 KiB per 64-token chunk
+ *   and value head: B * ceil(T / 64) * HV records must fit, at most 1129 of them, e.g.
+ *   T = 2240 tokens at 32 value heads uses 66.5 MB).
  *   - The array is a file-scope __device__ variable: every GPU that loads the
  *     library holds its 64 MiB until the process exits.
  *   - The first call on each device looks up the array's device address (with that

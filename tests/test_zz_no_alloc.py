@@ -80,7 +80,7 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row(gdn):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(gdn):
-    # 64 MiB holds 885 records of 74 KiB: 32 value heads x 128 chunks is more
+    # 64 MiB holds 1129 records of 58 KiB: 32 value heads x 128 chunks is more
     P = 0x10000
     rc = gdn.abi().gdn_prefill_noalloc(P, P, P, P, P, None, P, P, None, 1, 128 * 64, 16, 32, 128,
                                        128, 0, 0.0, 1, None)
