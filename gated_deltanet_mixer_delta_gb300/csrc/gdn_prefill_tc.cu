@@ -203,13 +203,18 @@ __device__ __forceinline__ void solve_block(float *sA, float *sT, float *sX, int
 #pragma unroll
     for (int e = 0; e < 4 * NQ; ++e) acc[e] = 0.f;
 #pragma unroll
-    for (int m = 0; m < N; ++m) {
-        const float a = sA[(r0 + r) * LDA + c0 + m];
+    for (int m4 = 0; m4 < N; m4 += 4) {
+        const float4 a4 = lds4(sA + (r0 + r) * LDA + c0 + m4);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            const float4 t4 = lds4(sT + (c0 + m) * LDA + c0 + cx + 4 * q);
-            acc[4 * q] += a * t4.x; acc[4 * q + 1] += a * t4.y;
-            acc[4 * q + 2] += a * t4.z; acc[4 * q + 3] += a * t4.w;
+        for (int mm = 0; mm < 4; ++mm) {
+            const float a = av[mm];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4 t4 = lds4(sT + (c0 + m4 + mm) * LDA + c0 + cx + 4 * q);
+                acc[4 * q] += a * t4.x; acc[4 * q + 1] += a * t4.y;
+                acc[4 * q + 2] += a * t4.z; acc[4 * q + 3] += a * t4.w;
+            }
         }
     }
 #pragma unroll
@@ -224,13 +229,18 @@ __device__ __forceinline__ void apply_block(float *sT, const float *sX, int r0, 
 #pragma unroll
     for (int e = 0; e < 4 * NQ; ++e) acc[e] = 0.f;
 #pragma unroll
-    for (int m = 0; m < N; ++m) {
-        const float t = sT[(r0 + r) * LDA + r0 + m];
+    for (int m4 = 0; m4 < N; m4 += 4) {
+        const float4 t4v = lds4(sT + (r0 + r) * LDA + r0 + m4);
+        const float tv[4] = {t4v.x, t4v.y, t4v.z, t4v.w};
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            const float4 x4 = lds4(sX + m * LDA + cx + 4 * q);
-            acc[4 * q] += t * x4.x; acc[4 * q + 1] += t * x4.y;
-            acc[4 * q + 2] += t * x4.z; acc[4 * q + 3] += t * x4.w;
+        for (int mm = 0; mm < 4; ++mm) {
+            const float t = tv[mm];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4 x4 = lds4(sX + (m4 + mm) * LDA + cx + 4 * q);
+                acc[4 * q] += t * x4.x; acc[4 * q + 1] += t * x4.y;
+                acc[4 * q + 2] += t * x4.z; acc[4 * q + 3] += t * x4.w;
+            }
         }
     }
 #pragma unroll
@@ -378,11 +388,16 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         const bool live = trow < len;
         const float G2t = sG2[trow], at = sB[trow] * sRk[trow], pt = sRq[trow];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const int jj = tcb * 32 + q;
-            const float e = (jj <= trow && jj < len) ? ex2_fast(G2t - sG2[jj]) * sRk[jj] : 0.f;
-            gr[q] = (live && jj < trow) ? at * e * gr[q] : 0.f;
-            qk[q] = pt * e * qk[q];
+        for (int q4 = 0; q4 < 32; q4 += 4) {
+            const float4 g4 = lds4(sG2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int q = q4 + qq, jj = tcb * 32 + q;
+                const float e = (jj <= trow && jj < len) ? ex2_fast(G2t - gv[qq]) * rv[qq] : 0.f;
+                gr[q] = (live && jj < trow) ? at * e * gr[q] : 0.f;
+                qk[q] = pt * e * qk[q];
+            }
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -400,7 +415,13 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         for (int r = 0; r < 16; ++r) {
             float acc = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int k = 0; k < r; ++k) acc -= sA[(base + r) * LDA + base + k] * x[k];
+            for (int k4 = 0; k4 < r; k4 += 4) {
+                const float4 a4 = lds4(sA + (base + r) * LDA + base + k4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    if (k4 + kk < r) acc -= av[kk] * x[k4 + kk];
+            }
             x[r] = (r < cc) ? 0.f : acc;
         }
 #pragma unroll
@@ -435,10 +456,16 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
             tv[4 * q] = t4.x; tv[4 * q + 1] = t4.y; tv[4 * q + 2] = t4.z; tv[4 * q + 3] = t4.w;
         }
 #pragma unroll
-        for (int q = 0; q < 32; ++q) x[q] = tv[q] * sC1[hh * 32 + q];
+        for (int q = 0; q < 32; q += 4) {
+            const float4 c4 = lds4(sC1 + hh * 32 + q);
+            x[q] = tv[q] * c4.x; x[q + 1] = tv[q + 1] * c4.y; x[q + 2] = tv[q + 2] * c4.z; x[q + 3] = tv[q + 3] * c4.w;
+        }
         store_half_row_hilo(sT1, sT1 + 8192, t, hh * 4, x);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) x[q] = tv[q] * sB[hh * 32 + q];   // beta is 0 past the end
+        for (int q = 0; q < 32; q += 4) {                    // beta is 0 past the end
+            const float4 b4 = lds4(sB + hh * 32 + q);
+            x[q] = tv[q] * b4.x; x[q + 1] = tv[q + 1] * b4.y; x[q + 2] = tv[q + 2] * b4.z; x[q + 3] = tv[q + 3] * b4.w;
+        }
         store_half_row_hilo(rec + REC_T2HI, rec + REC_T2LO, t, hh * 4, x);
     }
     fence_async_smem();
