@@ -47,6 +47,27 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def measured_traffic(profile, source):
+    """DRAM bytes per call (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
+    summary in profiles/, or None when the kernel source changed since the capture (the
+    summary records the sha256 of the source it profiled)."""
+    import hashlib
+    try:
+        fields = {}
+        with open(os.path.join(ROOT, "profiles", profile)) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 2 and parts[0] in ("traffic_bytes_per_call", "source_sha256"):
+                    fields[parts[0]] = parts[1]
+        with open(os.path.join(ROOT, "gated_deltanet_mixer_delta_gb300", "csrc", source), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if fields.get("source_sha256") != digest or "traffic_bytes_per_call" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_call"])
+
+
 # ---------------------------------------------------------------- algorithmic work
 def prefill_bytes(B_tokens, HK, HV, D, elt, n_states_in, n_states_out, states_tokens=0):
     """Bytes a prefill must move at least once: q, k, v, o (elt bytes), g and beta (fp32),
@@ -391,6 +412,9 @@ def main():
     if rank != 0:
         return
     achieved = head["bytes"] / (head["ms"] * 1e-3) / 1e9
+    # traffic of the headline workload's call (ncu capture at T = 4096 only)
+    traffic = (measured_traffic("prefill_kernels_T4096.md", "gdn_prefill_tc.cu")
+               if not args.prefill_T else None)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -402,7 +426,7 @@ def main():
                    "parallelism": f"replicas x{ws} (independent batches)"},
         "roofline": {"bound": "hbm", "kernel": "gdn_prefill (prep + scan)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": traffic, "peak_source": peak_src,
                      "algorithmic_bytes": head["bytes"], "flops": head["flops"]},
         "decode": {"workload": "decode_B256_hk16_hv32_d128", "value": 1e3 / dec_ms * ws,
                    "unit": "steps/s", "ms_per_step": dec_ms,
@@ -410,6 +434,7 @@ def main():
                                 "achieved": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9,
                                 "peak": hbm, "unit": "GB/s",
                                 "frac": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9 / hbm,
+                                "traffic": measured_traffic("decode_kernel_B256.md", "gdn_decode.cu"),
                                 "algorithmic_bytes": dec["bytes"]}},
         "e2e": {"value": e2e["tokens"] / e2e["s"] * ws, "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},

@@ -57,3 +57,22 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(1.5, 1) == 1.5
     assert bench.job_rate(100, 2.0, 1) == 50.0
+
+
+def test_measured_traffic_is_dropped_when_the_kernel_source_changes(tmp_path, monkeypatch):
+    # the roofline's traffic comes from a committed ncu summary only while the profiled
+    # source is unchanged
+    import bench
+    prof = tmp_path / "profiles"
+    src = tmp_path / "gated_deltanet_mixer_delta_gb300" / "csrc"
+    prof.mkdir()
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("kernel v1\n")
+    import hashlib
+    h = hashlib.sha256(b"kernel v1\n").hexdigest()
+    (prof / "k.md").write_text(f"summary\n\ntraffic_bytes_per_call 12345\nsource_sha256 {h}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_traffic("k.md", "k.cu") == 12345
+    (src / "k.cu").write_text("kernel v2\n")
+    assert bench.measured_traffic("k.md", "k.cu") is None
+    assert bench.measured_traffic("missing.md", "k.cu") is None
