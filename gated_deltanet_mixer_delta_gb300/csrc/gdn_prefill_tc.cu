@@ -864,16 +864,16 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             for (int q = 0; q < NV; ++q) S[q] = 0.f;
         }
         float *xf = reinterpret_cast<float *>(sm + OFF_X);
-        // every thread polls the barriers itself, then one barrier reduction makes the
-        // outcome uniform (a timeout anywhere stops every thread)
-        // (barrier, parity) pairs; a negative barrier index is skipped
+        // Up to four (barrier, parity) pairs, a negative barrier index being skipped: warp w
+        // polls pair w (all its threads), then one barrier reduction over the warpgroup
+        // joins them and makes the outcome uniform (a timeout anywhere stops every thread);
+        // the barrier also orders every thread after the phases the other warps observed.
         auto wg_wait4 = [&](int b1, uint32_t p1, int b2, uint32_t p2, int b3, uint32_t p3,
                             int b4, uint32_t p4) -> bool {
+            const int b = warp == 0 ? b1 : warp == 1 ? b2 : warp == 2 ? b3 : b4;
+            const uint32_t par = warp == 0 ? p1 : warp == 1 ? p2 : warp == 2 ? p3 : p4;
             bool ok = !*s_err;
-            if (ok && !mbar_wait(&bars[b1], p1)) { fail(); ok = false; }
-            if (ok && b2 >= 0 && !mbar_wait(&bars[b2], p2)) { fail(); ok = false; }
-            if (ok && b3 >= 0 && !mbar_wait(&bars[b3], p3)) { fail(); ok = false; }
-            if (ok && b4 >= 0 && !mbar_wait(&bars[b4], p4)) { fail(); ok = false; }
+            if (ok && b >= 0 && !mbar_wait(&bars[b], par)) { fail(); ok = false; }
             return wg_and(ok);
         };
         store_row_hilo128(sm + OFF_S, i, S);
@@ -991,7 +991,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             }
             __syncwarp();
             // ---- E2: new state (thread i = key row i)
-            if (!wg_wait4(B_D2, cc & 1, -1, 0, -1, 0, -1, 0)) break;
+            if (!wg_wait4(B_D2, cc & 1, B_QSD, cc & 1, -1, 0, -1, 0)) break;
             tc_fence_after();
             float ds[NV];
             {
@@ -1033,10 +1033,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             }
 #pragma unroll
             for (int c = 0; c < NV; ++c) S[c] = gl * S[c] + ds[c];
-            // Q' S of this chunk reads the state operand that is rewritten now (a timeout
-            // here is caught by the next warpgroup wait)
-            if (!*s_err && !mbar_wait(&bars[B_QSD], cc & 1)) fail();
-            store_row_hilo128(sm + OFF_S, i, S);
+            store_row_hilo128(sm + OFF_S, i, S);     // Q S of this chunk is done (QSD above)
             fence_async_smem();
             tc_fence_before();
             named_sync(1, 128);                 // the new state operand is complete
