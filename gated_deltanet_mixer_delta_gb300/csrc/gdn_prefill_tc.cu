@@ -537,12 +537,13 @@ teardown:
 //              products on the chain's critical path right after the step that enables
 //              them (no hand-off): after the state update warps 1, 2 the k-step halves
 //              of -W S of the next chunk, after U warps 2, 3 the k-step halves of K^T Z.
-//   warp 4     TMEM owner; issues the output products: once U of chunk cc is formed,
-//              P U_hi of chunk cc; once the new state is written, Q S of chunk cc + 1
+//   warp 4     TMEM owner; issues P U_hi of chunk cc once U of chunk cc is formed
 //   warp 5     TMA producer; also issues T'' V of chunk cc + 1 as soon as it sees ring A
 //              of chunk cc - 1 released, i.e. once -W S of chunk cc is done
-//   warps 6-7  output warps: read rows 64-127 of Q S and P U (TMEM lanes 64-127, one
-//              token per thread) and write the outputs
+//   warps 6-7  output warps: once -W S of chunk cc is done, lane 0 of each issues one
+//              k-step half of Q S of chunk cc (so that it runs while U is formed, when the
+//              tensor pipe is idle); then they read rows 64-127 of Q S and P U (TMEM lanes
+//              64-127, one token per thread) and write the outputs
 // A chunk's inputs come through two 2-deep rings that are released at different points:
 //   ring A  -W hi/lo, T'' hi/lo (the first 48 KiB of the record) and the value slice
 //           (64B swizzle: the MN-major B operand of T'' V as loaded); free once -W S and
@@ -575,8 +576,8 @@ constexpr uint32_t TM_W = 0,      // -W S [2], k-steps 0-3 / 4-7 (N = 64 each)
                    TM_UT = 128,   // T'' V [2]           (N = 32 each)
                    TM_S = 192,    // K^T Z, k-steps 0-1  (N = 64)
                    TM_S2 = 256,   // K^T Z, k-steps 2-3  (N = 64)
-                   TM_QS = 448,   // Q S                 (N = 64; rows 64-127 live)
-                   TM_PU = 416;   // P U_hi              (N = 32; rows 64-127 live)
+                   TM_QS = 320,   // Q S [2], k-steps 0-3 / 4-7 (N = 64 each; rows 64-127 live)
+                   TM_PU = 448;   // P U_hi              (N = 32; rows 64-127 live)
 constexpr uint32_t kTmemCols = 512;
 
 // barriers (arrival counts in brackets)
@@ -588,12 +589,11 @@ enum {
                                // output warps have read the factors)
     B_D1,                      // [3] both halves of -W S and T'' V of the chunk are done
     B_D2,                      // [2] both halves of K^T Z of the chunk are done
-    B_QSD,                     // [1] Q S of the chunk is done (it reads the state operand)
+    B_QSD,                     // [2] both halves of Q S of the chunk are done
     B_DO,                      // [1] P U_hi of the chunk is done
     B_OUT,                     // [2] the output warps have read Q S and P U
     B_E1DONE,                  // [1] Z and U_hi of the chunk are written
-    B_SREADY,                  // [1] the state operand for the next chunk is written
-    B_DRAIN,                   // [6] every MMA of every issuer is done (teardown)
+    B_DRAIN,                   // [8] every MMA of every issuer is done (teardown)
     B_COUNT
 };
 
@@ -659,10 +659,9 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         mbar_init(&bars[B_DO], 1);
         mbar_init(&bars[B_OUT], 2);
         mbar_init(&bars[B_D2], 2);
-        mbar_init(&bars[B_QSD], 1);
+        mbar_init(&bars[B_QSD], 2);
         mbar_init(&bars[B_E1DONE], 1);
-        mbar_init(&bars[B_SREADY], 1);
-        mbar_init(&bars[B_DRAIN], 6);
+        mbar_init(&bars[B_DRAIN], 8);
         *s_err = 0;
         fence_mbar_init();
         if (nch > 0) {
@@ -766,29 +765,13 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     } else if (warp == 4) {
         // ------------------------------------------------------------ off-path products
         if (lane == 0) {
-            constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
             constexpr uint32_t id_o = instr_desc(128, NV, kFmtBF16, 0, 1);
-            // Q S of chunk c once the state operand of chunk c - 1 is written and the output
-            // warps have read the outputs of chunk c - 1
-            auto issue_qs = [&](int c) -> bool {
-                if (!wait(B_SREADY, c & 1) || !wait(B_FULLB0 + (c & 1), (c >> 1) & 1)) return false;
-                if (c >= 1 && !wait(B_OUT, (c - 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t qa = smem_u32(ring_b(c) + kBQ - 8192);
-                const uint32_t d = tmem + TM_QS;
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(d, smem_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
-                             smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_qs, ks > 0);
-                mma_commit(&bars[B_QSD]);
-                return true;
-            };
             bool issued = false;
             for (int cc = 0; cc < nch; ++cc) {
-                if (cc == 0 && !issue_qs(0)) break;
+                // P U_hi (outputs only: one bf16 term) once U is formed and the output
+                // warps have read the previous chunk's
+                if (!wait(B_E1DONE, cc & 1) || (cc >= 1 && !wait(B_OUT, (cc - 1) & 1))) break;
                 issued = true;
-                // P U_hi (outputs only: one bf16 term)
-                if (!wait(B_E1DONE, cc & 1)) break;
                 tc_fence_after();
                 {
                     const uint32_t pa = smem_u32(ring_b(cc) + kBP - 8192), ub = smem_u32(sm + OFF_U);
@@ -799,7 +782,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     mma_commit(&bars[B_DO]);
                     mma_commit(&bars[B_EMPTYB0 + (cc & 1)]);
                 }
-                if (cc + 1 < nch && !issue_qs(cc + 1)) break;
             }
             if (issued) mma_commit(&bars[B_DRAIN]);
             else mbar_arrive(&bars[B_DRAIN]);
@@ -809,7 +791,31 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         // thread = token t (TMEM lane 64 + t of the stacked output accumulator)
         const int t = tid - 192;
         const uint32_t lb = lane_base(warp);
+        bool issued = false;
         for (int cc = 0; cc < nch; ++cc) {
+            // Q S of chunk cc, k-steps 4 (warp - 6) .. + 3: A = [any; Q] read from 8 KiB
+            // before the query tile so that the live rows land in TMEM lanes 64-127.  The
+            // state operand it reads was written before -W S of chunk cc was issued and is
+            // rewritten only after QSD; both output warps have read Q S of chunk cc - 1 (OUT).
+            if (lane == 0) {
+                bool ok2 = wait(B_D1, cc & 1) && wait(B_FULLB0 + (cc & 1), (cc >> 1) & 1) &&
+                           (cc == 0 || wait(B_OUT, (cc - 1) & 1));
+                if (ok2) {
+                    tc_fence_after();
+                    constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
+                    const uint32_t qa = smem_u32(ring_b(cc) + kBQ - 8192);
+                    const uint32_t dq = tmem + TM_QS + (uint32_t)((warp - 6) * 64);
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        const int ks = 4 * (warp - 6) + q;
+                        mma_bf16(dq, smem_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
+                                 smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_qs, q > 0);
+                    }
+                    mma_commit(&bars[B_QSD]);
+                    issued = true;
+                }
+            }
+            __syncwarp();
             // the chunk's query factor, then release ring B's factor rows
             bool ok = !*s_err && mbar_wait(&bars[B_FULLB0 + (cc & 1)], (cc >> 1) & 1);
             if (!ok) fail();
@@ -824,6 +830,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             float o1[NV], o2[NV], o3[NV];
             tmem_ld32(tmem + lb + TM_QS, o1);
             tmem_ld32(tmem + lb + TM_QS + 32, o2);
+            tmem_ld32(tmem + lb + TM_QS + 64, o3);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < NV; ++q) o1[q] += o2[q] + o3[q];
+            tmem_ld32(tmem + lb + TM_QS + 96, o2);
             tmem_ld32(tmem + lb + TM_PU, o3);
             tmem_ld_wait();
             tc_fence_before();
@@ -843,6 +854,10 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     *reinterpret_cast<uint4 *>(dst + q) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
+        }
+        if (lane == 0) {
+            if (issued) mma_commit(&bars[B_DRAIN]);
+            else mbar_arrive(&bars[B_DRAIN]);
         }
     } else {
         // ------------------------------------------------------------ epilogue warpgroup
@@ -879,7 +894,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         store_row_hilo128(sm + OFF_S, i, S);
         fence_async_smem();
         named_sync(1, 128);
-        if (lead) mbar_arrive(&bars[B_SREADY]);
         int nch_run = nch;
         bool issued = false;                // this lane has issued tensor-core work
         if (nch > 0) {
@@ -1037,10 +1051,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             fence_async_smem();
             tc_fence_before();
             named_sync(1, 128);                 // the new state operand is complete
-            if (lead) {
-                mbar_arrive(&bars[B_EMPTYB0 + st]);   // (with the P U commit)
-                mbar_arrive(&bars[B_SREADY]);
-            }
+            if (lead) mbar_arrive(&bars[B_EMPTYB0 + st]);   // (with the P U commit)
             if (cc + 1 < nch && lane == 0 && (warp == 1 || warp == 2)) {
                 issue_ws(warp, cc + 1);
                 issued = true;
