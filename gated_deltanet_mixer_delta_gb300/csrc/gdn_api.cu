@@ -17,9 +17,9 @@ int max_chunks_for(int64_t T_total, int n_seqs, bool packed, int T_seq) {
     return (int)((T_total + kChunk - 1) / kChunk + n_seqs);
 }
 
-// header | chunk_seq[max_chunks] | chunk_first[N+1] | records[max_chunks][HV]
+// header | chunk_seq[max_chunks] | chunk_first[N+1] | seq_order[N] | records[max_chunks][HV]
 static size_t table_bytes(int max_chunks, int n_seqs) {
-    return round_up(sizeof(int32_t) * ((size_t)max_chunks + n_seqs + 1), 256);
+    return round_up(sizeof(int32_t) * ((size_t)max_chunks + 2 * (size_t)n_seqs + 1), 256);
 }
 
 size_t prefill_workspace_bytes(int64_t T_total, int n_seqs, int HV, int Dk, int Dv) {
@@ -89,6 +89,7 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     p.status = (int32_t *)ws;
     p.chunk_seq = (int32_t *)(ws + kWsHeader);
     p.chunk_first = p.chunk_seq + mc;
+    p.seq_order = p.chunk_first + N + 1;
     p.rec = (float *)(ws + kWsHeader + table_bytes(mc, N));
     p.rec_floats = record_floats(Dk, Dv);
 

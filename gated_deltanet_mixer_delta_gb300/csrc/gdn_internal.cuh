@@ -35,6 +35,7 @@ struct PrefillParams {
     int32_t *status;              // workspace status words
     int32_t *chunk_seq;           // [max_chunks] sequence of chunk (packed batches)
     int32_t *chunk_first;         // [N + 1] first chunk of each sequence (packed batches)
+    int32_t *seq_order;           // [N] sequences by decreasing chunk count (packed batches)
     float *rec;                   // per (chunk, value head) records of the prep pass
     size_t rec_floats;            // floats per record
 };

@@ -65,6 +65,8 @@ __device__ __forceinline__ bool chunk_info(const PrefillParams &p, int c, ChunkI
 // ------------------------------------------------------------------ chunk table
 // One CTA: checks 0 = cu[0] <= cu[1] <= ... <= cu[N] = T_total, counts the chunks
 // of every sequence, and writes chunk_first (exclusive prefix) and chunk_seq.
+constexpr int kMaxRanked = 1024;
+
 __global__ void __launch_bounds__(1024) chunk_table_kernel(PrefillParams p) {
     __shared__ int s_bad;
     __shared__ int s_carry;
@@ -106,8 +108,27 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(PrefillParams p) {
         if (tid == blockDim.x - 1) s_carry = incl;
         __syncthreads();
     }
+    if (tid == 0) p.chunk_first[p.N] = s_carry;
+    // longest sequences first: seq_order[rank] = sequence, rank = number of sequences with
+    // more chunks (ties by index), so that the sequential kernels start the longest chains
+    // first; above kMaxRanked sequences the order is the identity
+    __syncthreads();
+    if (p.N <= kMaxRanked) {
+        if (tid < p.N) s_scan[tid] = (p.cu_seqlens[tid + 1] - p.cu_seqlens[tid] + C - 1) / C;
+        __syncthreads();
+        if (tid < p.N) {
+            const int ci = s_scan[tid];
+            int rank = 0;
+            for (int j2 = 0; j2 < p.N; ++j2) {
+                const int cj = s_scan[j2];
+                rank += (cj > ci) || (cj == ci && j2 < tid);
+            }
+            p.seq_order[rank] = tid;
+        }
+    } else {
+        for (int i = tid; i < p.N; i += blockDim.x) p.seq_order[i] = i;
+    }
     if (tid == 0) {
-        p.chunk_first[p.N] = s_carry;
         p.status[kChunkCountWord] = s_carry;
         p.status[kStatusWord] = GDN_OK;
     }

@@ -66,7 +66,7 @@ struct Params {
     float scale;
     int l2norm;
     int max_chunks;
-    int32_t *status, *chunk_seq, *chunk_first;
+    int32_t *status, *chunk_seq, *chunk_first, *seq_order;
     float *rec;                  // [chunks][HV] records of kRecBytes
 };
 
@@ -640,8 +640,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 8 * B_COUNT);
     volatile int *s_err = reinterpret_cast<volatile int *>(sm + OFF_BAR + 8 * B_COUNT + 4);
 
-    const int vs = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int vs = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // packed batches: the longest sequences first (the chunk-table kernel ranked them)
+    if (p.cu_seqlens && p.status[kStatusWord] != GDN_OK) return;
+    const int s = p.cu_seqlens ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
     SeqRange sr;
     if (!seq_range(p, s, sr)) return;
     if (!p.cu_seqlens && vs == 0 && h == 0 && s == 0 && tid == 0) p.status[kStatusWord] = GDN_OK;
@@ -1129,7 +1132,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     p.cu_seqlens = pp.cu_seqlens; p.N = pp.N; p.T_seq = pp.T_seq; p.T_total = pp.T_total;
     p.HK = pp.HK; p.HV = pp.HV; p.scale = pp.scale; p.l2norm = pp.l2norm;
     p.max_chunks = pp.max_chunks; p.status = pp.status; p.chunk_seq = pp.chunk_seq;
-    p.chunk_first = pp.chunk_first; p.rec = pp.rec;
+    p.chunk_first = pp.chunk_first; p.seq_order = pp.seq_order; p.rec = pp.rec;
     CUtensorMap mk, mq, mv;
     if (pp.T_total > 0) {
         if (!make_map(&mk, pp.k, pp.HK, pp.T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
