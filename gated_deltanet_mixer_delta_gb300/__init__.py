@@ -22,7 +22,8 @@ import torch
 from . import build as _build
 
 __all__ = ["prefill", "prefill_varlen", "decode_step", "state_layout", "workspace_size",
-           "workspace_status", "GdnError", "library_path", "load_library", "abi"]
+           "workspace_status", "selftest_wait_timeout", "GdnError", "library_path",
+           "load_library", "abi"]
 
 GDN_OK = 0
 _STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported shape or dtype",
@@ -84,6 +85,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_status_string.argtypes = [i]
     lib.gdn_abi_version.restype = i
     lib.gdn_abi_version.argtypes = []
+    lib.gdn_selftest_wait_timeout.restype = i
+    lib.gdn_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint64, vp]
     _lib = lib
     return lib
 
@@ -140,6 +143,19 @@ def workspace_status(workspace, stream=None) -> int:
     _check(load_library().gdn_workspace_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
            "gdn_workspace_status")
     return st.value
+
+
+def selftest_wait_timeout(limit_ns, device=None, stream=None):
+    """Run the library's bounded-wait self-test on the GPU: a wait on an mbarrier phase
+    that nothing completes must give up after ``limit_ns`` and report GDN_ERR_TIMEOUT.
+    Returns (status, microseconds waited)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    status = torch.full((2,), 12345, dtype=torch.int32, device=dev)
+    _check(load_library().gdn_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)),
+           "gdn_selftest_wait_timeout")
+    torch.cuda.synchronize(dev)
+    s = status.cpu().tolist()
+    return int(s[0]), int(s[1])
 
 
 def _workspace(workspace, nbytes, device):

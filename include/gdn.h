@@ -216,6 +216,20 @@ const char *gdn_status_string(int status);
 /* ABI version: major * 10000 + minor * 100 + patch. */
 int gdn_abi_version(void);
 
+/*
+ * Self-test of the bounded waits (no counterpart on the pages: failure handling of this
+ * library).  Every wait of the tensor-core kernels on an mbarrier phase gives up after a
+ * time limit and records GDN_ERR_TIMEOUT instead of hanging.  This call launches one
+ * thread on `cuda_stream` that waits, with the same helper, on a phase that nothing
+ * completes, for `limit_ns` nanoseconds (1 ns .. 2 s), then writes status[0] =
+ * GDN_ERR_TIMEOUT (or GDN_OK, which would mean the wait returned without the phase
+ * completing, i.e. a broken wait) and status[1] = the microseconds it waited.  `status`
+ * is a device pointer to two int32 owned by the caller (4-byte aligned).  Returns
+ * GDN_ERR_INVALID_ARG / GDN_ERR_MISALIGNED for bad arguments, GDN_ERR_CUDA if the
+ * launch fails, otherwise GDN_OK (asynchronous: read status after synchronising).
+ */
+int gdn_selftest_wait_timeout(int32_t *status, uint64_t limit_ns, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

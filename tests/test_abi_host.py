@@ -140,3 +140,15 @@ def _decode(lib, **kw):
 ])
 def test_decode_rejects_bad_arguments_on_host(lib, kw, code):
     assert _decode(lib, **kw) == code
+
+
+def test_selftest_wait_timeout_rejects_bad_arguments(lib):
+    # host-side checks only: nothing is launched for these
+    import ctypes
+    f = lib.gdn_selftest_wait_timeout
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+    assert f(None, 1000, None) == -1                      # GDN_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(0x10000), 0, None) == -1     # zero limit
+    assert f(ctypes.c_void_p(0x10000), 3_000_000_000, None) == -1   # above 2 s
+    assert f(ctypes.c_void_p(0x10002), 1000, None) == -3  # GDN_ERR_MISALIGNED
