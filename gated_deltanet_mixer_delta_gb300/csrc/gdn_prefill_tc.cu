@@ -613,6 +613,15 @@ __device__ __forceinline__ bool wg_and(bool v) {
     return r != 0;
 }
 
+// 8 fp32 values to global memory in one 32-byte streaming store (a whole sector);
+// dst must be 32-byte aligned
+__device__ __forceinline__ void st_cs_v8(float *dst, float a0, float a1, float a2, float a3, float a4,
+                                         float a5, float a6, float a7) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(dst), "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+                 : "memory");
+}
+
 // 32 fp32 values -> one 128-byte row [hi | lo] of a 128B-swizzled bf16 image
 __device__ __forceinline__ void store_row_hilo128(uint8_t *img, int row, const float (&x)[32]) {
 #pragma unroll
@@ -1040,12 +1049,14 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                         rs[c + 1] = al * rs[c + 1] + f * u4.y;
                         rs[c + 2] = al * rs[c + 2] + f * u4.z;
                         rs[c + 3] = al * rs[c + 3] + f * u4.w;
-                        const float4 o4 = last
-                            ? make_float4(gl * S[c] + ds[c], gl * S[c + 1] + ds[c + 1],
-                                          gl * S[c + 2] + ds[c + 2], gl * S[c + 3] + ds[c + 3])
-                            : make_float4(rs[c], rs[c + 1], rs[c + 2], rs[c + 3]);
-                        __stcs(reinterpret_cast<float4 *>(dst + c), o4);
                     }
+                    // the state after the chunk's last token is the carried chunk-form state
+                    float o[NV];
+#pragma unroll
+                    for (int c = 0; c < NV; ++c) o[c] = last ? gl * S[c] + ds[c] : rs[c];
+#pragma unroll
+                    for (int c = 0; c < NV; c += 8)
+                        st_cs_v8(dst + c, o[c], o[c + 1], o[c + 2], o[c + 3], o[c + 4], o[c + 5], o[c + 6], o[c + 7]);
                 }
             }
 #pragma unroll
