@@ -271,7 +271,11 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     uint64_t *bar = reinterpret_cast<uint64_t *>(sC1 + C);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
-    const int c = blockIdx.x, h = blockIdx.y;
+    // one CTA per (chunk, key head j): the key and query tiles, K K^T, Q K^T and the norms
+    // are shared by the value heads j r .. j r + r - 1 (r = HV / HK), which are handled one
+    // after the other
+    const int c = blockIdx.x, j = blockIdx.y;
+    const int ratio = p.HV / p.HK;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // chunk -> (sequence, first token, length)
     int64_t t0;
@@ -288,8 +292,6 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         t0 = (int64_t)s * p.T_seq + (int64_t)local * C;
         len = min(C, p.T_seq - local * C);
     }
-    const int j = h / (p.HV / p.HK);
-    uint8_t *rec = reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h) * kRecBytes;
 
     if (tid == 0) {
         for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
@@ -304,6 +306,8 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     const uint32_t lb = (uint32_t)(warp * 32) << 16;    // this warp's TMEM lanes
     const int trow = warp * 16 + (lane & 15), tcb = lane >> 4;   // row / column half of
                                                                   // the M = 64 results
+    float gr[32], qk[32];                               // Gram and Q K^T: row trow, 32 columns
+    bool ok = true;
 
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar[0], 32768);
@@ -312,26 +316,10 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         tma_load_3d(sQ, &mapQ, &bar[0], 0, j, (int)t0);
         tma_load_3d(sQ + 8192, &mapQ, &bar[0], 64, j, (int)t0);
     }
-    // gates of the chunk and the decay prefix (two warps, shuffle scan)
-    if (tid < C) {
-        const bool in = tid < len;
-        const size_t gi = (size_t)(t0 + tid) * p.HV + h;
-        float gv = in ? p.g[gi] : 0.f;
-        sg[tid] = gv;
-        sB[tid] = in ? p.beta[gi] : 0.f;
-        float x = gv;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            float y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        sG[tid] = x;   // inclusive within the warp
-    }
-    // T starts as zero (its upper part stays zero)
+    // T starts as zero (its upper part stays zero for every head)
     for (int e = tid; e < C * LDA / 4; e += kPrepThreads) sts4(sT + 4 * e, 0.f, 0.f, 0.f, 0.f);
-    bool ok = mbar_wait(&bar[0], 0);
+    ok = mbar_wait(&bar[0], 0);
     if (__syncthreads_or(!ok)) goto teardown;
-    if (tid >= 32 && tid < C) sG[tid] += sG[31];
     tc_fence_after();
     if (lane == 0 && warp < 2) {
         // Gram K K^T into columns 0-63 (thread 0), Q K^T into columns 64-127 (thread 32);
@@ -366,149 +354,176 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         if (half == 0) sRq[row] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
     }
-    if (tid < C) sG2[tid] = sG[tid] * kLog2e;
     ok = mbar_wait(&bar[1], 0) && mbar_wait(&bar[3], 0);
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
+    // Gram and Q K^T rows into registers (they serve every value head); the key
+    // normaliser from the Gram diagonal
+    tmem_row_split(tmem + lb, gr);
+    tmem_row_split(tmem + lb + 64, qk);
     {
-        // Gram row trow, columns tcb*32 .. +31; the key normaliser from its diagonal
-        float gr[32];
-        tmem_row_split(tmem + lb, gr);
-        {
-            float diag = 0.f;
+        float diag = 0.f;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) diag = (tcb * 32 + q == trow) ? gr[q] : diag;
-            if ((trow >> 5) == tcb) sRk[trow] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
-        }
-        __syncthreads();
-        // A_tj = beta_t e^{G_t-G_j} rk_t rk_j k_t.k_j (j < t) into smem and
-        // P_tj = e^{G_t-G_j} rq_t rk_j q_t.k_j (j <= t) into the record, one exponential
-        float qk[32];
-        tmem_row_split(tmem + lb + 64, qk);
-        const bool live = trow < len;
-        const float G2t = sG2[trow], at = sB[trow] * sRk[trow], pt = sRq[trow];
-#pragma unroll
-        for (int q4 = 0; q4 < 32; q4 += 4) {
-            const float4 g4 = lds4(sG2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
-            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                const int q = q4 + qq, jj = tcb * 32 + q;
-                const float e = (jj <= trow && jj < len) ? ex2_fast(G2t - gv[qq]) * rv[qq] : 0.f;
-                gr[q] = (live && jj < trow) ? at * e * gr[q] : 0.f;
-                qk[q] = pt * e * qk[q];
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            sts4(sA + trow * LDA + tcb * 32 + 4 * q, gr[4 * q], gr[4 * q + 1], gr[4 * q + 2], gr[4 * q + 3]);
-        store_half_row_bf16(rec + REC_P, trow, tcb * 4, qk);
+        for (int q = 0; q < 32; ++q) diag = (tcb * 32 + q == trow) ? gr[q] : diag;
+        if ((trow >> 5) == tcb) sRk[trow] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
     }
-    if (tid < C) sC1[tid] = tid < len ? sB[tid] * expf(sG[tid]) * sRk[tid] : 0.f;
-    __syncthreads();
-
-    // ---- T = (I + A)^{-1}: the four 16 x 16 diagonal blocks by forward substitution
-    if (tid < C) {
-        const int b = tid >> 4, cc = tid & 15, base = b * 16;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-            for (int k4 = 0; k4 < r; k4 += 4) {
-                const float4 a4 = lds4(sA + (base + r) * LDA + base + k4);
-                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    if (k4 + kk < r) acc -= av[kk] * x[k4 + kk];
-            }
-            x[r] = (r < cc) ? 0.f : acc;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(base + r) * LDA + base + cc] = x[r];
-    }
-    __syncthreads();
-    // ---- then by doubling: blocks (1,0) and (3,2) of 16 x 16 (64 threads each), then
-    // block (1,0) of 32 x 32 (all threads): T_ij = -T_ii A_ij T_jj
-    {
-        const int pb = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
-        solve_block<16, 1>(sA, sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
-        __syncthreads();
-        apply_block<16, 1>(sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
-        __syncthreads();
-    }
-    {
-        const int r = tid >> 2, cg = tid & 3;
-        solve_block<32, 2>(sA, sT, sX, 32, 0, r, cg);
-        __syncthreads();
-        apply_block<32, 2>(sT, sX, 32, 0, r, cg);
-        __syncthreads();
-    }
-
-    // ---- T' = T diag(beta gamma rk) as hi/lo operand images in shared memory (for W),
-    // T'' = T diag(beta) straight into the record (two threads per row, 32 columns each)
-    {
-        const int t = tid >> 1, hh = tid & 1;
-        float tv[32], x[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 t4 = lds4(sT + t * LDA + hh * 32 + 4 * q);
-            tv[4 * q] = t4.x; tv[4 * q + 1] = t4.y; tv[4 * q + 2] = t4.z; tv[4 * q + 3] = t4.w;
-        }
-#pragma unroll
-        for (int q = 0; q < 32; q += 4) {
-            const float4 c4 = lds4(sC1 + hh * 32 + q);
-            x[q] = tv[q] * c4.x; x[q + 1] = tv[q + 1] * c4.y; x[q + 2] = tv[q + 2] * c4.z; x[q + 3] = tv[q + 3] * c4.w;
-        }
-        store_half_row_hilo(sT1, sT1 + 8192, t, hh * 4, x);
-#pragma unroll
-        for (int q = 0; q < 32; q += 4) {                    // beta is 0 past the end
-            const float4 b4 = lds4(sB + hh * 32 + q);
-            x[q] = tv[q] * b4.x; x[q + 1] = tv[q + 1] * b4.y; x[q + 2] = tv[q + 2] * b4.z; x[q + 3] = tv[q + 3] * b4.w;
-        }
-        store_half_row_hilo(rec + REC_T2HI, rec + REC_T2LO, t, hh * 4, x);
-    }
-    fence_async_smem();
     tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-        // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens) into columns 0-63;
-        // A is the key tile read MN-major
-        const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
+
+    for (int hh = 0; hh < ratio; ++hh) {
+        const int h = j * ratio + hh;
+        uint8_t *rec = reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h) * kRecBytes;
+        // every reader of the previous head's vectors, A and T' images is done
+        __syncthreads();
+        // gates of the chunk and the decay prefix (two warps, shuffle scan)
+        if (tid < C) {
+            const bool in = tid < len;
+            const size_t gi = (size_t)(t0 + tid) * p.HV + h;
+            float gv = in ? p.g[gi] : 0.f;
+            sg[tid] = gv;
+            sB[tid] = in ? p.beta[gi] : 0.f;
+            float x = gv;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ka = smem_desc(smem_u32(sK + ks * 2048), 8192, 1024, kSwizzle128B);
-            const uint32_t th = smem_u32(sT1 + ks * 32);
-            mma_bf16(tmem, ka, smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
-            mma_bf16(tmem, ka, smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
+            for (int o = 1; o < 32; o <<= 1) {
+                float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            sG[tid] = x;   // inclusive within the warp
         }
-        mma_commit(&bar[2]);
-    }
-    // ---- per-token factors
-    if (tid < C) {
-        float *sc = reinterpret_cast<float *>(rec + REC_F);
-        const bool in = tid < len;
-        const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid];
-        sc[SC_QD * C + tid] = in ? sRq[tid] * expf(G) : 0.f;
-        sc[SC_KD * C + tid] = in ? rk * expf(Gl - G) : 0.f;
-        sc[SC_RK * C + tid] = in ? rk : 0.f;
-        sc[SC_ALPHA * C + tid] = in ? expf(sg[tid]) : 0.f;
-        sc[SC_MISC * C + tid] = tid == 0 ? expf(Gl) : (tid == 1 ? (float)len : 0.f);
-    }
-    // ---- -W hi/lo: thread i holds row i (key i) of W^T, i.e. row i of the MN-major
-    // operand of the chain's first product
-    ok = mbar_wait(&bar[2], 0);
-    if (__syncthreads_or(!ok)) goto teardown;
-    tc_fence_after();
+        __syncthreads();
+        if (tid >= 32 && tid < C) sG[tid] += sG[31];
+        __syncthreads();
+        if (tid < C) sG2[tid] = sG[tid] * kLog2e;
+        __syncthreads();
+        {
+            // A_tj = beta_t e^{G_t-G_j} rk_t rk_j k_t.k_j (j < t) into smem and
+            // P_tj = e^{G_t-G_j} rq_t rk_j q_t.k_j (j <= t) into the record, one exponential
+            const bool live = trow < len;
+            const float G2t = sG2[trow], at = sB[trow] * sRk[trow], pt = sRq[trow];
+            float av[32], pv[32];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        float wv[32];
-        tmem_ld32(tmem + lb + half * 32, wv);
-        tmem_ld_wait();
+            for (int q4 = 0; q4 < 32; q4 += 4) {
+                const float4 g4 = lds4(sG2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
+                const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-        for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
-        store_half_row_hilo(rec + REC_WHI, rec + REC_WLO, tid, half * 4, wv);
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int q = q4 + qq, jj = tcb * 32 + q;
+                    const float e = (jj <= trow && jj < len) ? ex2_fast(G2t - gv[qq]) * rv[qq] : 0.f;
+                    av[q] = (live && jj < trow) ? at * e * gr[q] : 0.f;
+                    pv[q] = pt * e * qk[q];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                sts4(sA + trow * LDA + tcb * 32 + 4 * q, av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
+            store_half_row_bf16(rec + REC_P, trow, tcb * 4, pv);
+        }
+        if (tid < C) sC1[tid] = tid < len ? sB[tid] * expf(sG[tid]) * sRk[tid] : 0.f;
+        __syncthreads();
+
+        // ---- T = (I + A)^{-1}: the four 16 x 16 diagonal blocks by forward substitution
+        if (tid < C) {
+            const int b = tid >> 4, cc = tid & 15, base = b * 16;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+                for (int k4 = 0; k4 < r; k4 += 4) {
+                    const float4 a4 = lds4(sA + (base + r) * LDA + base + k4);
+                    const float aw[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        if (k4 + kk < r) acc -= aw[kk] * x[k4 + kk];
+                }
+                x[r] = (r < cc) ? 0.f : acc;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(base + r) * LDA + base + cc] = x[r];
+        }
+        __syncthreads();
+        // ---- then by doubling: blocks (1,0) and (3,2) of 16 x 16 (64 threads each), then
+        // block (1,0) of 32 x 32 (all threads): T_ij = -T_ii A_ij T_jj
+        {
+            const int pb = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
+            solve_block<16, 1>(sA, sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
+            __syncthreads();
+            apply_block<16, 1>(sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
+            __syncthreads();
+        }
+        {
+            const int r = tid >> 2, cg = tid & 3;
+            solve_block<32, 2>(sA, sT, sX, 32, 0, r, cg);
+            __syncthreads();
+            apply_block<32, 2>(sT, sX, 32, 0, r, cg);
+            __syncthreads();
+        }
+
+        // ---- T' = T diag(beta gamma rk) as hi/lo operand images in shared memory (for W),
+        // T'' = T diag(beta) straight into the record (two threads per row, 32 columns each)
+        {
+            const int t = tid >> 1, hh2 = tid & 1;
+            float tv[32], x[32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 t4 = lds4(sT + t * LDA + hh2 * 32 + 4 * q);
+                tv[4 * q] = t4.x; tv[4 * q + 1] = t4.y; tv[4 * q + 2] = t4.z; tv[4 * q + 3] = t4.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {
+                const float4 c4 = lds4(sC1 + hh2 * 32 + q);
+                x[q] = tv[q] * c4.x; x[q + 1] = tv[q + 1] * c4.y; x[q + 2] = tv[q + 2] * c4.z; x[q + 3] = tv[q + 3] * c4.w;
+            }
+            store_half_row_hilo(sT1, sT1 + 8192, t, hh2 * 4, x);
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {                    // beta is 0 past the end
+                const float4 b4 = lds4(sB + hh2 * 32 + q);
+                x[q] = tv[q] * b4.x; x[q + 1] = tv[q + 1] * b4.y; x[q + 2] = tv[q + 2] * b4.z; x[q + 3] = tv[q + 3] * b4.w;
+            }
+            store_half_row_hilo(rec + REC_T2HI, rec + REC_T2LO, t, hh2 * 4, x);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens) into columns 0-63;
+            // A is the key tile read MN-major
+            const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ka = smem_desc(smem_u32(sK + ks * 2048), 8192, 1024, kSwizzle128B);
+                const uint32_t th = smem_u32(sT1 + ks * 32);
+                mma_bf16(tmem, ka, smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
+                mma_bf16(tmem, ka, smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
+            }
+            mma_commit(&bar[2]);
+        }
+        // ---- per-token factors
+        if (tid < C) {
+            float *sc = reinterpret_cast<float *>(rec + REC_F);
+            const bool in = tid < len;
+            const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid];
+            sc[SC_QD * C + tid] = in ? sRq[tid] * expf(G) : 0.f;
+            sc[SC_KD * C + tid] = in ? rk * expf(Gl - G) : 0.f;
+            sc[SC_RK * C + tid] = in ? rk : 0.f;
+            sc[SC_ALPHA * C + tid] = in ? expf(sg[tid]) : 0.f;
+            sc[SC_MISC * C + tid] = tid == 0 ? expf(Gl) : (tid == 1 ? (float)len : 0.f);
+        }
+        // ---- -W hi/lo: thread i holds row i (key i) of W^T, i.e. row i of the MN-major
+        // operand of the chain's first product
+        ok = mbar_wait(&bar[2], hh & 1);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float wv[32];
+            tmem_ld32(tmem + lb + half * 32, wv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
+            store_half_row_hilo(rec + REC_WHI, rec + REC_WLO, tid, half * 4, wv);
+        }
+        tc_fence_before();
     }
 teardown:
     if (!ok && tid == 0) set_error(p, GDN_ERR_TIMEOUT);
@@ -1157,7 +1172,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kPrepSmem)) != cudaSuccess)
             return e;
-        prep_kernel<<<dim3(pp.max_chunks, pp.HV), kPrepThreads, kPrepSmem, st>>>(mk, mq, p);
+        prep_kernel<<<dim3(pp.max_chunks, pp.HK), kPrepThreads, kPrepSmem, st>>>(mk, mq, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (pp.N > 0) {
