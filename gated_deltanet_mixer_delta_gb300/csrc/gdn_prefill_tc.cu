@@ -271,6 +271,9 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     uint64_t *bar = reinterpret_cast<uint64_t *>(sC1 + C);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
 
+    // the chain kernel may be scheduled as soon as every prep CTA has started; it waits for
+    // this grid's completion before it reads a record
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // one CTA per (chunk, key head j): the key and query tiles, K K^T, Q K^T and the norms
     // are shared by the value heads j r .. j r + r - 1 (r = HV / HK), which are handled one
     // after the other
@@ -671,7 +674,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     const int s = p.cu_seqlens ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
     SeqRange sr;
     if (!seq_range(p, s, sr)) return;
-    if (!p.cu_seqlens && vs == 0 && h == 0 && s == 0 && tid == 0) p.status[kStatusWord] = GDN_OK;
     const int j = h / (p.HV / p.HK);
     const int nch = sr.count;
 
@@ -753,6 +755,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 return true;
             };
             bool issued = false;
+            // the records come from the prep grid, which may still be running
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             // iteration cc: (once -W S of chunk cc - 2 is done) T'' V of chunk cc - 1, then
             // the loads of chunk cc; the last iteration only issues T'' V of chunk nch - 1.
             // T'' V of chunk 0 waits for its inputs, so it follows the loads of chunk 1.
@@ -1150,6 +1154,10 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     if ((size_t)pp.rec_floats * sizeof(float) < (size_t)kRecBytes) return cudaErrorInvalidValue;
     if (pp.cu_seqlens) {
         if ((e = launch_chunk_table(pp, st)) != cudaSuccess) return e;
+    } else {
+        // both kernels only ever move the status word from GDN_OK to an error code, so it
+        // starts clean here (a reused workspace may hold the last call's error)
+        if ((e = cudaMemsetAsync(pp.status, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return e;
     }
     Params p;
     memset(&p, 0, sizeof p);
@@ -1180,8 +1188,21 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kChainSmem)) != cudaSuccess)
             return e;
-        kern<<<dim3(D / NV, pp.HV, pp.N), kChainThreads, kChainSmem, st>>>(mk, mq, mv, p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // programmatic dependent launch: the chain's CTAs may start (barriers, TMEM, the
+        // initial state) while the last prep CTAs finish; its producer waits for the prep
+        // grid before the first record copy
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(D / NV, pp.HV, pp.N);
+        cfg.blockDim = dim3(kChainThreads);
+        cfg.dynamicSmemBytes = kChainSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = pp.max_chunks > 0 ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, kern, mk, mq, mv, p)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

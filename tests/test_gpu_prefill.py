@@ -155,6 +155,21 @@ def test_varlen_bad_cu_seqlens_sets_status_and_writes_nothing(gdn):
     assert gdn.workspace_status(ws) == 0
 
 
+def test_equal_length_prefill_clears_a_stale_status(gdn):
+    """A workspace that still holds the last call's error reports OK after a good call."""
+    T = 96
+    d = _cuda(workloads.draw_inputs(2, T, 2, 4, 128, 128, torch.bfloat16, 23))
+    ws = torch.empty(gdn.workspace_size(2 * T, 3, 4, 128, 128), dtype=torch.uint8, device="cuda")
+    cu = torch.tensor([0, 100, 50, 192], dtype=torch.int32, device="cuda")
+    flat = {k: d[k].reshape(1, 2 * T, *d[k].shape[2:]) for k in
+            ("queries", "keys", "values", "decays", "beta")}
+    gdn.prefill_varlen(flat["queries"], flat["keys"], flat["values"], flat["decays"],
+                       flat["beta"], cu, workspace=ws)
+    assert gdn.workspace_status(ws) == -7
+    gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"], workspace=ws)
+    assert gdn.workspace_status(ws) == 0
+
+
 def test_prefill_then_decode_continues_the_state(gdn):
     """prefill(t) then T-t decode steps gives the same outputs and state as prefill(T)."""
     d = _cuda(_inputs(3, 96, 2, 4, 128, torch.bfloat16, seed=8, s0=True, g_mode="weak"))
