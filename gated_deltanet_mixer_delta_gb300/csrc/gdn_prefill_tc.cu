@@ -12,11 +12,12 @@
 // products accumulated in fp32 in TMEM: x*y ~ hi(x)hi(y) + hi(x)lo(y) + lo(x)hi(y).
 //
 // Two kernels:
-//  prep  -- one CTA per (chunk, value head), all independent: TMA the key and query
-//           tiles, Gram K K^T and Q K^T on the tensor core, norms, decay prefix, A, then
-//           T = (I + A)^{-1} by a blocked forward substitution in fp32 (16 x 16 diagonal
-//           blocks, then block rows), W^T = K^T T'^T on the tensor core, P; writes -W
-//           (hi/lo), T'' (hi/lo) and P as operand images, and the per-token factors.
+//  prep  -- one CTA per (chunk, one or two value heads of a key head), all independent:
+//           TMA the key and query tiles, Gram K K^T and Q K^T on the tensor core, norms,
+//           decay prefix, A, then T = (I + A)^{-1} in place of A by a blocked forward
+//           substitution in fp32 (16 x 16 diagonal blocks, then doubling),
+//           W^T = K^T T'^T on the tensor core, P; writes -W (hi/lo), T'' (hi/lo) and P
+//           as operand images, and the per-token factors.
 //  chain -- one CTA per (sequence, value head, 32-wide value slice), the sequential
 //           chunk loop, warp-specialised (256 threads): a TMA producer warp, a warp that
 //           issues the products off the chain's critical path, two output warps, and an
@@ -150,16 +151,35 @@ __device__ __forceinline__ void store_half_row_bf16(uint8_t *img, int row, int c
 }
 
 // ================================================================== prep kernel
-// One CTA per (chunk, value head).  smem (from a 1024-aligned base):
+// One CTA per (chunk, HPC value heads that share a key head): HPC = 2 when the number of
+// value heads per key head is even, else 1.  The key and query tiles, K K^T, Q K^T and the
+// norms are shared by the CTA's heads, and the heads go through every step side by side,
+// so that they share the barriers and their independent work fills each other's latency.
+// The record images are assembled in shared memory and written with bulk copies (whole
+// lines, off the threads' critical path).
+// smem (from a 1024-aligned base):
 //   key tile   [2][64][128 B], 128B swizzle (TMA)
-//   query tile [2][64][128 B], 128B swizzle (TMA); once Q K^T is done it holds the X
-//              scratch of the solve, then the T' hi/lo operand images
-//   A [64][68] | T [64][68] fp32 (rows 16-byte aligned) | per-token vectors | barriers
+//   query tile [2][64][128 B], 128B swizzle (TMA); once Q K^T is done it stages the P
+//              images, then holds the X scratch of the solve ([HPC][1152] fp32), then
+//              the T' hi/lo operand images of one head at a time
+//   A/T [HPC][64][68] fp32: A of each head, overwritten in place by T = (I + A)^{-1},
+//              then by the T'' images of the head, then (two heads) by -W of head 0
+//   rk, rq | per head: G, G log2(e), beta, beta gamma rk | barriers
+// After the last product the key and query tiles stage -W of the last head.
 constexpr int kPrepThreads = 128;
 constexpr int LDA = C + 4;
-constexpr int kPrepVec = 7;                                  // per-token vectors of C floats
-constexpr size_t kPrepSmem = 1024 /*align*/ + 32768 + 2 * C * LDA * 4 + kPrepVec * C * 4 + 64;
-constexpr uint32_t kPrepTmemCols = 128;                      // Gram / W^T (0-63), Q K^T (64-127)
+constexpr int LDX = 36;                                      // X scratch rows (32 columns used)
+constexpr int kXHead = 2 * 16 * LDX;                         // == 32 * LDX floats per head
+constexpr int kPrepVecHead = 4;
+template <int HPC>
+constexpr size_t prep_smem_bytes() {
+    return 1024 /*align*/ + 32768 + (size_t)HPC * C * LDA * 4 +
+           (size_t)(2 + HPC * kPrepVecHead) * C * 4 + 64;
+}
+static_assert(2 * kXHead * 4 <= 16384, "solve scratch of two heads fits the query tile");
+static_assert(2 * C * LDA * 4 >= 32768 && C * LDA * 4 >= 16384, "A/T tiles stage the images");
+static_assert(REC_T2LO == REC_T2HI + 8192 && REC_WLO == REC_WHI + 16384, "record layout");
+constexpr uint32_t kPrepTmemCols = 128;                      // K K^T | Q K^T, then W^T of head 0 | 1
 
 // 2^x on the MUFU unit (relative error ~2^-22); underflows to 0.
 __device__ __forceinline__ float ex2_fast(float x) {
@@ -172,6 +192,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void sts4(float *p, float a, float b, float c, float d) {
     *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ float f4get(const float4 &v, int e) {
+    return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
 }
 
 // One row of an M = 64 accumulator pair (columns c0 .. c0+63) spread over a warp: the
@@ -190,95 +213,138 @@ __device__ __forceinline__ void tmem_row_split(uint32_t taddr, float (&x)[32]) {
     }
 }
 
-// Off-diagonal block of T = (I + A)^{-1} from two diagonal blocks already in T:
+// Off-diagonal block of T = (I + A)^{-1} from two diagonal blocks already in T, with A
+// and T in one array (T overwrites A block by block):
 //   X = A[rows, cols] T[cols, cols];  T[rows, cols] = -T[rows, rows] X
-// for an n x n block (n = 16 or 32) at row offset r0 and column offset c0; thread
-// (r, cg) computes a 1 x 4*NQ strip.  Full-length loops: T and A are zero above their
-// diagonals, so no bounds are needed.
-template <int N, int NQ>
-__device__ __forceinline__ void solve_block(float *sA, float *sT, float *sX, int r0, int c0, int r,
-                                            int cg) {
-    const int cx = cg * 4 * NQ;
-    float acc[4 * NQ];
+// for an N x N block (N = 16 or 32) at row offset r0 and column offset c0.  Thread
+// (tr, tc) owns rows tr, tr + 8, .. (RT of them) and columns 4 tc .. 4 tc + 3 of the block:
+// per k-step it reads one float4 of each of its rows and one float4 of the right-hand
+// factor, so that the eight lanes of a quarter-warp hit distinct banks.  Full-length
+// loops: T is zero above its diagonal and the A block read is wholly below it.  The A
+// block is read by solve_tile and replaced by apply_tile; a barrier separates the two.
+template <int N, int RT>
+__device__ __forceinline__ void solve_tile(const float *sAT, float *sX, int r0, int c0, int tr, int tc) {
+    float acc[RT][4];
 #pragma unroll
-    for (int e = 0; e < 4 * NQ; ++e) acc[e] = 0.f;
+    for (int a = 0; a < RT; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
 #pragma unroll
     for (int m4 = 0; m4 < N; m4 += 4) {
-        const float4 a4 = lds4(sA + (r0 + r) * LDA + c0 + m4);
-        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+        float4 a4[RT];
+#pragma unroll
+        for (int a = 0; a < RT; ++a) a4[a] = lds4(sAT + (r0 + tr + 8 * a) * LDA + c0 + m4);
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
-            const float a = av[mm];
+            const float4 t4 = lds4(sAT + (c0 + m4 + mm) * LDA + c0 + 4 * tc);
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const float4 t4 = lds4(sT + (c0 + m4 + mm) * LDA + c0 + cx + 4 * q);
-                acc[4 * q] += a * t4.x; acc[4 * q + 1] += a * t4.y;
-                acc[4 * q + 2] += a * t4.z; acc[4 * q + 3] += a * t4.w;
+            for (int a = 0; a < RT; ++a) {
+                const float av = f4get(a4[a], mm);
+                acc[a][0] += av * t4.x; acc[a][1] += av * t4.y;
+                acc[a][2] += av * t4.z; acc[a][3] += av * t4.w;
             }
         }
     }
 #pragma unroll
-    for (int q = 0; q < NQ; ++q)
-        sts4(sX + r * LDA + cx + 4 * q, acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    for (int a = 0; a < RT; ++a)
+        sts4(sX + (tr + 8 * a) * LDX + 4 * tc, acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
 }
-template <int N, int NQ>
-__device__ __forceinline__ void apply_block(float *sT, const float *sX, int r0, int c0, int r,
-                                            int cg) {
-    const int cx = cg * 4 * NQ;
-    float acc[4 * NQ];
+template <int N, int RT>
+__device__ __forceinline__ void apply_tile(float *sAT, const float *sX, int r0, int c0, int tr, int tc) {
+    float acc[RT][4];
 #pragma unroll
-    for (int e = 0; e < 4 * NQ; ++e) acc[e] = 0.f;
+    for (int a = 0; a < RT; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
 #pragma unroll
     for (int m4 = 0; m4 < N; m4 += 4) {
-        const float4 t4v = lds4(sT + (r0 + r) * LDA + r0 + m4);
-        const float tv[4] = {t4v.x, t4v.y, t4v.z, t4v.w};
+        float4 t4[RT];
+#pragma unroll
+        for (int a = 0; a < RT; ++a) t4[a] = lds4(sAT + (r0 + tr + 8 * a) * LDA + r0 + m4);
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
-            const float t = tv[mm];
+            const float4 x4 = lds4(sX + (m4 + mm) * LDX + 4 * tc);
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const float4 x4 = lds4(sX + (m4 + mm) * LDA + cx + 4 * q);
-                acc[4 * q] += t * x4.x; acc[4 * q + 1] += t * x4.y;
-                acc[4 * q + 2] += t * x4.z; acc[4 * q + 3] += t * x4.w;
+            for (int a = 0; a < RT; ++a) {
+                const float tv = f4get(t4[a], mm);
+                acc[a][0] += tv * x4.x; acc[a][1] += tv * x4.y;
+                acc[a][2] += tv * x4.z; acc[a][3] += tv * x4.w;
             }
         }
     }
 #pragma unroll
-    for (int q = 0; q < NQ; ++q)
-        sts4(sT + (r0 + r) * LDA + c0 + cx + 4 * q, -acc[4 * q], -acc[4 * q + 1], -acc[4 * q + 2],
-             -acc[4 * q + 3]);
+    for (int a = 0; a < RT; ++a)
+        sts4(sAT + (r0 + tr + 8 * a) * LDA + c0 + 4 * tc, -acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
 }
 
+// x (32 columns of a row of T) times diag(col) as hi/lo images (row t, chunks 4 half ..)
+__device__ __forceinline__ void store_scaled_row(const float (&tv)[32], const float *col, int t,
+                                                 int half, uint8_t *img_hi, uint8_t *img_lo) {
+    float x[32];
+#pragma unroll
+    for (int q = 0; q < 32; q += 4) {
+        const float4 c4 = lds4(col + half * 32 + q);
+        x[q] = tv[q] * c4.x; x[q + 1] = tv[q + 1] * c4.y; x[q + 2] = tv[q + 2] * c4.z; x[q + 3] = tv[q + 3] * c4.w;
+    }
+    store_half_row_hilo(img_hi, img_lo, t, half * 4, x);
+}
+
+// W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens) into TMEM columns
+// col .. col + 63; A is the key tile read MN-major, B the T' hi and lo images
+__device__ __forceinline__ void issue_w(uint32_t tmem_col, const uint8_t *sK, const uint8_t *sT1,
+                                        uint64_t *bar) {
+    const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t ka = smem_desc(smem_u32(sK + ks * 2048), 8192, 1024, kSwizzle128B);
+        const uint32_t th = smem_u32(sT1 + ks * 32);
+        mma_bf16(tmem_col, ka, smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
+        mma_bf16(tmem_col, ka, smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
+    }
+    mma_commit(bar);
+}
+
+// -W hi/lo images (hi at img, lo at img + 16 KiB): thread i holds row i (key i) of W^T,
+// i.e. row i of the MN-major operand of the chain's first product
+__device__ __forceinline__ void stage_minus_w(uint32_t taddr, uint8_t *img, int tid) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float wv[32];
+        tmem_ld32(taddr + half * 32, wv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
+        store_half_row_hilo(img, img + 16384, tid, half * 4, wv);
+    }
+}
+
+template <int HPC>
 __global__ void __launch_bounds__(kPrepThreads, 3)
 prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
             Params p) {
+    static_assert(HPC == 1 || HPC == 2, "one or two value heads per CTA");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t su = smem_u32(smem_raw);
     uint8_t *sm = smem_raw + (((su + 1023u) & ~1023u) - su);
     uint8_t *sK = sm;                                   // [2][64][128 B]
     uint8_t *sQ = sm + 16384;                           // [2][64][128 B]
-    float *sX = reinterpret_cast<float *>(sQ);          // [32][68], during the solve
+    float *sX = reinterpret_cast<float *>(sQ);          // [HPC][kXHead], during the solve
     uint8_t *sT1 = sQ;                                  // T' hi | lo images, after the solve
-    float *sA = reinterpret_cast<float *>(sm + 32768);  // [64][68]
-    float *sT = sA + C * LDA;                           // [64][68]
-    float *sG = sT + C * LDA;                           // decay prefix (natural log)
-    float *sG2 = sG + C;                                // decay prefix * log2(e)
-    float *sB = sG2 + C;                                // beta
-    float *sRk = sB + C;                                // key normaliser
+    float *sAT = reinterpret_cast<float *>(sm + 32768); // [HPC][64][68]
+    uint8_t *sAT8 = sm + 32768;
+    float *sRk = sAT + HPC * C * LDA;                   // key normaliser
     float *sRq = sRk + C;                               // query normaliser (with the scale)
-    float *sg = sRq + C;                                // g
-    float *sC1 = sg + C;                                // beta gamma rk (0 past the chunk end)
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sC1 + C);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    float *sV = sRq + C;                                // [HPC][4][64] per-head vectors
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sV + HPC * kPrepVecHead * C);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    // per-head vectors: decay prefix (natural log), the same times log2(e), beta,
+    // beta gamma rk (0 past the chunk end)
+    auto vG = [&](int i) { return sV + (i * kPrepVecHead + 0) * C; };
+    auto vG2 = [&](int i) { return sV + (i * kPrepVecHead + 1) * C; };
+    auto vB = [&](int i) { return sV + (i * kPrepVecHead + 2) * C; };
+    auto vC1 = [&](int i) { return sV + (i * kPrepVecHead + 3) * C; };
 
     // the chain kernel may be scheduled as soon as every prep CTA has started; it waits for
     // this grid's completion before it reads a record
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // one CTA per (chunk, key head j): the key and query tiles, K K^T, Q K^T and the norms
-    // are shared by the value heads j r .. j r + r - 1 (r = HV / HK), which are handled one
-    // after the other
-    const int c = blockIdx.x, j = blockIdx.y;
-    const int ratio = p.HV / p.HK;
+    const int c = blockIdx.x, h0 = blockIdx.y * HPC;
+    const int j = h0 / (p.HV / p.HK);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // chunk -> (sequence, first token, length)
     int64_t t0;
@@ -295,32 +361,58 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         t0 = (int64_t)s * p.T_seq + (int64_t)local * C;
         len = min(C, p.T_seq - local * C);
     }
+    auto record = [&](int i) {
+        return reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h0 + i) * kRecBytes;
+    };
 
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(&bar[b], 1);
+        for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
         prefetch_tensormap(&mapK);
         prefetch_tensormap(&mapQ);
-    }
-    if (warp == 0) { tmem_alloc(tslot, kPrepTmemCols); tmem_relinquish(); }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t lb = (uint32_t)(warp * 32) << 16;    // this warp's TMEM lanes
-    const int trow = warp * 16 + (lane & 15), tcb = lane >> 4;   // row / column half of
-                                                                  // the M = 64 results
-    float gr[32], qk[32];                               // Gram and Q K^T: row trow, 32 columns
-    bool ok = true;
-
-    if (tid == 0) {
         mbar_arrive_expect_tx(&bar[0], 32768);
         tma_load_3d(sK, &mapK, &bar[0], 0, j, (int)t0);
         tma_load_3d(sK + 8192, &mapK, &bar[0], 64, j, (int)t0);
         tma_load_3d(sQ, &mapQ, &bar[0], 0, j, (int)t0);
         tma_load_3d(sQ + 8192, &mapQ, &bar[0], 64, j, (int)t0);
     }
-    // T starts as zero (its upper part stays zero for every head)
-    for (int e = tid; e < C * LDA / 4; e += kPrepThreads) sts4(sT + 4 * e, 0.f, 0.f, 0.f, 0.f);
+    if (warp == 0) { tmem_alloc(tslot, kPrepTmemCols); tmem_relinquish(); }
+    // gate thread (head gh, token gt): its gate and beta are requested before anything
+    // waits, and it scans the decay prefix of its head (two warps per head)
+    const int gh = tid >> 6, gt = tid & 63;
+    const bool gthr = gh < HPC;
+    const bool gin = gthr && gt < len;
+    float g_in = 0.f, b_in = 0.f;
+    if (gin) {
+        const size_t gi = (size_t)(t0 + gt) * p.HV + h0 + gh;
+        g_in = p.g[gi];
+        b_in = p.beta[gi];
+    }
+    float Gx = g_in;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, Gx, o);
+        if (lane >= o) Gx += y;
+    }
+    if (gthr) vG(gh)[gt] = Gx;                          // inclusive within the warp
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;    // this warp's TMEM lanes
+    const int trow = warp * 16 + (lane & 15), tcb = lane >> 4;   // row / column half of
+                                                                  // the M = 64 results
+    const int hrow = tid >> 1, hhalf = tid & 1;         // row / column half, 2 threads a row
+    float gr[32], qk[32];                               // Gram and Q K^T: row trow, 32 columns
+    bool ok = true;
+
+    if (gthr) {
+        if (gt >= 32) {
+            Gx += vG(gh)[31];
+            vG(gh)[gt] = Gx;
+        }
+        vG2(gh)[gt] = Gx * kLog2e;
+        vB(gh)[gt] = b_in;
+    }
     ok = mbar_wait(&bar[0], 0);
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
@@ -340,12 +432,11 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     // query normalisers: two threads per row; the 16-byte chunks are visited in an order
     // that keeps the eight lanes of a quarter-warp on distinct banks
     {
-        const int row = tid >> 1, half = tid & 1;
-        const uint8_t *src = sQ + half * 8192 + row * 128;
+        const uint8_t *src = sQ + hhalf * 8192 + hrow * 128;
         float ss = 0.f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const int pc = q ^ (row & 7) ^ (half * 4);
+            const int pc = q ^ (hrow & 7) ^ (hhalf * 4);
             const uint4 w4 = *reinterpret_cast<const uint4 *>(src + pc * 16);
             const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
 #pragma unroll
@@ -355,13 +446,12 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
             }
         }
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (half == 0) sRq[row] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
+        if (hhalf == 0) sRq[hrow] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
     }
     ok = mbar_wait(&bar[1], 0) && mbar_wait(&bar[3], 0);
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
-    // Gram and Q K^T rows into registers (they serve every value head); the key
-    // normaliser from the Gram diagonal
+    // Gram and Q K^T rows into registers; the key normaliser from the Gram diagonal
     tmem_row_split(tmem + lb, gr);
     tmem_row_split(tmem + lb + 64, qk);
     {
@@ -371,41 +461,22 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
         if ((trow >> 5) == tcb) sRk[trow] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
     }
     tc_fence_before();
-
-    for (int hh = 0; hh < ratio; ++hh) {
-        const int h = j * ratio + hh;
-        uint8_t *rec = reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h) * kRecBytes;
-        // every reader of the previous head's vectors, A and T' images is done
-        __syncthreads();
-        // gates of the chunk and the decay prefix (two warps, shuffle scan)
-        if (tid < C) {
-            const bool in = tid < len;
-            const size_t gi = (size_t)(t0 + tid) * p.HV + h;
-            float gv = in ? p.g[gi] : 0.f;
-            sg[tid] = gv;
-            sB[tid] = in ? p.beta[gi] : 0.f;
-            float x = gv;
+    __syncthreads();
+    if (gthr) vC1(gh)[gt] = gin ? b_in * expf(Gx) * sRk[gt] : 0.f;
+    {
+        // per head: A_tj = beta_t e^{G_t-G_j} rk_t rk_j k_t.k_j (j < t) into shared memory
+        // and P_tj = e^{G_t-G_j} rq_t rk_j q_t.k_j (j <= t) as an image in the free query
+        // tile, one exponential for both
+        const bool live = trow < len;
+        const float rkt = sRk[trow], pt = sRq[trow];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                float y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            sG[tid] = x;   // inclusive within the warp
-        }
-        __syncthreads();
-        if (tid >= 32 && tid < C) sG[tid] += sG[31];
-        __syncthreads();
-        if (tid < C) sG2[tid] = sG[tid] * kLog2e;
-        __syncthreads();
-        {
-            // A_tj = beta_t e^{G_t-G_j} rk_t rk_j k_t.k_j (j < t) into smem and
-            // P_tj = e^{G_t-G_j} rq_t rk_j q_t.k_j (j <= t) into the record, one exponential
-            const bool live = trow < len;
-            const float G2t = sG2[trow], at = sB[trow] * sRk[trow], pt = sRq[trow];
+        for (int i = 0; i < HPC; ++i) {
+            const float *G2 = vG2(i);
+            const float G2t = G2[trow], at = vB(i)[trow] * rkt;
             float av[32], pv[32];
 #pragma unroll
             for (int q4 = 0; q4 < 32; q4 += 4) {
-                const float4 g4 = lds4(sG2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
+                const float4 g4 = lds4(G2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
                 const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
@@ -415,18 +486,28 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
                     pv[q] = pt * e * qk[q];
                 }
             }
+            float *sA = sAT + i * C * LDA;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 sts4(sA + trow * LDA + tcb * 32 + 4 * q, av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
-            store_half_row_bf16(rec + REC_P, trow, tcb * 4, pv);
+            store_half_row_bf16(sQ + i * 8192, trow, tcb * 4, pv);
         }
-        if (tid < C) sC1[tid] = tid < len ? sB[tid] * expf(sG[tid]) * sRk[tid] : 0.f;
-        __syncthreads();
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < HPC; ++i) bulk_store(record(i) + REC_P, sQ + i * 8192, 8192);
+        bulk_commit();
+    }
 
-        // ---- T = (I + A)^{-1}: the four 16 x 16 diagonal blocks by forward substitution
-        if (tid < C) {
-            const int b = tid >> 4, cc = tid & 15, base = b * 16;
-            float x[16];
+    // ---- T = (I + A)^{-1}, in place: the four 16 x 16 diagonal blocks of each head by
+    // forward substitution (one thread per column), written once every thread has read A
+    {
+        const int dh = tid >> 6, b = (tid >> 4) & 3, cc = tid & 15, base = b * 16;
+        float *sA = sAT + (dh < HPC ? dh : 0) * C * LDA;
+        float x[16];
+        if (dh < HPC) {
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 float acc = (r == cc) ? 1.f : 0.f;
@@ -440,96 +521,120 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
                 }
                 x[r] = (r < cc) ? 0.f : acc;
             }
+        }
+        // the P images have left the query tile before it becomes the solve's scratch
+        if (tid == 0) bulk_wait_read_all();
+        __syncthreads();
+        if (dh < HPC) {
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(base + r) * LDA + base + cc] = x[r];
+            for (int r = 0; r < 16; ++r) sA[(base + r) * LDA + base + cc] = x[r];
         }
         __syncthreads();
-        // ---- then by doubling: blocks (1,0) and (3,2) of 16 x 16 (64 threads each), then
-        // block (1,0) of 32 x 32 (all threads): T_ij = -T_ii A_ij T_jj
-        {
-            const int pb = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
-            solve_block<16, 1>(sA, sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
-            __syncthreads();
-            apply_block<16, 1>(sT, sX + pb * 16 * LDA, 16 + 32 * pb, 32 * pb, r, cg);
-            __syncthreads();
-        }
-        {
-            const int r = tid >> 2, cg = tid & 3;
-            solve_block<32, 2>(sA, sT, sX, 32, 0, r, cg);
-            __syncthreads();
-            apply_block<32, 2>(sT, sX, 32, 0, r, cg);
-            __syncthreads();
-        }
+    }
+    // ---- then by doubling, 64 threads per head: blocks (1,0) and (3,2) of 16 x 16 (a warp
+    // each, 2 x 4 tiles), then block (1,0) of 32 x 32 (4 x 4 tiles): T_ij = -T_ii A_ij T_jj
+    if ((tid >> 6) < HPC) {
+        const int i = tid >> 6, pb = (tid >> 5) & 1;
+        float *sATi = sAT + i * C * LDA, *sXi = sX + i * kXHead;
+        solve_tile<16, 2>(sATi, sXi + pb * 16 * LDX, 16 + 32 * pb, 32 * pb, lane >> 2, lane & 3);
+    }
+    __syncthreads();
+    if ((tid >> 6) < HPC) {
+        const int i = tid >> 6, pb = (tid >> 5) & 1;
+        float *sATi = sAT + i * C * LDA, *sXi = sX + i * kXHead;
+        apply_tile<16, 2>(sATi, sXi + pb * 16 * LDX, 16 + 32 * pb, 32 * pb, lane >> 2, lane & 3);
+    }
+    __syncthreads();
+    if ((tid >> 6) < HPC) {
+        const int i = tid >> 6, t = tid & 63;
+        solve_tile<32, 4>(sAT + i * C * LDA, sX + i * kXHead, 32, 0, t >> 3, t & 7);
+    }
+    __syncthreads();
+    if ((tid >> 6) < HPC) {
+        const int i = tid >> 6, t = tid & 63;
+        apply_tile<32, 4>(sAT + i * C * LDA, sX + i * kXHead, 32, 0, t >> 3, t & 7);
+    }
+    __syncthreads();
 
-        // ---- T' = T diag(beta gamma rk) as hi/lo operand images in shared memory (for W),
-        // T'' = T diag(beta) straight into the record (two threads per row, 32 columns each)
-        {
-            const int t = tid >> 1, hh2 = tid & 1;
-            float tv[32], x[32];
+    {
+        // rows of T (two threads a row, 32 columns each) into registers, then:
+        // T' = T diag(beta gamma rk) of head 0 as operand images for W in the query tile,
+        // T'' = T diag(beta) of every head as images in place of its T, bulk-copied out
+        float tv[HPC][32];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 t4 = lds4(sT + t * LDA + hh2 * 32 + 4 * q);
-                tv[4 * q] = t4.x; tv[4 * q + 1] = t4.y; tv[4 * q + 2] = t4.z; tv[4 * q + 3] = t4.w;
-            }
+        for (int i = 0; i < HPC; ++i)
 #pragma unroll
             for (int q = 0; q < 32; q += 4) {
-                const float4 c4 = lds4(sC1 + hh2 * 32 + q);
-                x[q] = tv[q] * c4.x; x[q + 1] = tv[q + 1] * c4.y; x[q + 2] = tv[q + 2] * c4.z; x[q + 3] = tv[q + 3] * c4.w;
+                const float4 t4 = lds4(sAT + i * C * LDA + hrow * LDA + hhalf * 32 + q);
+                tv[i][q] = t4.x; tv[i][q + 1] = t4.y; tv[i][q + 2] = t4.z; tv[i][q + 3] = t4.w;
             }
-            store_half_row_hilo(sT1, sT1 + 8192, t, hh2 * 4, x);
-#pragma unroll
-            for (int q = 0; q < 32; q += 4) {                    // beta is 0 past the end
-                const float4 b4 = lds4(sB + hh2 * 32 + q);
-                x[q] = tv[q] * b4.x; x[q + 1] = tv[q + 1] * b4.y; x[q + 2] = tv[q + 2] * b4.z; x[q + 3] = tv[q + 3] * b4.w;
-            }
-            store_half_row_hilo(rec + REC_T2HI, rec + REC_T2LO, t, hh2 * 4, x);
-        }
+        store_scaled_row(tv[0], vC1(0), hrow, hhalf, sT1, sT1 + 8192);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (tid == 0) issue_w(tmem, sK, sT1, &bar[2]);
+#pragma unroll
+        for (int i = 0; i < HPC; ++i)
+            store_scaled_row(tv[i], vB(i), hrow, hhalf, sAT8 + i * C * LDA * 4, sAT8 + i * C * LDA * 4 + 8192);
+        // ---- per-token factors of every head (one coalesced row each)
+        if (gthr) {
+            float *sc = reinterpret_cast<float *>(record(gh) + REC_F);
+            const float Gl = vG(gh)[len - 1], rk = sRk[gt];
+            sc[SC_QD * C + gt] = gin ? sRq[gt] * expf(Gx) : 0.f;
+            sc[SC_KD * C + gt] = gin ? rk * expf(Gl - Gx) : 0.f;
+            sc[SC_RK * C + gt] = gin ? rk : 0.f;
+            sc[SC_ALPHA * C + gt] = gin ? expf(g_in) : 0.f;
+            sc[SC_MISC * C + gt] = gt == 0 ? expf(Gl) : (gt == 1 ? (float)len : 0.f);
+        }
+        fence_async_smem();
+        __syncthreads();
         if (tid == 0) {
-            // W^T = K^T T'^T (M = 128 keys, N = 64 tokens, K = 64 tokens) into columns 0-63;
-            // A is the key tile read MN-major
-            const uint32_t id_w = instr_desc(128, 64, kFmtBF16, 1, 0);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ka = smem_desc(smem_u32(sK + ks * 2048), 8192, 1024, kSwizzle128B);
-                const uint32_t th = smem_u32(sT1 + ks * 32);
-                mma_bf16(tmem, ka, smem_desc(th, 16, 1024, kSwizzle128B), id_w, ks > 0);
-                mma_bf16(tmem, ka, smem_desc(th + 8192, 16, 1024, kSwizzle128B), id_w, 1);
-            }
-            mma_commit(&bar[2]);
+            for (int i = 0; i < HPC; ++i)
+                bulk_store(record(i) + REC_T2HI, sAT8 + i * C * LDA * 4, 16384);
+            bulk_commit();
         }
-        // ---- per-token factors
-        if (tid < C) {
-            float *sc = reinterpret_cast<float *>(rec + REC_F);
-            const bool in = tid < len;
-            const float G = sG[tid], Gl = sG[len - 1], rk = sRk[tid];
-            sc[SC_QD * C + tid] = in ? sRq[tid] * expf(G) : 0.f;
-            sc[SC_KD * C + tid] = in ? rk * expf(Gl - G) : 0.f;
-            sc[SC_RK * C + tid] = in ? rk : 0.f;
-            sc[SC_ALPHA * C + tid] = in ? expf(sg[tid]) : 0.f;
-            sc[SC_MISC * C + tid] = tid == 0 ? expf(Gl) : (tid == 1 ? (float)len : 0.f);
-        }
-        // ---- -W hi/lo: thread i holds row i (key i) of W^T, i.e. row i of the MN-major
-        // operand of the chain's first product
-        ok = mbar_wait(&bar[2], hh & 1);
-        if (__syncthreads_or(!ok)) break;
+        ok = mbar_wait(&bar[2], 0);
+        if (__syncthreads_or(!ok)) goto teardown;
         tc_fence_after();
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float wv[32];
-            tmem_ld32(tmem + lb + half * 32, wv);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) wv[q] = -wv[q];
-            store_half_row_hilo(rec + REC_WHI, rec + REC_WLO, tid, half * 4, wv);
+        if constexpr (HPC == 2) {
+            // W of head 1 into columns 64-127 while -W of head 0 is staged in place of the
+            // T'' images (once their copies have read them)
+            store_scaled_row(tv[1], vC1(1), hrow, hhalf, sT1, sT1 + 8192);
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (tid == 0) {
+                issue_w(tmem + 64, sK, sT1, &bar[4]);
+                bulk_wait_read_all();
+            }
+            __syncthreads();
+            stage_minus_w(tmem + lb, sAT8, tid);
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_store(record(0) + REC_WHI, sAT8, 32768);
+                bulk_commit();
+            }
+            ok = mbar_wait(&bar[4], 0);
+            if (__syncthreads_or(!ok)) goto teardown;
+            tc_fence_after();
         }
-        tc_fence_before();
+    }
+    // -W of the last head, staged in the key and query tiles (free once its product is done)
+    stage_minus_w(tmem + lb + (HPC - 1) * 64, sm, tid);
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(record(HPC - 1) + REC_WHI, sm, 32768);
+        bulk_commit();
     }
 teardown:
     if (!ok && tid == 0) set_error(p, GDN_ERR_TIMEOUT);
+    // shared memory stays until every bulk copy has read it
+    if (tid == 0) bulk_wait_read_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
@@ -1177,10 +1282,20 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         memset(&mk, 0, sizeof mk); memset(&mq, 0, sizeof mq); memset(&mv, 0, sizeof mv);
     }
     if (pp.max_chunks > 0) {
-        if ((e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kPrepSmem)) != cudaSuccess)
-            return e;
-        prep_kernel<<<dim3(pp.max_chunks, pp.HK), kPrepThreads, kPrepSmem, st>>>(mk, mq, p);
+        // value heads in pairs when each key head serves an even number of them
+        if ((pp.HV / pp.HK) % 2 == 0) {
+            constexpr size_t smem = prep_smem_bytes<2>();
+            if ((e = cudaFuncSetAttribute(prep_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem)) != cudaSuccess)
+                return e;
+            prep_kernel<2><<<dim3(pp.max_chunks, pp.HV / 2), kPrepThreads, smem, st>>>(mk, mq, p);
+        } else {
+            constexpr size_t smem = prep_smem_bytes<1>();
+            if ((e = cudaFuncSetAttribute(prep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem)) != cudaSuccess)
+                return e;
+            prep_kernel<1><<<dim3(pp.max_chunks, pp.HV), kPrepThreads, smem, st>>>(mk, mq, p);
+        }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (pp.N > 0) {

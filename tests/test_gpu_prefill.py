@@ -109,6 +109,21 @@ def test_gqa_equals_repeated_heads_exactly(gdn):
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
 
 
+@pytest.mark.parametrize("HK,HV", [(2, 6), (3, 3), (1, 4)])
+def test_gqa_ratios_match_oracle_and_repeated_heads(gdn, HK, HV):
+    """Odd and even numbers of value heads per key head (one value head per prep CTA when
+    the number is odd, two otherwise) agree with the oracle and, bit for bit, with the
+    same heads given their own repeated queries and keys."""
+    d = _inputs(1, 130, HK, HV, 128, torch.bfloat16, seed=13 + HV, s0=True)
+    o1, f1, _ = _check_vs_oracle(gdn, d)
+    g = _cuda(d)
+    r = HV // HK
+    q2 = g["queries"].repeat_interleave(r, dim=2).contiguous()
+    k2 = g["keys"].repeat_interleave(r, dim=2).contiguous()
+    o2, f2, _ = gdn.prefill(q2, k2, g["values"], g["decays"], g["beta"], g["initial_state"])
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
 def test_varlen_matches_oracle_and_separate_runs(gdn):
     lens = [5, 0, 64, 130, 1, 77]
     T = sum(lens)
