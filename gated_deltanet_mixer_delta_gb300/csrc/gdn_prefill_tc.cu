@@ -829,14 +829,14 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     auto issue_ws = [&](int w, int cc) {
         tc_fence_after();
         constexpr uint32_t id_ws = instr_desc(128, 64, kFmtBF16, 1, 1);
-        const uint32_t wa = smem_u32(ring_a(cc) + kAW + REC_WHI);
+        const uint32_t k0 = (uint32_t)(w - 1) * 4 * 2048;
+        const uint64_t a0 = smem_desc(smem_u32(ring_a(cc) + kAW + REC_WHI) + k0, REC_WLO - REC_WHI, 1024,
+                                      kSwizzle128B);
+        const uint64_t b0 = smem_desc(s_img + k0, 16, 1024, kSwizzle128B);
         const uint32_t d = tmem + TM_W + (uint32_t)((w - 1) * 64);
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            const int ks = 4 * (w - 1) + q;
-            mma_bf16(d, smem_desc(wa + ks * 2048, REC_WLO - REC_WHI, 1024, kSwizzle128B),
-                     smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_ws, q > 0);
-        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            mma_bf16(d, desc_adv(a0, q * 2048), desc_adv(b0, q * 2048), id_ws, q > 0);
         mma_commit(&bars[B_D1]);
     };
 
@@ -850,12 +850,12 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 if (!wait(B_FULLA0 + (c & 1), (c >> 1) & 1)) return false;
                 tc_fence_after();
                 uint8_t *sa = ring_a(c);
-                const uint32_t ta = smem_u32(sa + kAW + REC_T2HI), va = smem_u32(sa + kAV);
-#pragma unroll 1
+                const uint64_t a0 = smem_desc(smem_u32(sa + kAW + REC_T2HI), 16, 1024, kSwizzle128B);
+                const uint64_t b0 = smem_desc(smem_u32(sa + kAV), 16, 512, kSwizzle64B);
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_UT + (uint32_t)((c & 1) * NV),
-                             smem_desc(ta + ks * 32, 16, 1024, kSwizzle128B),
-                             smem_desc(va + ks * 1024, 16, 512, kSwizzle64B), id_u, ks > 0);
+                    mma_bf16(tmem + TM_UT + (uint32_t)((c & 1) * NV), desc_adv(a0, ks * 32),
+                             desc_adv(b0, ks * 1024), id_u, ks > 0);
                 mma_commit(&bars[B_D1]);
                 return true;
             };
@@ -910,11 +910,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 issued = true;
                 tc_fence_after();
                 {
-                    const uint32_t pa = smem_u32(ring_b(cc) + kBP - 8192), ub = smem_u32(sm + OFF_U);
-#pragma unroll 1
+                    const uint64_t a0 = smem_desc(smem_u32(ring_b(cc) + kBP - 8192), 16, 1024, kSwizzle128B);
+                    const uint64_t b0 = smem_desc(smem_u32(sm + OFF_U), 16, 512, kSwizzle64B);
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem + TM_PU, smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B),
-                                 smem_desc(ub + ks * 1024, 16, 512, kSwizzle64B), id_o, ks > 0);
+                        mma_bf16(tmem + TM_PU, desc_adv(a0, ks * 32), desc_adv(b0, ks * 1024), id_o, ks > 0);
                     mma_commit(&bars[B_DO]);
                     mma_commit(&bars[B_EMPTYB0 + (cc & 1)]);
                 }
@@ -939,14 +939,16 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 if (ok2) {
                     tc_fence_after();
                     constexpr uint32_t id_qs = instr_desc(128, 64, kFmtBF16, 0, 1);
-                    const uint32_t qa = smem_u32(ring_b(cc) + kBQ - 8192);
-                    const uint32_t dq = tmem + TM_QS + (uint32_t)((warp - 6) * 64);
-#pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        const int ks = 4 * (warp - 6) + q;
-                        mma_bf16(dq, smem_desc(qa + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
-                                 smem_desc(s_img + ks * 2048, 16, 1024, kSwizzle128B), id_qs, q > 0);
-                    }
+                    // k-steps 4 (warp - 6) + q: the query half (warp - 6) at 32 q bytes, the
+                    // state rows at (4 (warp - 6) + q) 2 KiB
+                    const uint32_t half = (uint32_t)(warp - 6);
+                    const uint64_t a0 = smem_desc(smem_u32(ring_b(cc) + kBQ - 8192) + half * 8192, 16, 1024,
+                                                  kSwizzle128B);
+                    const uint64_t b0 = smem_desc(s_img + half * 4 * 2048, 16, 1024, kSwizzle128B);
+                    const uint32_t dq = tmem + TM_QS + half * 64;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        mma_bf16(dq, desc_adv(a0, q * 32), desc_adv(b0, q * 2048), id_qs, q > 0);
                     mma_commit(&bars[B_QSD]);
                     issued = true;
                 }
@@ -1129,13 +1131,13 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 // K^T [Z_hi | Z_lo]: A = key tile read MN-major; k-steps 0-1 / 2-3
                 tc_fence_after();
                 constexpr uint32_t id_kz = instr_desc(128, 64, kFmtBF16, 1, 1);
-                const uint32_t ka = smem_u32(sb + kBK);
-                const int k0 = (warp - 2) * 2;
+                const uint32_t k0 = (uint32_t)(warp - 2) * 2 * 2048;
+                const uint64_t a0 = smem_desc(smem_u32(sb + kBK) + k0, 8192, 1024, kSwizzle128B);
+                const uint64_t b0 = smem_desc(z_img + k0, 16, 1024, kSwizzle128B);
                 const uint32_t d = tmem + (warp == 2 ? TM_S : TM_S2);
-#pragma unroll 1
-                for (int ks = k0; ks < k0 + 2; ++ks)
-                    mma_bf16(d, smem_desc(ka + ks * 2048, 8192, 1024, kSwizzle128B),
-                             smem_desc(z_img + ks * 2048, 16, 1024, kSwizzle128B), id_kz, ks > k0);
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    mma_bf16(d, desc_adv(a0, q * 2048), desc_adv(b0, q * 2048), id_kz, q > 0);
                 mma_commit(&bars[B_D2]);
                 issued = true;
             }

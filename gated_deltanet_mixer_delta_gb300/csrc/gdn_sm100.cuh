@@ -216,6 +216,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// The same descriptor with its start address moved by `bytes` (a multiple of 16): the
+// field counts 16-byte units and shared addresses stay below 256 KiB, so it cannot carry.
+__device__ __forceinline__ uint64_t desc_adv(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 enum : uint32_t { kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2 };
 // Instruction descriptor of a dense kind::f16 / kind::tf32 MMA with fp32 accumulation.
 // a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
