@@ -18,7 +18,10 @@ with k_t = l2norm(k_t), q_t = l2norm(q_t) * Dk**-0.5.  State layout
 Pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms (T=1 output, beta=0, g -> -inf), the Widrow-Hoff
 projection property with orthonormal keys, an independent one-chunk WY/UT
-solve, continuation, linearity and the GQA interleave of the pages.
+solve, continuation, linearity and the GQA interleave of the pages; the
+gated RMS norm of the output against a hand-worked example, the identity
+silu(z) - silu(-z) = z, its scale invariance and the unit RMS of the
+normalised row.
 """
 import ctypes
 import os
@@ -47,6 +50,9 @@ def _load():
             dp, ctypes.c_ssize_t, dp, ctypes.c_ssize_t, dp, ctypes.c_ssize_t,
             dp, dp, ctypes.c_ssize_t, dp, dp, ctypes.c_ssize_t, dp, dp, ctypes.c_ssize_t,
             ctypes.c_double, ctypes.c_int]
+        lib.gdn_oracle_gated_rmsnorm.restype = ctypes.c_int
+        lib.gdn_oracle_gated_rmsnorm.argtypes = [dp, dp, dp, dp, ctypes.c_int64, ctypes.c_int,
+                                                 ctypes.c_double]
         _lib = lib
     return _lib
 
@@ -165,3 +171,24 @@ def chain(queries, keys, values, decays, beta, initial_state=None, scale=None,
     if rc != 0:
         raise RuntimeError("gdn_oracle_chain failed")
     return out, final, states
+
+
+GATED_NORM_EPS = 1e-6
+
+
+def gated_rmsnorm(y, z, weight, eps=GATED_NORM_EPS):
+    """Gated RMS norm of the mixer output, norm(y, gate=silu(z)) with gain = weight
+    (qwen3_5_text page, Notes -> "The DeltaNet mixer"): per row of the last axis (Dv),
+    y / sqrt(mean(y^2) + eps) * weight * silu(z).  y, z [..., Dv], weight [Dv].
+    Returns float64 of y's shape."""
+    yy, zz, ww = _f64(y), _f64(z), _f64(weight)
+    Dv = yy.shape[-1]
+    if zz.shape != yy.shape or ww.shape != (Dv,):
+        raise ValueError("gated_rmsnorm: y, z must match and weight must be [Dv]")
+    out = np.zeros_like(yy)
+    rows = yy.size // Dv if Dv else 0
+    rc = _load().gdn_oracle_gated_rmsnorm(_ptr(yy), _ptr(zz), _ptr(ww), _ptr(out), rows, Dv,
+                                          float(eps))
+    if rc != 0:
+        raise RuntimeError("gdn_oracle_gated_rmsnorm failed")
+    return out

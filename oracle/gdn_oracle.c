@@ -219,3 +219,36 @@ int gdn_oracle_forward(const double *queries, const double *keys, const double *
     pthread_mutex_destroy(&J.lock);
     return J.err;
 }
+
+/*
+ * Gated RMS norm of the mixer's output (qwen3_5_text page, Notes -> "The DeltaNet
+ * mixer": out = out_proj(norm(y, gate=silu(z))), "gain: weight"; the DeltaNet's own
+ * output norm multiplies by its weight, not by 1 + weight, Notes -> "The readout is the
+ * plain projection").  For each row of Dv values (one token of one value head):
+ *
+ *     r     = 1 / sqrt(mean_c(y_c^2) + eps)
+ *     out_c = y_c * r * weight_c * silu(z_c),    silu(z) = z / (1 + exp(-z))
+ *
+ * Readings where the pages are silent: the mean runs over the head's Dv values, the
+ * weight has Dv entries shared by all heads, and the gate multiplies after the norm
+ * and the gain.  rows = number of rows; y, z, out are [rows][Dv], weight is [Dv].
+ * Returns 0, or -1 on a bad argument.
+ */
+int gdn_oracle_gated_rmsnorm(const double *y, const double *z, const double *weight, double *out,
+                             int64_t rows, int Dv, double eps)
+{
+    if (!y || !z || !weight || !out || rows < 0 || Dv <= 0 || eps < 0.0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *yr = y + r * Dv, *zr = z + r * Dv;
+        double *orow = out + r * Dv;
+        double ms = 0.0;
+        for (int c = 0; c < Dv; ++c) ms += yr[c] * yr[c];
+        ms /= (double)Dv;
+        const double inv = 1.0 / sqrt(ms + eps);
+        for (int c = 0; c < Dv; ++c) {
+            const double gate = zr[c] / (1.0 + exp(-zr[c]));
+            orow[c] = yr[c] * inv * weight[c] * gate;
+        }
+    }
+    return 0;
+}

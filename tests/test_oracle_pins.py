@@ -310,3 +310,59 @@ def test_per_token_states_are_the_running_state(oracle_mod):
     for t in range(10):
         np.testing.assert_allclose(o[0, t, 0], st[0, t, 0].T @ qn[t], rtol=0, atol=1e-13)
     np.testing.assert_array_equal(st[0, -1, 0], sf[0, 0])
+
+
+# ---------------------------------------------------------------- gated RMS norm
+def test_gated_norm_hand_worked_example(oracle_mod):
+    """tests/golden/gated_norm_hand_Dv4.txt: two rows computed by hand (mean over the
+    head's values, gain = weight, silu gate after the norm)."""
+    G = _parse_golden(os.path.join(GOLDEN, "gated_norm_hand_Dv4.txt"))
+    for r in range(2):
+        out = oracle_mod.gated_rmsnorm(G["y"][r:r + 1], G["z"][r:r + 1], G["weight"][r], eps=0.0)
+        np.testing.assert_allclose(out[0], G["out"][r], atol=1e-15, rtol=0)
+
+
+def _norm_case(rng, rows, Dv):
+    y = rng.standard_normal((rows, Dv)) * np.exp(rng.standard_normal((rows, 1)))
+    z = rng.standard_normal((rows, Dv)) * 2.0
+    w = 1.0 + 0.3 * rng.standard_normal(Dv)
+    return y, z, w
+
+
+@pytest.mark.parametrize("Dv", [4, 32, 128])
+def test_gated_norm_gate_is_silu_after_the_norm(oracle_mod, Dv):
+    """silu(z) - silu(-z) = z, so out(y, z) - out(y, -z) = y r w z when the gate
+    multiplies after the norm (r does not depend on z); and rms(y r) = 1 at eps = 0
+    (the mean, not the sum, of the squares)."""
+    y, z, w = _norm_case(_rng(50 + Dv), 9, Dv)
+    d = oracle_mod.gated_rmsnorm(y, z, w, eps=0.0) - oracle_mod.gated_rmsnorm(y, -z, w, eps=0.0)
+    yr = d / (w[None, :] * z)
+    np.testing.assert_allclose(np.sqrt((yr * yr).mean(-1)), 1.0, rtol=1e-12)
+    np.testing.assert_allclose(yr / y, (yr / y)[:, :1].repeat(Dv, 1), rtol=1e-11)
+
+
+def test_gated_norm_invariances(oracle_mod):
+    """At eps = 0 the norm ignores a positive scale of its row and is odd in y; the gain
+    is the weight itself (weight 0 gives 0, not the gate); rows do not interact."""
+    y, z, w = _norm_case(_rng(60), 6, 16)
+    o = oracle_mod.gated_rmsnorm(y, z, w, eps=0.0)
+    np.testing.assert_allclose(oracle_mod.gated_rmsnorm(37.5 * y, z, w, eps=0.0), o, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(oracle_mod.gated_rmsnorm(-y, z, w, eps=0.0), -o, rtol=0, atol=0)
+    assert np.all(oracle_mod.gated_rmsnorm(y, z, np.zeros_like(w)) == 0.0)
+    y2 = y.copy()
+    y2[3] *= 1e3
+    o2 = oracle_mod.gated_rmsnorm(y2, z, w, eps=0.0)
+    np.testing.assert_array_equal(np.delete(o2, 3, 0), np.delete(o, 3, 0))
+
+
+def test_gated_norm_epsilon_and_zero_rows(oracle_mod):
+    """eps sits inside the root next to the mean square: a constant row c with c^2 = eps
+    comes out at 1/sqrt(2) of its eps-free value; an all-zero row stays zero (finite)."""
+    c = 1e-3
+    y = np.full((1, 8), c)
+    z = np.linspace(-3, 3, 8)[None, :]
+    w = np.linspace(0.5, 1.5, 8)
+    ratio = oracle_mod.gated_rmsnorm(y, z, w, eps=c * c) / oracle_mod.gated_rmsnorm(y, z, w, eps=0.0)
+    np.testing.assert_allclose(ratio, 2 ** -0.5, rtol=1e-12)
+    zero = oracle_mod.gated_rmsnorm(np.zeros((2, 8)), np.ones((2, 8)), w)
+    assert np.all(zero == 0.0)
