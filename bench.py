@@ -224,6 +224,49 @@ def bench_decode(gdn, w, iters, warmup):
     return res
 
 
+def bench_decode_gated(gdn, w, iters, warmup):
+    """The decode step with the gated RMS norm fused in (gdn_decode_step_gated)."""
+    d = workloads.decode_inputs(w, steps=16, device="cuda")
+    state = d["initial_state"]
+    out = torch.empty(w.B, w.HV, w.Dv, dtype=w.dtype, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(4)
+    z = torch.randn(16, w.B, w.HV, w.Dv, generator=gen, device="cuda").to(w.dtype)
+    wt = 1.0 + 0.3 * torch.randn(w.Dv, generator=gen, device="cuda")
+    i = [0]
+
+    def fn():
+        s = i[0] % 16
+        i[0] += 1
+        gdn.decode_step(d["queries"][s], d["keys"][s], d["values"][s], d["decays"][s],
+                        d["beta"][s], state, out=out, gate=z[s], norm_weight=wt)
+
+    times = Timer(flush=False).run(fn, iters, warmup)
+    nbytes = decode_bytes(w.B, w.HK, w.HV, w.Dk, 2) + w.B * w.HV * w.Dv * 2 + w.Dv * 4
+    res = dict(ms=statistics.mean(times), ms_min=min(times), bytes=nbytes)
+    del d, state, out, z, wt
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_gated_norm(gdn, w, iters, warmup, copies=4):
+    """The gated RMS norm on the outputs of `copies` prefills of workload w (y, gate in, out
+    back): y and the gate together are larger than L2, so no flush is needed."""
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    shape = (w.B * copies, w.T, w.HV, w.Dv)
+    y = torch.randn(shape, generator=gen, device="cuda").to(w.dtype)
+    z = torch.randn(shape, generator=gen, device="cuda").to(w.dtype)
+    wt = 1.0 + 0.3 * torch.randn(w.Dv, generator=gen, device="cuda")
+    out = torch.empty_like(y)
+    fn = lambda: gdn.gated_rmsnorm(y, z, wt, out=out)
+    times = Timer(flush=False).run(fn, iters, warmup)
+    rows = w.B * copies * w.T * w.HV
+    nbytes = rows * w.Dv * y.element_size() * 3 + w.Dv * 4
+    res = dict(rows=rows, ms=statistics.mean(times), ms_min=min(times), bytes=nbytes)
+    del y, z, wt, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_e2e(gdn, w, iters, warmup):
     """Public API end to end: pinned host inputs -> device, prefill, out and final state
     back to pinned host memory, every step."""
@@ -392,7 +435,9 @@ def main():
     if not args.quick:
         for key, name, kw in (("varlen", "varlen8_512to8192_hk16_hv32_d128", {}),
                               ("long_prefill", "long_prefill_B2_T65536_hk16_hv32_d128", {}),
-                              ("states", "states_B4_T1024_hk16_hv32_d128", {"states": True})):
+                              ("states", "states_B4_T1024_hk16_hv32_d128", {"states": True}),
+                              ("prefill_hv48", "qwen35_27b_prefill_T4096_hk16_hv48_d128", {}),
+                              ("prefill_hv16", "qwen35_0p8b_prefill_T4096_hk16_hv16_d128", {})):
             r = bench_prefill(gdn, W[name], max(3, min(args.steps, 5)), 3, **kw)
             subs[key] = dict(workload=name, tokens=r["tokens"], ms=r["ms"],
                              tokens_per_s=r["tokens"] / (r["ms"] * 1e-3),
@@ -400,6 +445,22 @@ def main():
                                        "peak": hbm, "unit": "GB/s",
                                        "frac": r["bytes"] / (r["ms"] * 1e-3) / 1e9 / hbm,
                                        "algorithmic_bytes": r["bytes"]})
+        dg = bench_decode_gated(gdn, W["decode_B256_hk16_hv32_d128"], max(args.steps, 20),
+                                args.warmup)
+        subs["decode_gated_norm"] = dict(
+            workload="decode_B256_hk16_hv32_d128 + gated RMS norm fused", ms=dg["ms"],
+            steps_per_s=1e3 / dg["ms"],
+            roofline={"bound": "hbm", "achieved": dg["bytes"] / (dg["ms"] * 1e-3) / 1e9, "peak": hbm,
+                      "unit": "GB/s", "frac": dg["bytes"] / (dg["ms"] * 1e-3) / 1e9 / hbm,
+                      "algorithmic_bytes": dg["bytes"]})
+        gn = bench_gated_norm(gdn, head_w, max(args.steps, 20), args.warmup)
+        subs["gated_norm"] = dict(
+            workload="gated RMS norm of 4 next_prefill_T4096_hk16_hv32_d128 outputs "
+                     "(y and gate 268 MB, larger than L2: no flush)", rows=gn["rows"],
+            ms=gn["ms"],
+            roofline={"bound": "hbm", "achieved": gn["bytes"] / (gn["ms"] * 1e-3) / 1e9, "peak": hbm,
+                      "unit": "GB/s", "frac": gn["bytes"] / (gn["ms"] * 1e-3) / 1e9 / hbm,
+                      "algorithmic_bytes": gn["bytes"]})
     e2e = bench_e2e(gdn, head_w, max(5, min(args.steps, 20)), 2)
     clk = clocks.stop()
 

@@ -21,7 +21,7 @@ import torch
 
 from . import build as _build
 
-__all__ = ["prefill", "prefill_varlen", "decode_step", "state_layout", "workspace_size",
+__all__ = ["prefill", "prefill_varlen", "decode_step", "gated_rmsnorm", "state_layout", "workspace_size",
            "workspace_status", "selftest_wait_timeout", "GdnError", "library_path",
            "load_library", "abi"]
 
@@ -75,6 +75,11 @@ def load_library(build_if_missing: bool = False):
                                        i, f, i, vp, sz, vp]
     lib.gdn_decode_step.restype = i
     lib.gdn_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.gdn_decode_step_gated.restype = i
+    lib.gdn_decode_step_gated.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, fp, f, i, i, i, i, i, i,
+                                          f, i, vp]
+    lib.gdn_gated_rmsnorm.restype = i
+    lib.gdn_gated_rmsnorm.argtypes = [vp, vp, fp, vp, ctypes.c_int64, i, i, f, vp]
     lib.gdn_state_layout.restype = i
     lib.gdn_state_layout.argtypes = [i, i, i, i, ctypes.POINTER(_StateLayout)]
     lib.gdn_prefill_workspace_size.restype = sz
@@ -259,10 +264,12 @@ def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_stat
 
 
 def decode_step(queries, keys, values, decays, beta, state, *, scale=None, use_qk_l2norm=True,
-                out=None, stream=None):
+                out=None, gate=None, norm_weight=None, norm_eps=1e-6, stream=None):
     """One decode step (gdn_decode_step): queries/keys [B, HK, Dk], values [B, HV, Dv],
     decays/beta [B, HV], state [B, HV, Dk, Dv] float32 updated in place.  Returns out
-    [B, HV, Dv]."""
+    [B, HV, Dv].  With ``gate`` ([B, HV, Dv], dtype of the values) and ``norm_weight``
+    ([Dv] float32) the gated RMS norm is fused in (gdn_decode_step_gated): out is then
+    norm(y, gate=silu(gate)) * norm_weight."""
     _need(queries, "queries")
     dev, dt = queries.device, queries.dtype
     if dt not in _DTYPES:
@@ -277,9 +284,41 @@ def decode_step(queries, keys, values, decays, beta, state, *, scale=None, use_q
     if out is None:
         out = torch.empty(B, HV, Dv, dtype=dt, device=dev)
     _need(out, "out", dt, dev, (B, HV, Dv))
+    if (gate is None) != (norm_weight is None):
+        raise ValueError("gate and norm_weight go together")
+    if gate is not None:
+        _need(gate, "gate", dt, dev, (B, HV, Dv))
+        _need(norm_weight, "norm_weight", torch.float32, dev, (Dv,))
+        rc = load_library().gdn_decode_step_gated(
+            _ptr(queries), _ptr(keys), _ptr(values), _ptr(decays), _ptr(beta), _ptr(state),
+            _ptr(out), _ptr(gate), _ptr(norm_weight), float(norm_eps), B, HK, HV, Dk, Dv,
+            _DTYPES[dt], float(scale or 0.0), int(bool(use_qk_l2norm)), _stream(stream))
+        _check(rc, "gdn_decode_step_gated")
+        return out
     rc = load_library().gdn_decode_step(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays),
                                         _ptr(beta), _ptr(state), _ptr(out), B, HK, HV, Dk, Dv,
                                         _DTYPES[dt], float(scale or 0.0),
                                         int(bool(use_qk_l2norm)), _stream(stream))
     _check(rc, "gdn_decode_step")
+    return out
+
+
+def gated_rmsnorm(y, gate, norm_weight, *, eps=1e-6, out=None, stream=None):
+    """Gated RMS norm of the mixer output (gdn_gated_rmsnorm): y, gate [..., Dv] (bf16 or
+    float32, same dtype), norm_weight [Dv] float32.  Returns
+    y / sqrt(mean(y^2) + eps) * norm_weight * silu(gate) per row of Dv; ``out`` may be y."""
+    _need(y, "y")
+    dev, dt = y.device, y.dtype
+    if dt not in _DTYPES:
+        raise ValueError("y must be bfloat16 or float32")
+    Dv = y.shape[-1]
+    _need(gate, "gate", dt, dev, tuple(y.shape))
+    _need(norm_weight, "norm_weight", torch.float32, dev, (Dv,))
+    if out is None:
+        out = torch.empty_like(y)
+    _need(out, "out", dt, dev, tuple(y.shape))
+    rows = y.numel() // Dv if Dv else 0
+    rc = load_library().gdn_gated_rmsnorm(_ptr(y), _ptr(gate), _ptr(norm_weight), _ptr(out), rows,
+                                          Dv, _DTYPES[dt], float(eps), _stream(stream))
+    _check(rc, "gdn_gated_rmsnorm")
     return out

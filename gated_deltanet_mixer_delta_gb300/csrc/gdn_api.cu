@@ -132,23 +132,58 @@ int gdn_prefill_varlen(const void *queries, const void *keys, const void *values
                           use_qk_l2norm, workspace, workspace_bytes, cuda_stream);
 }
 
-int gdn_decode_step(const void *queries, const void *keys, const void *values,
-                    const float *decays, const float *beta, float *state, void *out, int B,
-                    int HK, int HV, int Dk, int Dv, gdn_dtype dtype, float scale,
-                    int use_qk_l2norm, void *cuda_stream) {
+static int decode_common(const void *queries, const void *keys, const void *values,
+                         const float *decays, const float *beta, float *state, void *out, int B,
+                         int HK, int HV, int Dk, int Dv, gdn_dtype dtype, float scale,
+                         int use_qk_l2norm, const void *gate_z, const float *norm_weight,
+                         float norm_eps, void *cuda_stream) {
     int rc = check_common(HK, HV, Dk, Dv, dtype, scale);
     if (rc != GDN_OK) return rc;
     if (B < 0) return GDN_ERR_INVALID_ARG;
     if (B == 0) return GDN_OK;
     if (!queries || !keys || !values || !decays || !beta || !state || !out)
         return GDN_ERR_INVALID_ARG;
-    const void *ptrs[] = {queries, keys, values, decays, beta, state, out};
+    const void *ptrs[] = {queries, keys, values, decays, beta, state, out, gate_z, norm_weight};
     for (const void *p : ptrs)
-        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
     if ((int64_t)B * HV > INT32_MAX) return GDN_ERR_UNSUPPORTED;
     cudaError_t e = launch_decode(queries, keys, values, decays, beta, state, out, B, HK, HV, Dk,
                                   Dv, dtype, resolve_scale(scale, Dk), use_qk_l2norm ? 1 : 0,
-                                  (cudaStream_t)cuda_stream);
+                                  gate_z, norm_weight, norm_eps, (cudaStream_t)cuda_stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_decode_step(const void *queries, const void *keys, const void *values,
+                    const float *decays, const float *beta, float *state, void *out, int B,
+                    int HK, int HV, int Dk, int Dv, gdn_dtype dtype, float scale,
+                    int use_qk_l2norm, void *cuda_stream) {
+    return decode_common(queries, keys, values, decays, beta, state, out, B, HK, HV, Dk, Dv,
+                         dtype, scale, use_qk_l2norm, nullptr, nullptr, 0.f, cuda_stream);
+}
+
+int gdn_decode_step_gated(const void *queries, const void *keys, const void *values,
+                          const float *decays, const float *beta, float *state, void *out,
+                          const void *gate_z, const float *norm_weight, float norm_eps, int B,
+                          int HK, int HV, int Dk, int Dv, gdn_dtype dtype, float scale,
+                          int use_qk_l2norm, void *cuda_stream) {
+    if (!gate_z || !norm_weight) return GDN_ERR_INVALID_ARG;
+    if (!(norm_eps >= 0.f) || isinf(norm_eps)) return GDN_ERR_INVALID_ARG;
+    return decode_common(queries, keys, values, decays, beta, state, out, B, HK, HV, Dk, Dv,
+                         dtype, scale, use_qk_l2norm, gate_z, norm_weight, norm_eps, cuda_stream);
+}
+
+int gdn_gated_rmsnorm(const void *y, const void *gate_z, const float *norm_weight, void *out,
+                      int64_t rows, int Dv, gdn_dtype dtype, float norm_eps, void *cuda_stream) {
+    if (rows < 0 || !(norm_eps >= 0.f) || isinf(norm_eps)) return GDN_ERR_INVALID_ARG;
+    if (!dim_ok(Dv)) return GDN_ERR_UNSUPPORTED;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+    if (rows == 0) return GDN_OK;
+    if (!y || !gate_z || !norm_weight || !out) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {y, gate_z, norm_weight, out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    cudaError_t e = launch_gated_norm(y, gate_z, norm_weight, out, rows, Dv, dtype, norm_eps,
+                                      (cudaStream_t)cuda_stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -18,6 +18,10 @@
 // 128-bit transaction.  The two reductions over the key index (S^T k, S^T q)
 // run first inside each thread over its rows, then across the row groups
 // through shared memory.  All loads of the tile are issued before any is used.
+//
+// GATED: the output goes through the gated RMS norm that follows the rule in the
+// mixer (out = norm(y, gate=silu(z)) * weight, qwen3_5_text page, "The DeltaNet
+// mixer"), from the fp32 y of the CTA's whole head, so y never goes to memory.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -25,12 +29,12 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 
-template <int DK, int DV, typename Tin>
+template <int DK, int DV, typename Tin, bool GATED>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
               const float *__restrict__ g, const float *__restrict__ beta,
               float *__restrict__ state, Tin *__restrict__ out, int HK, int HV, float scale,
-              int l2norm) {
+              int l2norm, const Tin *__restrict__ gz, const float *__restrict__ gw, float eps) {
     constexpr int TPR = DV / 4;                    // threads per state row
     constexpr int NRG = kDecodeThreads / TPR;      // row groups
     constexpr int RPT = DK / NRG;                  // rows per thread
@@ -39,6 +43,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
     __shared__ float s_q[DK], s_k[DK], s_u[DV];
     __shared__ float s_red[2][NRG][DV];
     __shared__ float s_scal[4];
+    __shared__ float s_nrm[DV / 32];
 
     const int bh = blockIdx.x;                     // b * HV + h
     const int b = bh / HV, h = bh - b * HV;
@@ -51,6 +56,11 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
     float4 s[RPT];
 #pragma unroll
     for (int a = 0; a < RPT; ++a) s[a] = __ldcs(&S4[(rg + a * NRG) * TPR + cg]);
+    float gzv = 0.f, gwv = 0.f;                    // gate and gain of column tid
+    if (GATED && tid < DV) {
+        gzv = to_f32(gz[(size_t)bh * DV + tid]);
+        gwv = gw[tid];
+    }
 
     // 2. q, k of key head j; norms and q.k in warp 0
     const Tin *qr = q + ((size_t)b * HK + j) * DK;
@@ -89,6 +99,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
 
     // 4. finish the reductions, form u and o
     const float alpha = expf(g[bh]);
+    float yo = 0.f;                                // y of column tid
     if (tid < DV) {
         float x = 0.f, y = 0.f;
 #pragma unroll 8
@@ -97,7 +108,13 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
         const float vv = to_f32(v[(size_t)bh * DV + tid]);
         const float u = beta[bh] * (vv - alpha * rk * x);
         s_u[tid] = u;
-        out[(size_t)bh * DV + tid] = from_f32<Tin>(alpha * rq * y + kq * u);
+        yo = alpha * rq * y + kq * u;
+        if (GATED) {
+            const float ss = warp_sum(yo * yo);      // DV is a multiple of 32: whole warps
+            if ((tid & 31) == 0) s_nrm[tid >> 5] = ss;
+        } else {
+            out[(size_t)bh * DV + tid] = from_f32<Tin>(yo);
+        }
     }
     __syncthreads();
 
@@ -115,26 +132,41 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
         o.w = alpha * s[a].w + kk * u4.w;
         __stcs(&S4[i * TPR + cg], o);
     }
+    // the gated output once the state stores are on their way
+    if (GATED && tid < DV) {
+        float ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < DV / 32; ++w) ss += s_nrm[w];
+        const float inv = rsqrtf(ss * (1.f / DV) + eps);
+        out[(size_t)bh * DV + tid] = from_f32<Tin>(yo * inv * gwv * (gzv / (1.f + expf(-gzv))));
+    }
 }
 
 template <int DK, int DV, typename Tin>
 cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g,
                      const float *beta, float *state, void *out, int B, int HK, int HV,
-                     float scale, int l2norm, cudaStream_t st) {
-    decode_kernel<DK, DV, Tin><<<B * HV, kDecodeThreads, 0, st>>>(
-        (const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, state, (Tin *)out, HK, HV,
-        scale, l2norm);
+                     float scale, int l2norm, const void *gz, const float *gw, float eps,
+                     cudaStream_t st) {
+    if (gz)
+        decode_kernel<DK, DV, Tin, true><<<B * HV, kDecodeThreads, 0, st>>>(
+            (const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, state, (Tin *)out, HK, HV,
+            scale, l2norm, (const Tin *)gz, gw, eps);
+    else
+        decode_kernel<DK, DV, Tin, false><<<B * HV, kDecodeThreads, 0, st>>>(
+            (const Tin *)q, (const Tin *)k, (const Tin *)v, g, beta, state, (Tin *)out, HK, HV,
+            scale, l2norm, nullptr, nullptr, 0.f);
     return cudaGetLastError();
 }
 
 template <typename Tin>
 cudaError_t dispatch_dims(int Dk, int Dv, const void *q, const void *k, const void *v,
                           const float *g, const float *beta, float *state, void *out, int B,
-                          int HK, int HV, float scale, int l2norm, cudaStream_t st) {
+                          int HK, int HV, float scale, int l2norm, const void *gz,
+                          const float *gw, float eps, cudaStream_t st) {
 #define GDN_DEC_CASE(DK_, DV_)                                                             \
     if (Dk == DK_ && Dv == DV_)                                                            \
         return launch_t<DK_, DV_, Tin>(q, k, v, g, beta, state, out, B, HK, HV, scale,     \
-                                       l2norm, st);
+                                       l2norm, gz, gw, eps, st);
     GDN_DEC_CASE(32, 32) GDN_DEC_CASE(64, 64) GDN_DEC_CASE(128, 128)
 #undef GDN_DEC_CASE
     return cudaErrorInvalidValue;
@@ -145,13 +177,14 @@ cudaError_t dispatch_dims(int Dk, int Dv, const void *q, const void *k, const vo
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int B, int HK, int HV,
                           int Dk, int Dv, gdn_dtype dtype, float scale, int l2norm,
+                          const void *gate_z, const float *norm_weight, float norm_eps,
                           cudaStream_t st) {
     if (B == 0) return cudaSuccess;
     if (dtype == GDN_BF16)
         return dispatch_dims<__nv_bfloat16>(Dk, Dv, q, k, v, g, beta, state, out, B, HK, HV,
-                                            scale, l2norm, st);
+                                            scale, l2norm, gate_z, norm_weight, norm_eps, st);
     return dispatch_dims<float>(Dk, Dv, q, k, v, g, beta, state, out, B, HK, HV, scale,
-                                l2norm, st);
+                                l2norm, gate_z, norm_weight, norm_eps, st);
 }
 
 }  // namespace gdn

@@ -61,10 +61,15 @@ cudaError_t launch_chunk_table(const PrefillParams &p, cudaStream_t st);
 bool tc_supported(int Dk, int Dv, gdn_dtype dtype);
 size_t tc_record_bytes();
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st);
+// gate_z == nullptr: out = y; otherwise out = norm(y, gate=silu(gate_z)) * norm_weight
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float *state, void *out, int B, int HK, int HV,
                           int Dk, int Dv, gdn_dtype dtype, float scale, int l2norm,
+                          const void *gate_z, const float *norm_weight, float norm_eps,
                           cudaStream_t st);
+// Gated RMS norm of rows of Dv values: out = y / sqrt(mean(y^2) + eps) * w * silu(z)
+cudaError_t launch_gated_norm(const void *y, const void *z, const float *w, void *out, int64_t rows,
+                              int Dv, gdn_dtype dtype, float eps, cudaStream_t st);
 
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ float to_f32(float x) { return x; }

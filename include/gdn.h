@@ -149,6 +149,42 @@ int gdn_decode_step(const void *queries, const void *keys, const void *values,
                     float scale, int use_qk_l2norm, void *cuda_stream);
 
 /*
+ * Gated RMS norm of the mixer output, the step that follows the rule in the mixer
+ * (qwen3_5_text page, Notes -> "The DeltaNet mixer": out = out_proj(norm(y,
+ * gate=silu(z))), "gain: weight"; the DeltaNet's own output norm multiplies by its
+ * weight, not by 1 + weight, Notes -> "The readout is the plain projection").  For each
+ * row of Dv values (one token of one value head):
+ *
+ *     out_c = y_c / sqrt(mean_c(y^2) + norm_eps) * norm_weight_c * silu(gate_z_c)
+ *
+ * The pages give no epsilon (1e-6 is the usual choice) and do not spell out the order
+ * inside norm(): the gate multiplies after the norm and the gain.
+ *   y, gate_z, out  [rows, Dv]  dtype, contiguous; out may be y (in place)
+ *   norm_weight     [Dv]        float32, shared by all heads
+ * Dv in {32, 64, 128}.  rows == 0 is allowed.  norm_eps must be finite and >= 0.
+ * Errors: GDN_ERR_INVALID_ARG (null pointer, rows < 0, bad eps), GDN_ERR_UNSUPPORTED
+ * (Dv, dtype), GDN_ERR_MISALIGNED (a pointer not 16-byte aligned), GDN_ERR_CUDA.
+ */
+int gdn_gated_rmsnorm(const void *y, const void *gate_z, const float *norm_weight, void *out,
+                      int64_t rows, int Dv, gdn_dtype dtype, float norm_eps, void *cuda_stream);
+
+/*
+ * gdn_decode_step with the gated RMS norm above fused into the same kernel: `out`
+ * receives norm(y, gate=silu(gate_z)) * norm_weight, formed from the fp32 y of the whole
+ * head (y itself is never rounded to dtype or written).
+ *   gate_z       [B, HV, Dv]  dtype
+ *   norm_weight  [Dv]         float32
+ * Everything else (arguments, in-place state, errors) as gdn_decode_step; gate_z or
+ * norm_weight NULL, or a negative or non-finite norm_eps, is GDN_ERR_INVALID_ARG.
+ */
+int gdn_decode_step_gated(const void *queries, const void *keys, const void *values,
+                          const float *decays, const float *beta,
+                          float *state, void *out,
+                          const void *gate_z, const float *norm_weight, float norm_eps,
+                          int B, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                          float scale, int use_qk_l2norm, void *cuda_stream);
+
+/*
  * gdn_prefill for callers that cannot allocate device memory (no counterpart on the
  * pages: it exists for deployments, not for the method).  Engines that carve up
  * device memory once in their own pool, plugins that only see the buffers their

@@ -34,7 +34,8 @@ def header_functions():
 def test_header_declares_the_entry_points():
     names = header_functions()
     for n in ["gdn_prefill", "gdn_prefill_varlen", "gdn_decode_step", "gdn_state_layout",
-              "gdn_prefill_workspace_size", "gdn_workspace_status", "gdn_status_string"]:
+              "gdn_prefill_workspace_size", "gdn_workspace_status", "gdn_status_string",
+              "gdn_gated_rmsnorm", "gdn_decode_step_gated"]:
         assert n in names
 
 
@@ -152,3 +153,37 @@ def test_selftest_wait_timeout_rejects_bad_arguments(lib):
     assert f(ctypes.c_void_p(0x10000), 0, None) == -1     # zero limit
     assert f(ctypes.c_void_p(0x10000), 3_000_000_000, None) == -1   # above 2 s
     assert f(ctypes.c_void_p(0x10002), 1000, None) == -3  # GDN_ERR_MISALIGNED
+
+
+def _norm(lib, **kw):
+    a = dict(y=P, z=P, w=P, out=P, rows=10, Dv=128, dtype=0, eps=1e-6, stream=None)
+    a.update(kw)
+    return lib.gdn_gated_rmsnorm(a["y"], a["z"], a["w"], a["out"], a["rows"], a["Dv"], a["dtype"],
+                                 a["eps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=-1), -1), (dict(eps=-1e-3), -1), (dict(eps=float("inf")), -1),
+    (dict(eps=float("nan")), -1), (dict(y=None), -1), (dict(w=None), -1),
+    (dict(Dv=48), -2), (dict(dtype=5), -2), (dict(z=P + 8), -3), (dict(out=P + 2), -3),
+    (dict(rows=0, y=None, z=None, w=None, out=None), 0),
+])
+def test_gated_norm_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _norm(lib, **kw) == code
+
+
+def _decode_gated(lib, **kw):
+    a = dict(q=P, k=P, v=P, g=P, b=P, s=P, out=P, z=P, w=P, eps=1e-6, B=4, HK=2, HV=4, Dk=128,
+             Dv=128, dtype=0, scale=0.0, l2=1, stream=None)
+    a.update(kw)
+    return lib.gdn_decode_step_gated(a["q"], a["k"], a["v"], a["g"], a["b"], a["s"], a["out"],
+                                     a["z"], a["w"], a["eps"], a["B"], a["HK"], a["HV"], a["Dk"],
+                                     a["Dv"], a["dtype"], a["scale"], a["l2"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(z=None), -1), (dict(w=None), -1), (dict(eps=-1.0), -1), (dict(HV=5), -1),
+    (dict(z=P + 4), -3), (dict(w=P + 8), -3), (dict(Dk=48, Dv=48), -2), (dict(B=0), 0),
+])
+def test_gated_decode_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _decode_gated(lib, **kw) == code

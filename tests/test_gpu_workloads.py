@@ -91,3 +91,22 @@ def test_per_token_states_B4_T1024(gdn):
         assert_out_close(out[b, :, h], o_r, torch.bfloat16, f"chain {(b, h)}")
         assert_states_close(st[b, :, h], s_r, f"states of chain {(b, h)}")
         assert_states_close(fin[b, h], f_r, f"chain {(b, h)}")
+
+
+@pytest.mark.parametrize("name,heads", [
+    ("qwen35_27b_prefill_T4096_hk16_hv48_d128", (0, 1, 2, 25, 46, 47)),
+    ("qwen35_0p8b_prefill_T4096_hk16_hv16_d128", (0, 7, 15)),
+])
+def test_other_head_layouts_T4096(gdn, name, heads):
+    """Head layouts of other sizes of the family (three value heads per key head on 27B,
+    one on 0.8B), T=4096: sampled value heads (all three of key head 0 on 27B) against
+    the oracle over every token."""
+    w = W[name]
+    d = workloads.workload_inputs(w, device="cuda")
+    out, fin, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                              workspace=_ws(gdn, w.T, 1, w))
+    torch.cuda.synchronize()
+    ref = oracle_chains(d, [(0, h) for h in heads])
+    for (s, h), (o_r, f_r, _) in ref.items():
+        assert_out_close(out[0, :, h], o_r, torch.bfloat16, f"head {h}")
+        assert_states_close(fin[0, h], f_r, f"head {h}")

@@ -67,6 +67,14 @@ WORKLOADS = {
         Workload("states_B4_T1024_hk16_hv32_d128", B=4, T=1024, HK=16, HV=32, Dk=128, Dv=128,
                  dtype=torch.bfloat16, seed=1006, g_shift=0.01, emit_states=True,
                  notes="prefill emitting per-token states [4,1024,32,128,128] fp32"),
+        # head layouts of other sizes of the family (qwen3_5_text page, "The DeltaNet
+        # mixer": 0.8B and 2B 16 key heads over 16 value heads, 27B over 48)
+        Workload("qwen35_27b_prefill_T4096_hk16_hv48_d128", B=1, T=4096, HK=16, HV=48, Dk=128,
+                 Dv=128, dtype=torch.bfloat16, seed=1007,
+                 notes="27B-shaped prefill (three value heads per key head)"),
+        Workload("qwen35_0p8b_prefill_T4096_hk16_hv16_d128", B=1, T=4096, HK=16, HV=16, Dk=128,
+                 Dv=128, dtype=torch.bfloat16, seed=1008,
+                 notes="0.8B-shaped prefill (one value head per key head)"),
     ]
 }
 
