@@ -21,7 +21,11 @@ projection property with orthonormal keys, an independent one-chunk WY/UT
 solve, continuation, linearity and the GQA interleave of the pages; the
 gated RMS norm of the output against a hand-worked example, the identity
 silu(z) - silu(-z) = z, its scale invariance and the unit RMS of the
-normalised row.
+normalised row; the convolution of the step before the rule by its impulse
+response (causal, depthwise, width 4), continuation through the carried conv
+state and packed-vs-separate runs; the gates by closed forms and the
+softplus odd-part identity; the regroup of the fused projections against a
+hand-listed column layout.
 """
 import ctypes
 import os
@@ -50,6 +54,10 @@ def _load():
             dp, ctypes.c_ssize_t, dp, ctypes.c_ssize_t, dp, ctypes.c_ssize_t,
             dp, dp, ctypes.c_ssize_t, dp, dp, ctypes.c_ssize_t, dp, dp, ctypes.c_ssize_t,
             ctypes.c_double, ctypes.c_int]
+        lib.gdn_oracle_conv_gate.restype = ctypes.c_int
+        lib.gdn_oracle_conv_gate.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
+                                             ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, dp, dp, dp]
         lib.gdn_oracle_gated_rmsnorm.restype = ctypes.c_int
         lib.gdn_oracle_gated_rmsnorm.argtypes = [dp, dp, dp, dp, ctypes.c_int64, ctypes.c_int,
                                                  ctypes.c_double]
@@ -192,3 +200,76 @@ def gated_rmsnorm(y, z, weight, eps=GATED_NORM_EPS):
     if rc != 0:
         raise RuntimeError("gdn_oracle_gated_rmsnorm failed")
     return out
+
+
+def conv_gate(x, b, a, conv_weight, A_log, dt_bias, conv_state=None, cu_seqlens=None,
+              want_state=False):
+    """The step before the rule (qwen3_5_text page, Notes -> "The DeltaNet mixer"):
+    y = silu(causal depthwise conv1d of width 4) over the cat(q, k, v) channels,
+    beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias).
+
+    x [B, T, C]; b, a [B, T, HV]; conv_weight [C, 4] (tap 3 multiplies the current
+    token); A_log, dt_bias [HV]; conv_state [N, 3, C] (the three inputs before each
+    sequence, oldest first) or None for the start of a prompt.  Packed form: B == 1 and
+    ``cu_seqlens`` [N+1].  Returns (y [B, T, C], beta [B, T, HV], g [B, T, HV],
+    state_out [N, 3, C] or None), float64."""
+    xx, bb, aa = _f64(x), _f64(b), _f64(a)
+    w, al, db = _f64(conv_weight), _f64(A_log), _f64(dt_bias)
+    B, T, C = xx.shape
+    HV = bb.shape[-1]
+    if cu_seqlens is None:
+        cu = np.arange(B + 1, dtype=np.int64) * T
+    else:
+        if B != 1:
+            raise ValueError("packed form needs batch 1")
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64))
+    N = len(cu) - 1
+    st = _f64(conv_state)
+    if st is not None and st.shape != (N, 3, C):
+        raise ValueError("conv_state must be [N, 3, C]")
+    y = np.zeros((B, T, C))
+    beta = np.zeros((B, T, HV))
+    g = np.zeros((B, T, HV))
+    st_out = np.zeros((N, 3, C)) if want_state else None
+    rc = _load().gdn_oracle_conv_gate(
+        _ptr(xx), _ptr(bb), _ptr(aa), _ptr(w), _ptr(al), _ptr(db), _ptr(st), _ptr(st_out),
+        cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), N, C, HV, _ptr(y), _ptr(beta), _ptr(g))
+    if rc != 0:
+        raise RuntimeError("gdn_oracle_conv_gate failed")
+    return y, beta, g, st_out
+
+
+def split_qkv(y, HK, HV, Dk, Dv):
+    """split(...) of the mixer: the cat(q, k, v) channels of y [.., C] into queries
+    [.., HK, Dk], keys [.., HK, Dk] and values [.., HV, Dv] (head-major channels)."""
+    lead = y.shape[:-1]
+    q = y[..., :HK * Dk].reshape(*lead, HK, Dk)
+    k = y[..., HK * Dk:2 * HK * Dk].reshape(*lead, HK, Dk)
+    v = y[..., 2 * HK * Dk:].reshape(*lead, HV, Dv)
+    return q, k, v
+
+
+def regroup_qkvz(qkvz, ba, HK, HV, Dk, Dv):
+    """The regroup of the fused projections (qwen3_next page, Notes -> "The DeltaNet mixer
+    fuses its projections per key head"): in_proj_qkvz holds, for each key head j, its
+    query (Dk), its key (Dk), then the values of the r = HV/HK value heads it serves
+    (r x Dv), then their output gates (r x Dv); in_proj_ba holds per key head the r
+    value heads' b, then their a.  Returns (q [.., HK, Dk], k [.., HK, Dk],
+    v [.., HV, Dv], z [.., HV, Dv], b [.., HV], a [.., HV]) as float64 views of the
+    inputs' columns."""
+    X, Y = _f64(qkvz), _f64(ba)
+    r = HV // HK
+    lead = X.shape[:-1]
+    per = 2 * Dk + 2 * r * Dv
+    if X.shape[-1] != HK * per or Y.shape[-1] != HK * 2 * r:
+        raise ValueError("regroup_qkvz: widths do not match the head layout")
+    Xh = X.reshape(*lead, HK, per)
+    Yh = Y.reshape(*lead, HK, 2 * r)
+    q = Xh[..., :Dk]
+    k = Xh[..., Dk:2 * Dk]
+    v = Xh[..., 2 * Dk:2 * Dk + r * Dv].reshape(*lead, HV, Dv)
+    z = Xh[..., 2 * Dk + r * Dv:].reshape(*lead, HV, Dv)
+    b = Yh[..., :r].reshape(*lead, HV)
+    a = Yh[..., r:].reshape(*lead, HV)
+    return q, k, v, z, b, a

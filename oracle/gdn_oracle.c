@@ -252,3 +252,68 @@ int gdn_oracle_gated_rmsnorm(const double *y, const double *z, const double *wei
     }
     return 0;
 }
+
+/*
+ * The step before the rule in the mixer (qwen3_5_text page, Notes -> "The DeltaNet
+ * mixer"; qwen3_next page, Notes -> "The DeltaNet mixer fuses its projections per key
+ * head"):
+ *
+ *     q, k, v = split(silu(conv1d(cat(q, k, v))))     causal, width 4
+ *     beta    = sigmoid(b)
+ *     g       = -exp(A_log) * softplus(a + dt_bias)
+ *
+ * conv1d is the depthwise Conv1d of the module listings (kernel_size 4, padding 3,
+ * groups = channels, no bias), cut to the causal outputs: for channel c of token t,
+ *
+ *     conv_t[c] = sum_{i=0..3} w[c][i] * x_{t-3+i}[c]
+ *
+ * where x_tau for tau before the sequence's first token is 0 at the start of a prompt, or
+ * comes from the carried conv state: state[s][3 + tau - start][c] holds x_tau for
+ * tau = start-3 .. start-1 (rows 0, 1, 2 = the third-last, second-last and last input
+ * before the sequence).  The state after the sequence (the last three inputs, reaching
+ * back into the carried state for sequences shorter than three) goes to state_out.
+ *
+ *   x      [T][C]   conv inputs (cat(q, k, v) channels)     y [T][C] = silu(conv)
+ *   b, a   [T][HV]                                          beta, g [T][HV]
+ *   w      [C][4];  A_log, dt_bias [HV]
+ *   state_in / state_out  [N][3][C] or NULL;  cu [N+1] token offsets of the sequences
+ * Returns 0, or -1 on a bad argument.
+ */
+int gdn_oracle_conv_gate(const double *x, const double *b, const double *a, const double *w,
+                         const double *A_log, const double *dt_bias, const double *state_in,
+                         double *state_out, const int64_t *cu, int N, int C, int HV,
+                         double *y, double *beta, double *g)
+{
+    if (!x || !w || !cu || !y || N < 0 || C <= 0 || HV < 0) return -1;
+    if (HV > 0 && (!b || !a || !A_log || !dt_bias || !beta || !g)) return -1;
+    for (int s = 0; s < N; ++s) {
+        const int64_t t0 = cu[s], t1 = cu[s + 1];
+        if (t1 < t0) return -1;
+        /* input of channel c at token tau (tau < t0 reaches into the carried state) */
+#define ORACLE_X(tau, c)                                                                   \
+    ((tau) >= t0 ? x[(tau) * C + (c)]                                                      \
+                 : ((tau) >= t0 - 3 && state_in ? state_in[((int64_t)s * 3 + 3 + ((tau) - t0)) * C + (c)] \
+                                                : 0.0))
+        for (int64_t t = t0; t < t1; ++t) {
+            for (int c = 0; c < C; ++c) {
+                double acc = 0.0;
+                for (int i = 0; i < 4; ++i) acc += w[c * 4 + i] * ORACLE_X(t - 3 + i, c);
+                y[t * C + c] = acc / (1.0 + exp(-acc));
+            }
+            for (int h = 0; h < HV; ++h) {
+                const double bb = b[t * HV + h], aa = a[t * HV + h] + dt_bias[h];
+                beta[t * HV + h] = 1.0 / (1.0 + exp(-bb));
+                /* softplus(u) = log(1 + e^u), written so that it neither overflows nor
+                 * loses the small values */
+                const double sp = aa > 0.0 ? aa + log1p(exp(-aa)) : log1p(exp(aa));
+                g[t * HV + h] = -exp(A_log[h]) * sp;
+            }
+        }
+        if (state_out)
+            for (int r = 0; r < 3; ++r)
+                for (int c = 0; c < C; ++c)
+                    state_out[((int64_t)s * 3 + r) * C + c] = ORACLE_X(t1 - 3 + r, c);
+#undef ORACLE_X
+    }
+    return 0;
+}

@@ -366,3 +366,117 @@ def test_gated_norm_epsilon_and_zero_rows(oracle_mod):
     np.testing.assert_allclose(ratio, 2 ** -0.5, rtol=1e-12)
     zero = oracle_mod.gated_rmsnorm(np.zeros((2, 8)), np.ones((2, 8)), w)
     assert np.all(zero == 0.0)
+
+
+# ---------------------------------------------------------------- conv + gates prologue
+def _conv_case(rng, T, C, HV=2):
+    x = rng.standard_normal((1, T, C))
+    b = rng.standard_normal((1, T, HV)) * 3
+    a = rng.standard_normal((1, T, HV)) * 3
+    w = rng.standard_normal((C, 4))
+    al = rng.standard_normal(HV)
+    db = rng.standard_normal(HV)
+    return x, b, a, w, al, db
+
+
+def _conv_only(oracle_mod, x, w, **kw):
+    """The convolution itself: silu(u) - silu(-u) = u and the convolution is odd in x."""
+    HV = 1
+    z = np.zeros(x.shape[:-1] + (HV,))
+    yp = oracle_mod.conv_gate(x, z, z, w, np.zeros(HV), np.zeros(HV), **kw)[0]
+    kw2 = dict(kw)
+    if kw2.get("conv_state") is not None:
+        kw2["conv_state"] = -kw2["conv_state"]
+    ym = oracle_mod.conv_gate(-x, z, z, w, np.zeros(HV), np.zeros(HV), **kw2)[0]
+    return yp - ym
+
+
+def test_conv_impulse_response_is_causal_depthwise_width_4(oracle_mod):
+    """A unit input on one channel at token 2 comes out on that channel only, at tokens
+    2, 3, 4, 5, weighted by taps 3, 2, 1, 0 (tap 3 on the current token), and nowhere
+    else: causal, depthwise, width 4 (Conv1d(kernel_size=4, padding=3, groups=C))."""
+    T, C = 9, 3
+    w = _rng(70).standard_normal((C, 4))
+    x = np.zeros((1, T, C))
+    x[0, 2, 1] = 1.0
+    conv = _conv_only(oracle_mod, x, w)[0]
+    expect = np.zeros((T, C))
+    expect[2:6, 1] = w[1, ::-1]
+    np.testing.assert_allclose(conv, expect, atol=1e-15, rtol=1e-14)
+
+
+def test_conv_state_continues_the_sequence(oracle_mod):
+    """Prefill of t tokens, then the rest from the carried state, then token by token
+    (decode), all equal one pass over the whole sequence; a sequence shorter than three
+    tokens carries part of the incoming state on."""
+    x, b, a, w, al, db = _conv_case(_rng(71), 11, 5)
+    full = oracle_mod.conv_gate(x, b, a, w, al, db, want_state=True)
+    p1 = oracle_mod.conv_gate(x[:, :4], b[:, :4], a[:, :4], w, al, db, want_state=True)
+    p2 = oracle_mod.conv_gate(x[:, 4:], b[:, 4:], a[:, 4:], w, al, db, conv_state=p1[3],
+                              want_state=True)
+    for i in range(3):
+        np.testing.assert_array_equal(np.concatenate([p1[i], p2[i]], 1), full[i])
+    np.testing.assert_array_equal(p2[3], full[3])
+    st = None
+    for t in range(11):
+        y, _, _, st = oracle_mod.conv_gate(x[:, t:t + 1], b[:, t:t + 1], a[:, t:t + 1], w, al, db,
+                                           conv_state=st, want_state=True)
+        np.testing.assert_array_equal(y[0, 0], full[0][0, t])
+    # a 1-token sequence: the window slides by one
+    s_in = _rng(72).standard_normal((1, 3, 5))
+    _, _, _, s_out = oracle_mod.conv_gate(x[:, :1], b[:, :1], a[:, :1], w, al, db, conv_state=s_in,
+                                          want_state=True)
+    np.testing.assert_array_equal(s_out[0], np.stack([s_in[0, 1], s_in[0, 2], x[0, 0]]))
+
+
+def test_conv_packed_equals_separate(oracle_mod):
+    """Packed sequences restart their windows at each sequence start (from their own
+    carried state), exactly as separate runs."""
+    lens = [5, 1, 0, 7]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    x, b, a, w, al, db = _conv_case(_rng(73), int(cu[-1]), 4)
+    st = _rng(74).standard_normal((len(lens), 3, 4))
+    y, be, g, so = oracle_mod.conv_gate(x, b, a, w, al, db, conv_state=st, cu_seqlens=cu,
+                                        want_state=True)
+    for s, (p, e) in enumerate(zip(cu[:-1], cu[1:])):
+        ys, bs, gs, ss = oracle_mod.conv_gate(x[:, p:e], b[:, p:e], a[:, p:e], w, al, db,
+                                              conv_state=st[s:s + 1], want_state=True)
+        np.testing.assert_array_equal(y[:, p:e], ys)
+        np.testing.assert_array_equal(g[:, p:e], gs)
+        np.testing.assert_array_equal(so[s], ss[0])
+    np.testing.assert_array_equal(so[2], st[2])          # empty sequence: state unchanged
+
+
+def test_gates_closed_forms(oracle_mod):
+    """beta = sigmoid(b): 1/2 at 0, sigmoid(b) + sigmoid(-b) = 1.  g = -exp(A_log)
+    softplus(a + dt_bias): -ln 2 at 0; softplus(u) - softplus(-u) = u gives
+    g(a) - g(-a) = -exp(A_log) a; dt_bias adds to a; no overflow at |a| = 50, and g <= 0."""
+    T, HV = 6, 3
+    x = np.zeros((1, T, 1))
+    w = np.zeros((1, 4))
+    bvals = np.array([0.0, 1.0, -2.5, 7.0, -40.0, 40.0])[None, :, None].repeat(HV, 2)
+    a = np.array([0.0, 0.3, -1.2, 3.0, 50.0, -50.0])[None, :, None].repeat(HV, 2)
+    al = np.array([0.0, np.log(2.0), -1.0])
+    zero = np.zeros(HV)
+    _, beta, g, _ = oracle_mod.conv_gate(x, bvals, a, w, al, zero)
+    _, beta_m, g_m, _ = oracle_mod.conv_gate(x, -bvals, -a, w, al, zero)
+    assert beta[0, 0, 0] == 0.5
+    np.testing.assert_allclose(beta + beta_m, 1.0, rtol=1e-15)
+    np.testing.assert_allclose(g[0, 0], -np.exp(al) * np.log(2.0), rtol=1e-15)
+    np.testing.assert_allclose(g - g_m, -np.exp(al)[None, None, :] * a, rtol=1e-12, atol=1e-14)
+    assert np.all(g <= 0.0) and np.all(np.isfinite(g))
+    db = np.array([0.5, -0.25, 2.0])
+    _, _, g_db, _ = oracle_mod.conv_gate(x, bvals, a, w, al, db)
+    _, _, g_sh, _ = oracle_mod.conv_gate(x, bvals, a + db[None, None, :], w, al, zero)
+    np.testing.assert_allclose(g_db, g_sh, rtol=1e-15)
+
+
+def test_regroup_matches_the_hand_listed_layout(oracle_mod):
+    """tests/golden/regroup_qkvz_hk2_hv4_d2.txt: the columns each field takes, listed by
+    hand from the page's description of the per-key-head layout."""
+    G = _parse_golden(os.path.join(GOLDEN, "regroup_qkvz_hk2_hv4_d2.txt"))
+    qkvz = np.arange(24, dtype=float)[None, :]
+    ba = np.arange(8, dtype=float)[None, :]
+    q, k, v, z, b, a = oracle_mod.regroup_qkvz(qkvz, ba, HK=2, HV=4, Dk=2, Dv=2)
+    for name, got in zip("qkvzba", (q, k, v, z, b, a)):
+        np.testing.assert_array_equal(got[0].reshape(G[name].shape), G[name])
