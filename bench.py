@@ -267,6 +267,31 @@ def bench_gated_norm(gdn, w, iters, warmup, copies=4):
     return res
 
 
+def bench_prologue(gdn, w, iters, warmup, copies=4):
+    """The step before the rule from Qwen3-Next's fused projections of `copies` prompts of
+    workload w (regroup, conv + SiLU, gates, z copied out): the projections are larger
+    than L2, so no flush is needed."""
+    gen = torch.Generator(device="cuda").manual_seed(6)
+    HK, HV, D, T = w.HK, w.HV, w.Dk, w.B * w.T * copies
+    r = HV // HK
+    C = 2 * HK * D + HV * D
+    W = HK * (2 * D + 2 * r * D)
+    proj = torch.randn(copies, T // copies, W, generator=gen, device="cuda").to(w.dtype)
+    ba = torch.randn(copies, T // copies, 2 * HV, generator=gen, device="cuda").to(w.dtype)
+    cw = torch.randn(C, 4, generator=gen, device="cuda") * 0.5
+    al = torch.randn(HV, generator=gen, device="cuda") * 0.5
+    db = torch.randn(HV, generator=gen, device="cuda") * 0.5
+    fn = lambda: gdn.conv_gate_prologue(proj, ba, None, cw, al, db, HK=HK, HV=HV, Dk=D, Dv=D,
+                                        layout="qkvz")
+    times = Timer(flush=False).run(fn, iters, warmup)
+    elt = proj.element_size()
+    nbytes = T * (W * elt + 2 * HV * elt + C * elt + HV * D * elt + 2 * HV * 4) + C * 16 + HV * 8
+    res = dict(tokens=T, ms=statistics.mean(times), bytes=nbytes)
+    del proj, ba, cw, al, db
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_e2e(gdn, w, iters, warmup):
     """Public API end to end: pinned host inputs -> device, prefill, out and final state
     back to pinned host memory, every step."""
@@ -453,6 +478,14 @@ def main():
             roofline={"bound": "hbm", "achieved": dg["bytes"] / (dg["ms"] * 1e-3) / 1e9, "peak": hbm,
                       "unit": "GB/s", "frac": dg["bytes"] / (dg["ms"] * 1e-3) / 1e9 / hbm,
                       "algorithmic_bytes": dg["bytes"]})
+        pr = bench_prologue(gdn, head_w, max(args.steps, 20), args.warmup)
+        subs["prologue"] = dict(
+            workload="conv + gates from the fused projections of 4 next_prefill_T4096_hk16_hv32_d128 "
+                     "prompts (400 MB, larger than L2: no flush)",
+            tokens=pr["tokens"], ms=pr["ms"],
+            roofline={"bound": "hbm", "achieved": pr["bytes"] / (pr["ms"] * 1e-3) / 1e9, "peak": hbm,
+                      "unit": "GB/s", "frac": pr["bytes"] / (pr["ms"] * 1e-3) / 1e9 / hbm,
+                      "algorithmic_bytes": pr["bytes"]})
         gn = bench_gated_norm(gdn, head_w, max(args.steps, 20), args.warmup)
         subs["gated_norm"] = dict(
             workload="gated RMS norm of 4 next_prefill_T4096_hk16_hv32_d128 outputs "

@@ -21,7 +21,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["prefill", "prefill_varlen", "decode_step", "gated_rmsnorm", "state_layout", "workspace_size",
+__all__ = ["prefill", "prefill_varlen", "decode_step", "gated_rmsnorm", "conv_gate_prologue",
+           "state_layout", "workspace_size",
            "workspace_status", "selftest_wait_timeout", "GdnError", "library_path",
            "load_library", "abi"]
 
@@ -78,6 +79,9 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_decode_step_gated.restype = i
     lib.gdn_decode_step_gated.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, fp, f, i, i, i, i, i, i,
                                           f, i, vp]
+    lib.gdn_conv_gate_prologue.restype = i
+    lib.gdn_conv_gate_prologue.argtypes = [vp, vp, vp, i, fp, fp, fp, vp, vp, vp, i, ctypes.c_int64,
+                                           i, i, i, i, i, vp, vp, vp, vp, fp, fp, vp]
     lib.gdn_gated_rmsnorm.restype = i
     lib.gdn_gated_rmsnorm.argtypes = [vp, vp, fp, vp, ctypes.c_int64, i, i, f, vp]
     lib.gdn_state_layout.restype = i
@@ -322,3 +326,58 @@ def gated_rmsnorm(y, gate, norm_weight, *, eps=1e-6, out=None, stream=None):
                                           Dv, _DTYPES[dt], float(eps), _stream(stream))
     _check(rc, "gdn_gated_rmsnorm")
     return out
+
+
+LAYOUTS = {"qkv": 0, "qkvz": 1}
+
+
+def conv_gate_prologue(proj, proj_b, proj_a, conv_weight, A_log, dt_bias, *, HK, HV, Dk, Dv,
+                       layout="qkv", conv_state=None, conv_state_out=None, cu_seqlens=None,
+                       stream=None):
+    """The step before the rule (gdn_conv_gate_prologue): from the projections' outputs
+    proj [B, T, W] (layout "qkv": the cat(q, k, v) channels, with proj_b, proj_a
+    [B, T, HV]; layout "qkvz": Qwen3-Next's per-key-head fused layout, with proj_b the
+    fused b/a [B, T, 2 HV] and proj_a None), conv_weight [C, 4], A_log and dt_bias [HV]
+    (float32), the carried conv_state [N, 3, C] or None.  ``conv_state_out`` receives the
+    state after each sequence (it may be conv_state).  Packed form: B == 1 and
+    ``cu_seqlens`` [N+1] int32.  Returns a dict with queries, keys [B, T, HK, Dk],
+    values [B, T, HV, Dv], beta, decays [B, T, HV] float32 and, for "qkvz", z
+    [B, T, HV, Dv]."""
+    _need(proj, "proj")
+    dev, dt = proj.device, proj.dtype
+    if dt not in _DTYPES:
+        raise ValueError("proj must be bfloat16 or float32")
+    B, T = proj.shape[0], proj.shape[1]
+    lay = LAYOUTS[layout]
+    C = 2 * HK * Dk + HV * Dv
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("packed form needs batch 1")
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    _need(proj_b, "proj_b", dt, dev)
+    if lay == 0:
+        _need(proj_a, "proj_a", dt, dev, tuple(proj_b.shape))
+    _need(conv_weight, "conv_weight", torch.float32, dev, (C, 4))
+    _need(A_log, "A_log", torch.float32, dev, (HV,))
+    _need(dt_bias, "dt_bias", torch.float32, dev, (HV,))
+    if conv_state is not None:
+        _need(conv_state, "conv_state", dt, dev, (N, 3, C))
+    if conv_state_out is not None:
+        _need(conv_state_out, "conv_state_out", dt, dev, (N, 3, C))
+    o = dict(queries=torch.empty(B, T, HK, Dk, dtype=dt, device=dev),
+             keys=torch.empty(B, T, HK, Dk, dtype=dt, device=dev),
+             values=torch.empty(B, T, HV, Dv, dtype=dt, device=dev),
+             beta=torch.empty(B, T, HV, dtype=torch.float32, device=dev),
+             decays=torch.empty(B, T, HV, dtype=torch.float32, device=dev))
+    if lay == 1:
+        o["z"] = torch.empty(B, T, HV, Dv, dtype=dt, device=dev)
+    rc = load_library().gdn_conv_gate_prologue(
+        _ptr(proj), _ptr(proj_b), _ptr(proj_a), lay, _ptr(conv_weight), _ptr(A_log),
+        _ptr(dt_bias), _ptr(conv_state), _ptr(conv_state_out), _ptr(cu_seqlens), N, B * T,
+        HK, HV, Dk, Dv, _DTYPES[dt], _ptr(o["queries"]), _ptr(o["keys"]), _ptr(o["values"]),
+        _ptr(o.get("z")), _ptr(o["beta"]), _ptr(o["decays"]), _stream(stream))
+    _check(rc, "gdn_conv_gate_prologue")
+    return o

@@ -172,6 +172,39 @@ int gdn_decode_step_gated(const void *queries, const void *keys, const void *val
                          dtype, scale, use_qk_l2norm, gate_z, norm_weight, norm_eps, cuda_stream);
 }
 
+int gdn_conv_gate_prologue(const void *proj, const void *proj_b, const void *proj_a,
+                           gdn_proj_layout layout, const float *conv_weight, const float *A_log,
+                           const float *dt_bias, const void *conv_state_in, void *conv_state_out,
+                           const int32_t *cu_seqlens, int N, int64_t T_total, int HK, int HV,
+                           int Dk, int Dv, gdn_dtype dtype, void *queries, void *keys,
+                           void *values, void *gate_z, float *beta, float *decays,
+                           void *cuda_stream) {
+    int rc = check_common(HK, HV, Dk, Dv, dtype, 1.f);
+    if (rc != GDN_OK) return rc;
+    if (layout != GDN_LAYOUT_QKV && layout != GDN_LAYOUT_QKVZ) return GDN_ERR_INVALID_ARG;
+    if (N < 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
+    if (N > 65535) return GDN_ERR_UNSUPPORTED;
+    if (!cu_seqlens && (N == 0 ? T_total != 0 : T_total % N != 0)) return GDN_ERR_INVALID_ARG;
+    if (T_total > 0) {
+        if (!proj || !proj_b || !conv_weight || !A_log || !dt_bias || !queries || !keys ||
+            !values || !beta || !decays)
+            return GDN_ERR_INVALID_ARG;
+        if (layout == GDN_LAYOUT_QKV && !proj_a) return GDN_ERR_INVALID_ARG;
+    }
+    if (layout == GDN_LAYOUT_QKV && gate_z) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {proj, proj_b, proj_a, conv_weight, A_log, dt_bias, conv_state_in,
+                          conv_state_out, cu_seqlens, queries, keys, values, gate_z, beta, decays};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+    const int T_seq = (!cu_seqlens && N > 0) ? (int)(T_total / N) : 0;
+    if (!cu_seqlens && N > 0 && T_total / N > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+    cudaError_t e = launch_prologue(proj, proj_b, proj_a, (int)layout, conv_weight, A_log, dt_bias,
+                                    conv_state_in, conv_state_out, cu_seqlens, N, T_seq, T_total,
+                                    HK, HV, Dk, Dv, dtype, queries, keys, values, gate_z, beta,
+                                    decays, (cudaStream_t)cuda_stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int gdn_gated_rmsnorm(const void *y, const void *gate_z, const float *norm_weight, void *out,
                       int64_t rows, int Dv, gdn_dtype dtype, float norm_eps, void *cuda_stream) {
     if (rows < 0 || !(norm_eps >= 0.f) || isinf(norm_eps)) return GDN_ERR_INVALID_ARG;

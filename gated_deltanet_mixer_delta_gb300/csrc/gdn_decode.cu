@@ -138,7 +138,7 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
 #pragma unroll
         for (int w = 0; w < DV / 32; ++w) ss += s_nrm[w];
         const float inv = rsqrtf(ss * (1.f / DV) + eps);
-        out[(size_t)bh * DV + tid] = from_f32<Tin>(yo * inv * gwv * (gzv / (1.f + expf(-gzv))));
+        out[(size_t)bh * DV + tid] = from_f32<Tin>(yo * inv * gwv * silu_f(gzv));
     }
 }
 

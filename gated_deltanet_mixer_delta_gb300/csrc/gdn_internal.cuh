@@ -67,6 +67,14 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
                           int Dk, int Dv, gdn_dtype dtype, float scale, int l2norm,
                           const void *gate_z, const float *norm_weight, float norm_eps,
                           cudaStream_t st);
+// The step before the rule: conv + SiLU of the cat(q, k, v) channels, gates; the conv
+// state after each sequence when state_out is given (may be state_in)
+cudaError_t launch_prologue(const void *proj, const void *proj_b, const void *proj_a, int layout,
+                            const float *conv_w, const float *A_log, const float *dt_bias,
+                            const void *state_in, void *state_out, const int32_t *cu, int N,
+                            int T_seq, int64_t T, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                            void *q, void *k, void *v, void *z, float *beta, float *g,
+                            cudaStream_t st);
 // Gated RMS norm of rows of Dv values: out = y / sqrt(mean(y^2) + eps) * w * silu(z)
 cudaError_t launch_gated_norm(const void *y, const void *z, const float *w, void *out, int64_t rows,
                               int Dv, gdn_dtype dtype, float eps, cudaStream_t st);
@@ -79,6 +87,10 @@ template <> __device__ __forceinline__ float from_f32<float>(float x) { return x
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
 }
+
+// silu(x) = x sigmoid(x) from the MUFU exponential and the approximate division (a few
+// parts in 1e6 relative; x -> -inf gives -0, x -> +inf gives x)
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll

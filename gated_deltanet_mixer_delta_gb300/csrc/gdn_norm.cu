@@ -19,8 +19,6 @@ namespace {
 constexpr int kNormThreads = 256;
 constexpr int kNormRowsPerThread = 1;
 
-__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
-
 // 16 bytes of T as floats
 template <typename T> struct Pack16;
 template <> struct Pack16<__nv_bfloat16> {
@@ -104,7 +102,7 @@ gated_norm_kernel(const T *__restrict__ y, const T *__restrict__ z, const float 
         const float inv = rsqrtf(ss * (1.f / DV) + eps);
         float o[E];
 #pragma unroll
-        for (int i = 0; i < E; ++i) o[i] = yv[i] * inv * wt[i] * silu(zv[i]);
+        for (int i = 0; i < E; ++i) o[i] = yv[i] * inv * wt[i] * silu_f(zv[i]);
         if (r < rows) __stcs(reinterpret_cast<uint4 *>(out + r * DV) + l, Pack16<T>::pack(o));
     }
 }

@@ -73,6 +73,12 @@ typedef enum {
 
 typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
 
+/* Layout of the projections feeding gdn_conv_gate_prologue */
+typedef enum {
+    GDN_LAYOUT_QKV = 0,   /* in_proj_qkv: the cat(q, k, v) channels; in_proj_b, in_proj_a */
+    GDN_LAYOUT_QKVZ = 1   /* in_proj_qkvz / in_proj_ba grouped per key head (Qwen3-Next)  */
+} gdn_proj_layout;
+
 /*
  * Chunked prefill over a batch of equal-length sequences ("a prompt's chunked
  * one", linear_attn value table).  Runs the rule over every (batch row, value
@@ -147,6 +153,56 @@ int gdn_decode_step(const void *queries, const void *keys, const void *values,
                     float *state, void *out,
                     int B, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
                     float scale, int use_qk_l2norm, void *cuda_stream);
+
+/*
+ * The step before the rule in the mixer (qwen3_5_text page, Notes -> "The DeltaNet
+ * mixer"; qwen3_next page, Notes -> "The DeltaNet mixer fuses its projections per key
+ * head"), writing the rule's inputs:
+ *
+ *     queries, keys, values = split(silu(conv1d(cat(q, k, v))))   causal, width 4
+ *     beta   = sigmoid(b)
+ *     decays = -exp(A_log) * softplus(a + dt_bias)
+ *
+ * conv1d is the depthwise Conv1d of the pages' module listings (kernel_size 4, padding 3,
+ * groups = channels, no bias), causal: channel c at token t is
+ * sum_{i=0..3} conv_weight[c][i] * x_{t-3+i}[c].  C = 2*HK*Dk + HV*Dv channels in the
+ * order q (head-major), k, v.
+ *
+ *   layout GDN_LAYOUT_QKV (Qwen3.5):
+ *     proj    [T_total, C] dtype       in_proj_qkv output
+ *     proj_b  [T_total, HV] dtype      in_proj_b output;  proj_a [T_total, HV] in_proj_a
+ *   layout GDN_LAYOUT_QKVZ (Qwen3-Next), regrouped on the fly:
+ *     proj    [T_total, HK*(2*Dk + 2*r*Dv)] dtype, r = HV/HK: per key head its query,
+ *             its key, the values of its r value heads, then their output gates
+ *     proj_b  [T_total, HK*2*r] dtype: per key head the r value heads' b, then their a;
+ *     proj_a  unused (NULL)
+ *     gate_z  [T_total, HV, Dv] dtype receives the output gates z (for the gated norm),
+ *             or NULL
+ *   conv_weight  [C, 4] float32 (a Conv1d weight [C, 1, 4]; tap 3 is the current token)
+ *   A_log, dt_bias [HV] float32
+ *   conv_state_in  [N, 3, C] dtype: the three inputs before each sequence, oldest first
+ *                  (a prompt's continuation, or the decode cache), or NULL (zeros: the
+ *                  start of a prompt)
+ *   conv_state_out [N, 3, C] dtype: the three inputs before the token after each
+ *                  sequence, or NULL; may be conv_state_in (updated in place)
+ *   cu_seqlens     [N+1] int32 device token offsets, or NULL: N sequences of
+ *                  T_total / N tokens (a decode step is N sequences of one token)
+ *   queries, keys  [T_total, HK, Dk] dtype;  values [T_total, HV, Dv] dtype
+ *   beta, decays   [T_total, HV] float32
+ * Dk = Dv in {32, 64, 128}; HV % HK == 0.  T_total == 0 with conv_state_out copies the
+ * states.  All pointers 16-byte aligned, tensors contiguous.
+ * Errors: GDN_ERR_INVALID_ARG (null pointer, bad sizes, T_total % N != 0 without
+ * cu_seqlens), GDN_ERR_UNSUPPORTED, GDN_ERR_MISALIGNED, GDN_ERR_CUDA.  cu_seqlens is not
+ * validated on the device: it must be nondecreasing from 0 to T_total.
+ */
+int gdn_conv_gate_prologue(const void *proj, const void *proj_b, const void *proj_a,
+                           gdn_proj_layout layout, const float *conv_weight,
+                           const float *A_log, const float *dt_bias,
+                           const void *conv_state_in, void *conv_state_out,
+                           const int32_t *cu_seqlens, int N, int64_t T_total,
+                           int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                           void *queries, void *keys, void *values, void *gate_z,
+                           float *beta, float *decays, void *cuda_stream);
 
 /*
  * Gated RMS norm of the mixer output, the step that follows the rule in the mixer
