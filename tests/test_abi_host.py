@@ -187,3 +187,25 @@ def _decode_gated(lib, **kw):
 ])
 def test_gated_decode_rejects_bad_arguments_on_host(lib, kw, code):
     assert _decode_gated(lib, **kw) == code
+
+
+def _prologue(lib, **kw):
+    a = dict(proj=P, pb=P, pa=P, layout=0, w=P, al=P, db=P, sin=None, sout=None, cu=None, N=2,
+             T=64, HK=2, HV=4, Dk=128, Dv=128, dtype=0, q=P, k=P, v=P, z=None, beta=P, g=P,
+             stream=None)
+    a.update(kw)
+    return lib.gdn_conv_gate_prologue(a["proj"], a["pb"], a["pa"], a["layout"], a["w"], a["al"],
+                                      a["db"], a["sin"], a["sout"], a["cu"], a["N"], a["T"], a["HK"],
+                                      a["HV"], a["Dk"], a["Dv"], a["dtype"], a["q"], a["k"], a["v"],
+                                      a["z"], a["beta"], a["g"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(layout=2), -1), (dict(N=-1), -1), (dict(T=-4), -1), (dict(T=63), -1),
+    (dict(pa=None), -1), (dict(proj=None), -1), (dict(w=None), -1), (dict(g=None), -1),
+    (dict(z=P), -1), (dict(HV=3), -1), (dict(Dk=96, Dv=96), -2), (dict(dtype=4), -2),
+    (dict(N=70000, T=70000), -2), (dict(proj=P + 8), -3), (dict(sin=P + 4), -3),
+    (dict(layout=1, pa=None, z=P + 2), -3),
+])
+def test_prologue_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _prologue(lib, **kw) == code
