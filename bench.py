@@ -428,6 +428,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline and decode only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="comma list of prologue, gated_norm, decode_gated_norm: time just those "
+                         "steps and print one line each (profiling; not the bench line)")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="override the headline prefill length (profiling a case larger than L2)")
     args = ap.parse_args()
@@ -448,6 +451,18 @@ def main():
 
     W = workloads.WORKLOADS
     head_w = W["next_prefill_T4096_hk16_hv32_d128"]
+    if args.only:
+        runs = {"prologue": lambda: bench_prologue(gdn, head_w, args.steps, args.warmup),
+                "gated_norm": lambda: bench_gated_norm(gdn, head_w, args.steps, args.warmup),
+                "decode_gated_norm": lambda: bench_decode_gated(gdn, W["decode_B256_hk16_hv32_d128"],
+                                                                args.steps, args.warmup)}
+        for name in args.only.split(","):
+            r = runs[name]()
+            if rank == 0:
+                print(json.dumps({"only": name, "ms": r["ms"], "bytes": r["bytes"],
+                                  "hbm_frac": r["bytes"] / (r["ms"] * 1e-3) / 1e9 / hbm}))
+        clocks.stop()
+        return
     barrier(ws)
     head = bench_prefill(gdn, head_w, args.steps, args.warmup, T_override=args.prefill_T or None)
     barrier(ws)

@@ -14,10 +14,11 @@
 // before a sequence's first token come from its carried conv state [N][3][C] (the three
 // inputs before it, oldest first) or are zero.
 //
-// HBM-bound elementwise work: every thread owns 16 bytes of consecutive channels (8 bf16
-// or 4 fp32, never straddling a head) over a tile of 8 tokens, requests their inputs
-// together (the three before the tile come mostly from L2), runs a sliding three-token
-// window in registers, and writes the SiLU'd values straight into
+// HBM-bound elementwise work: every conv thread owns 8 bytes of consecutive channels (4
+// bf16 or 2 fp32, never straddling a head) over a tile of 16 tokens; it stages the tile's
+// inputs and the three before it (mostly L2 hits) in shared memory with asynchronous
+// copies, which hold no registers while in flight, so that several blocks fit on an SM;
+// it runs a sliding three-token window in registers and writes the SiLU'd values into
 // the queries / keys / values tensors of the rule.  One block per tile forms the gates;
 // with the fused layout further blocks copy the output gates z out.  The conv state after
 // each sequence is written by a second kernel, once every read of the incoming state is
@@ -28,7 +29,7 @@ namespace gdn {
 namespace {
 
 constexpr int kProThreads = 256;
-constexpr int kProTile = 8;                            // tokens per tile
+constexpr int kProTile = 16;                           // tokens per tile
 constexpr int kProBatch = 8;                           // tokens whose loads go out together
 
 struct ProParams {
@@ -82,6 +83,43 @@ template <> struct V16<float> {
     }
 };
 
+// 8 bytes of T (4 bf16 or 2 fp32): the conv's per-thread channel group
+template <typename T> struct V8;
+template <> struct V8<__nv_bfloat16> {
+    static constexpr int E = 4;
+    static __device__ __forceinline__ void unpack(const uint2 &r, float (&x)[4]) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r);
+        const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    }
+    static __device__ __forceinline__ uint2 pack(const float (&x)[4]) {
+        uint2 r;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&r);
+        h[0] = __floats2bfloat162_rn(x[0], x[1]);
+        h[1] = __floats2bfloat162_rn(x[2], x[3]);
+        return r;
+    }
+};
+template <> struct V8<float> {
+    static constexpr int E = 2;
+    static __device__ __forceinline__ void unpack(const uint2 &r, float (&x)[2]) {
+        x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
+    }
+    static __device__ __forceinline__ uint2 pack(const float (&x)[2]) {
+        return make_uint2(__float_as_uint(x[0]), __float_as_uint(x[1]));
+    }
+};
+
+// 8-byte global -> shared copy that holds no register while in flight
+__device__ __forceinline__ void cp_async8(void *sdst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ int64_t seq_start(const ProParams &p, int s) {
     return p.cu ? (int64_t)p.cu[s] : (int64_t)s * p.T_seq;
 }
@@ -115,9 +153,12 @@ __device__ __forceinline__ int64_t proj_width(const ProParams &p) {
 template <typename T>
 __global__ void __launch_bounds__(kProThreads)
 prologue_kernel(ProParams p) {
-    constexpr int E = V16<T>::E;
+    constexpr int E = V16<T>::E;                       // z copy: 16 bytes a thread
+    constexpr int EC = V8<T>::E;                       // conv: 8 bytes a thread
+    // the conv thread's inputs: the tile's tokens and the three before it
+    __shared__ uint2 sx[kProTile + 3][kProThreads];
     const int C = 2 * p.HK * p.Dk + p.HV * p.Dv;
-    const int nconv = (C / E + kProThreads - 1) / kProThreads;
+    const int nconv = (C / EC + kProThreads - 1) / kProThreads;
     const int nz = p.z ? ((p.HV * p.Dv) / E + kProThreads - 1) / kProThreads : 0;
     const int64_t tb = (int64_t)blockIdx.x * kProTile;   // token tile along x (no limit)
     const int64_t te = min(p.T, tb + kProTile);
@@ -126,16 +167,23 @@ prologue_kernel(ProParams p) {
     const int bx = blockIdx.y;                            // conv / z / gate block
 
     if (bx < nconv) {
-        // ---- conv + SiLU of E consecutive channels
-        const int c = (bx * kProThreads + threadIdx.x) * E;
+        // ---- conv + SiLU of EC consecutive channels
+        const int c = (bx * kProThreads + threadIdx.x) * EC;
         if (c >= C) return;
-        float w[4][E];
+        const int64_t col = proj_col(p, c);
+        // every input row the tile may read, fetched asynchronously; a thread reads back
+        // only its own slots, so no barrier is needed
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
+        for (int i = 0; i < kProTile + 3; ++i) {
+            const int64_t tau = tb - 3 + i;
+            if (tau >= 0 && tau < te) cp_async8(&sx[i][threadIdx.x], proj + tau * W + col);
+        }
+        float w[4][EC];
+#pragma unroll
+        for (int e = 0; e < EC; ++e) {
             const float4 w4 = *reinterpret_cast<const float4 *>(p.conv_w + (size_t)(c + e) * 4);
             w[0][e] = w4.x; w[1][e] = w4.y; w[2][e] = w4.z; w[3][e] = w4.w;
         }
-        const int64_t col = proj_col(p, c);
         const int nq = p.HK * p.Dk;
         T *dst;
         int64_t dstride;
@@ -145,53 +193,48 @@ prologue_kernel(ProParams p) {
         const T *sin = reinterpret_cast<const T *>(p.state_in);
         int s = seq_of(p, tb);
         int64_t t0 = seq_start(p, s), t1 = seq_start(p, s + 1);
+        cp_async_wait_all();
         // x_tau of this thread's channels, tau in the sequence s or its three predecessors
-        auto xin = [&](int64_t tau, float (&x)[E]) {
+        auto xin = [&](int64_t tau, float (&x)[EC]) {
             if (tau >= t0) {
-                V16<T>::get(proj + tau * W + col, x);
+                V8<T>::unpack(sx[tau - (tb - 3)][threadIdx.x], x);
             } else if (sin && tau >= t0 - 3) {
-                V16<T>::get(sin + ((int64_t)s * 3 + 3 + (tau - t0)) * C + c, x);
+                V8<T>::unpack(*reinterpret_cast<const uint2 *>(sin + ((int64_t)s * 3 + 3 + (tau - t0)) * C + c), x);
             } else {
 #pragma unroll
-                for (int e = 0; e < E; ++e) x[e] = 0.f;
+                for (int e = 0; e < EC; ++e) x[e] = 0.f;
             }
         };
-        float x3[E], x2[E], x1[E];                     // x_{t-3}, x_{t-2}, x_{t-1}
+        float x3[EC], x2[EC], x1[EC];                  // x_{t-3}, x_{t-2}, x_{t-1}
         xin(tb - 3, x3);
         xin(tb - 2, x2);
         xin(tb - 1, x1);
-        for (int64_t t8 = tb; t8 < te; t8 += kProBatch) {
-            uint4 raw[kProBatch];                      // the batch's inputs, requested together
 #pragma unroll
-            for (int u = 0; u < kProBatch; ++u)
-                if (t8 + u < te) raw[u] = *reinterpret_cast<const uint4 *>(proj + (t8 + u) * W + col);
-#pragma unroll
-            for (int u = 0; u < kProBatch; ++u) {
-                const int64_t t = t8 + u;
-                if (t >= te) break;
-                if (t >= t1) {
-                    // next non-empty sequence: its window comes from its carried state
-                    do {
-                        ++s;
-                        t0 = seq_start(p, s);
-                        t1 = seq_start(p, s + 1);
-                    } while (t >= t1);
-                    xin(t - 3, x3);
-                    xin(t - 2, x2);
-                    xin(t - 1, x1);
-                }
-                float x0[E], o[E];
-                V16<T>::unpack(raw[u], x0);
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float acc = w[0][e] * x3[e] + w[1][e] * x2[e] + w[2][e] * x1[e] + w[3][e] * x0[e];
-                    o[e] = silu_f(acc);
-                    x3[e] = x2[e];
-                    x2[e] = x1[e];
-                    x1[e] = x0[e];
-                }
-                V16<T>::put(dst + t * dstride, o);
+        for (int u = 0; u < kProTile; ++u) {
+            const int64_t t = tb + u;
+            if (t >= te) break;
+            if (t >= t1) {
+                // next non-empty sequence: its window comes from its carried state
+                do {
+                    ++s;
+                    t0 = seq_start(p, s);
+                    t1 = seq_start(p, s + 1);
+                } while (t >= t1);
+                xin(t - 3, x3);
+                xin(t - 2, x2);
+                xin(t - 1, x1);
             }
+            float x0[EC], o[EC];
+            V8<T>::unpack(sx[u + 3][threadIdx.x], x0);
+#pragma unroll
+            for (int e = 0; e < EC; ++e) {
+                const float acc = w[0][e] * x3[e] + w[1][e] * x2[e] + w[2][e] * x1[e] + w[3][e] * x0[e];
+                o[e] = silu_f(acc);
+                x3[e] = x2[e];
+                x2[e] = x1[e];
+                x1[e] = x0[e];
+            }
+            *reinterpret_cast<uint2 *>(dst + t * dstride) = V8<T>::pack(o);
         }
     } else if (bx < nconv + nz) {
         // ---- output gates z of the fused layout, copied out per value head
@@ -271,9 +314,9 @@ conv_state_kernel(ProParams p) {
 
 template <typename T>
 cudaError_t launch_t(const ProParams &p, cudaStream_t st) {
-    constexpr int E = V16<T>::E;
+    constexpr int E = V16<T>::E, EC = V8<T>::E;
     const int C = 2 * p.HK * p.Dk + p.HV * p.Dv;
-    const int nconv = (C / E + kProThreads - 1) / kProThreads;
+    const int nconv = (C / EC + kProThreads - 1) / kProThreads;
     const int nz = p.z ? ((p.HV * p.Dv) / E + kProThreads - 1) / kProThreads : 0;
     const int64_t tiles = (p.T + kProTile - 1) / kProTile;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
