@@ -293,37 +293,63 @@ def bench_prologue(gdn, w, iters, warmup, copies=4):
 
 
 def bench_e2e(gdn, w, iters, warmup):
-    """Public API end to end: pinned host inputs -> device, prefill, out and final state
-    back to pinned host memory, every step."""
+    """Public API end to end: every step copies its inputs from pinned host memory to the
+    device, runs the prefill and copies the output and the final state back to pinned
+    host memory.  Consecutive steps are pipelined the way a serving loop runs them: step
+    i + 1's inputs go in and step i - 1's results come out while step i computes (two
+    buffer sets, one stream each for copies in, compute and copies out, ordered by
+    events).  The wall-clock time of all steps, to the last result on the host, is
+    divided by the steps."""
     d = workloads.workload_inputs(w, device="cpu")
     names = ("queries", "keys", "values", "decays", "beta")
     host = {n: d[n].pin_memory() for n in names}
-    dev = {n: torch.empty_like(host[n], device="cuda") for n in names}
     B, T = w.B, w.T
-    out_h = torch.empty(B, T, w.HV, w.Dv, dtype=w.dtype).pin_memory()
-    fin_h = torch.empty(B, w.HV, w.Dk, w.Dv, dtype=torch.float32).pin_memory()
-    out_d = torch.empty_like(out_h, device="cuda")
-    fin_d = torch.empty_like(fin_h, device="cuda")
+    nb = 2
+    dev = [{n: torch.empty_like(host[n], device="cuda") for n in names} for _ in range(nb)]
+    out_h = [torch.empty(B, T, w.HV, w.Dv, dtype=w.dtype).pin_memory() for _ in range(nb)]
+    fin_h = [torch.empty(B, w.HV, w.Dk, w.Dv, dtype=torch.float32).pin_memory() for _ in range(nb)]
+    out_d = [torch.empty_like(out_h[0], device="cuda") for _ in range(nb)]
+    fin_d = [torch.empty_like(fin_h[0], device="cuda") for _ in range(nb)]
     ws = torch.empty(gdn.workspace_size(B * T, B, w.HV, w.Dk, w.Dv), dtype=torch.uint8,
                      device="cuda")
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nb)]
+    ev_run = [torch.cuda.Event() for _ in range(nb)]
+    ev_out = [torch.cuda.Event() for _ in range(nb)]
+    started = [False] * nb
 
-    def step():
-        for n in names:
-            dev[n].copy_(host[n], non_blocking=True)
-        gdn.prefill(dev["queries"], dev["keys"], dev["values"], dev["decays"], dev["beta"],
-                    None, out=out_d, final_state=fin_d, workspace=ws)
-        out_h.copy_(out_d, non_blocking=True)
-        fin_h.copy_(fin_d, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+    def step(i):
+        b = i % nb
+        if started[b]:
+            s_in.wait_event(ev_run[b])              # step i - 2 has read buffer set b
+        with torch.cuda.stream(s_in):
+            for n in names:
+                dev[b][n].copy_(host[n], non_blocking=True)
+        ev_in[b].record(s_in)
+        s_run.wait_event(ev_in[b])
+        if started[b]:
+            s_run.wait_event(ev_out[b])             # step i - 2's results have left
+        gdn.prefill(dev[b]["queries"], dev[b]["keys"], dev[b]["values"], dev[b]["decays"],
+                    dev[b]["beta"], None, out=out_d[b], final_state=fin_d[b], workspace=ws,
+                    stream=s_run)
+        ev_run[b].record(s_run)
+        s_out.wait_event(ev_run[b])
+        with torch.cuda.stream(s_out):
+            out_h[b].copy_(out_d[b], non_blocking=True)
+            fin_h[b].copy_(fin_d[b], non_blocking=True)
+        ev_out[b].record(s_out)
+        started[b] = True
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(iters):
-        step()
+    for i in range(iters):
+        step(warmup + i)
+    torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / iters
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * 4
+    d2h = out_h[0].numel() * out_h[0].element_size() + fin_h[0].numel() * 4
     return dict(s=dt, h2d=h2d, d2h=d2h, tokens=B * T)
 
 
