@@ -96,24 +96,25 @@ def test_prologue_matches_oracle(gdn, layout, HK, HV, D, dtype, with_state):
         assert np.array_equal(out["z"].double().cpu().numpy(), ref["z"])
 
 
-def test_prologue_packed_sequences_and_in_place_state(gdn):
-    """Packed sequences (some shorter than the window, one empty) with their own carried
-    conv states, the states updated in place; against the oracle and bitwise against
-    separate calls."""
+@pytest.mark.parametrize("layout", ["qkv", "qkvz"])
+def test_prologue_packed_sequences_and_in_place_state(gdn, layout):
+    """Packed sequences (some shorter than the window, one empty, one spanning several
+    tiles) with their own carried conv states, the states updated in place; against the
+    oracle and bitwise against separate calls."""
     HK, HV, D, dtype = 2, 4, 128, torch.bfloat16
     lens = [40, 1, 2, 0, 33, 5]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     T = int(cu[-1])
-    proj, pb, pa, w, al, db, _ = _params(HK, HV, D, 17, dtype, "qkv", 1, T, False)
+    proj, pb, pa, w, al, db, _ = _params(HK, HV, D, 17, dtype, layout, 1, T, False)
     C = 2 * HK * D + HV * D
     st = torch.randn(len(lens), 3, C, generator=torch.Generator().manual_seed(18)).to(dtype)
     cp, cb, ca, cw, cal, cdb, cst = _cuda(proj, pb, pa, w, al, db, st)
     st_before = cst.clone()
-    out = gdn.conv_gate_prologue(cp, cb, ca, cw, cal, cdb, HK=HK, HV=HV, Dk=D, Dv=D,
+    out = gdn.conv_gate_prologue(cp, cb, ca, cw, cal, cdb, HK=HK, HV=HV, Dk=D, Dv=D, layout=layout,
                                  conv_state=cst, conv_state_out=cst,
                                  cu_seqlens=torch.from_numpy(cu).cuda())
     torch.cuda.synchronize()
-    ref = _oracle(proj, pb, pa, w, al, db, st, HK, HV, D, "qkv", cu=cu)
+    ref = _oracle(proj, pb, pa, w, al, db, st, HK, HV, D, layout, cu=cu)
     for key in ("queries", "keys", "values"):
         _close(out[key], ref[key], RTOL[dtype], what=key)
     assert np.array_equal(cst.double().cpu().numpy(), ref["state"])
@@ -122,10 +123,11 @@ def test_prologue_packed_sequences_and_in_place_state(gdn):
         if a == b:
             continue
         # fresh (16-byte aligned) copies of the sequence's rows
-        one = gdn.conv_gate_prologue(cp[:, a:b].clone(), cb[:, a:b].clone(), ca[:, a:b].clone(),
-                                     cw, cal, cdb, HK=HK, HV=HV, Dk=D, Dv=D,
+        one = gdn.conv_gate_prologue(cp[:, a:b].clone(), cb[:, a:b].clone(),
+                                     None if ca is None else ca[:, a:b].clone(),
+                                     cw, cal, cdb, HK=HK, HV=HV, Dk=D, Dv=D, layout=layout,
                                      conv_state=st_before[s:s + 1].clone())
-        for key in ("queries", "values", "decays"):
+        for key in ("queries", "values", "decays") + (("z",) if layout == "qkvz" else ()):
             assert torch.equal(one[key][0], out[key][0, a:b])
 
 
