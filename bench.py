@@ -170,7 +170,9 @@ class Timer:
         return [a.elapsed_time(b) for a, b in evs]   # ms
 
 
-def bench_prefill(gdn, w, iters, warmup, states=False, T_override=None):
+def bench_prefill(gdn, w, iters, warmup, states=False, T_override=None, gated=False):
+    """One prefill call of workload w; ``gated``: followed by the gated RMS norm of the
+    output (gdn_prefill_gated / gdn_prefill_varlen_gated)."""
     d = workloads.workload_inputs(w, device="cuda", T_override=T_override)
     q, k, v, g, b = d["queries"], d["keys"], d["values"], d["decays"], d["beta"]
     s0 = d["initial_state"]
@@ -185,20 +187,27 @@ def bench_prefill(gdn, w, iters, warmup, states=False, T_override=None):
     fin = torch.empty(N, HV, D, D, dtype=torch.float32, device=dev)
     st = torch.empty(*v.shape[:-1], D, D, dtype=torch.float32, device=dev) if states else None
     ws = torch.empty(gdn.workspace_size(T_total, N, HV, D, D), dtype=torch.uint8, device=dev)
+    gk = {}
+    if gated:
+        gen = torch.Generator(device="cuda").manual_seed(7)
+        gk = dict(gate=torch.randn(v.shape, generator=gen, device=dev).to(v.dtype),
+                  norm_weight=1.0 + 0.3 * torch.randn(D, generator=gen, device=dev))
     if w.n_seqs:
         fn = lambda: gdn.prefill_varlen(q, k, v, g, b, cu, s0, out=out, final_state=fin,
-                                        states=st, workspace=ws)
+                                        states=st, workspace=ws, **gk)
     else:
         fn = lambda: gdn.prefill(q, k, v, g, b, s0, out=out, final_state=fin, states=st,
-                                 workspace=ws)
+                                 workspace=ws, **gk)
     times = Timer(flush=True).run(fn, iters, warmup)
     elt = q.element_size()
     nbytes = prefill_bytes(T_total, w.HK, HV, D, elt, N if s0 is not None else 0, N,
                            T_total if states else 0)
+    if gated:
+        nbytes += T_total * HV * D * elt + D * 4             # the gate z and the gain
     flops = prefill_flops(T_total, HV, D)
     res = dict(tokens=T_total, ms=statistics.mean(times), ms_min=min(times), bytes=nbytes,
                flops=flops, launches_per_call=(3 if w.n_seqs else 2))
-    del q, k, v, g, b, s0, out, fin, st, ws, d
+    del q, k, v, g, b, s0, out, fin, st, ws, d, gk
     torch.cuda.empty_cache()
     return res
 
@@ -519,6 +528,13 @@ def main():
             roofline={"bound": "hbm", "achieved": dg["bytes"] / (dg["ms"] * 1e-3) / 1e9, "peak": hbm,
                       "unit": "GB/s", "frac": dg["bytes"] / (dg["ms"] * 1e-3) / 1e9 / hbm,
                       "algorithmic_bytes": dg["bytes"]})
+        r = bench_prefill(gdn, head_w, max(3, min(args.steps, 20)), 3, gated=True)
+        subs["prefill_gated_norm"] = dict(
+            workload=head_w.name + " followed by the gated RMS norm (gdn_prefill_gated)",
+            tokens=r["tokens"], ms=r["ms"], tokens_per_s=r["tokens"] / (r["ms"] * 1e-3),
+            roofline={"bound": "hbm", "achieved": r["bytes"] / (r["ms"] * 1e-3) / 1e9, "peak": hbm,
+                      "unit": "GB/s", "frac": r["bytes"] / (r["ms"] * 1e-3) / 1e9 / hbm,
+                      "algorithmic_bytes": r["bytes"]})
         pr = bench_prologue(gdn, head_w, max(args.steps, 20), args.warmup)
         subs["prologue"] = dict(
             workload="conv + gates from the fused projections of 4 next_prefill_T4096_hk16_hv32_d128 "

@@ -74,6 +74,12 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_prefill_varlen.restype = i
     lib.gdn_prefill_varlen.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, vp, i, i, i, i, i, i,
                                        i, f, i, vp, sz, vp]
+    lib.gdn_prefill_gated.restype = i
+    lib.gdn_prefill_gated.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, vp, fp, f, i, i, i, i,
+                                      i, i, i, f, i, vp, sz, vp]
+    lib.gdn_prefill_varlen_gated.restype = i
+    lib.gdn_prefill_varlen_gated.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, vp, fp, f, vp, i,
+                                             i, i, i, i, i, i, f, i, vp, sz, vp]
     lib.gdn_decode_step.restype = i
     lib.gdn_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, i, f, i, vp]
     lib.gdn_decode_step_gated.restype = i
@@ -167,6 +173,17 @@ def selftest_wait_timeout(limit_ns, device=None, stream=None):
     return int(s[0]), int(s[1])
 
 
+def _gated(gate, norm_weight, dtype, device, shape):
+    """Checks the gated-norm arguments; True when they are given."""
+    if (gate is None) != (norm_weight is None):
+        raise ValueError("gate and norm_weight go together")
+    if gate is None:
+        return False
+    _need(gate, "gate", dtype, device, shape)
+    _need(norm_weight, "norm_weight", torch.float32, device, (shape[-1],))
+    return True
+
+
 def _workspace(workspace, nbytes, device):
     if workspace is None:
         return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
@@ -178,11 +195,14 @@ def _workspace(workspace, nbytes, device):
 
 def prefill(queries, keys, values, decays, beta, initial_state=None, *, scale=None,
             use_qk_l2norm=True, output_states=False, out=None, final_state=None, states=None,
-            workspace=None, stream=None):
+            workspace=None, gate=None, norm_weight=None, norm_eps=1e-6, stream=None):
     """Chunked prefill over a batch of equal-length sequences (gdn_prefill).
 
     Returns ``(out, final_state, states)``; ``states`` is None unless
-    ``output_states`` is set or a ``states`` tensor is passed.
+    ``output_states`` is set or a ``states`` tensor is passed.  With ``gate``
+    ([B, T, HV, Dv], dtype of the values) and ``norm_weight`` ([Dv] float32) the gated
+    RMS norm is formed in the same pass (gdn_prefill_gated): out is then
+    norm(y, gate=silu(gate)) * norm_weight.
     """
     _need(queries, "queries")
     dev, dt = queries.device, queries.dtype
@@ -209,6 +229,14 @@ def prefill(queries, keys, values, decays, beta, initial_state=None, *, scale=No
     lib = load_library()
     nbytes = lib.gdn_prefill_workspace_size(B * T, B, HV, Dk, Dv)
     ws = _workspace(workspace, nbytes, dev)
+    if _gated(gate, norm_weight, dt, dev, (B, T, HV, Dv)):
+        rc = lib.gdn_prefill_gated(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays),
+                                   _ptr(beta), _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                   _ptr(states), _ptr(gate), _ptr(norm_weight), float(norm_eps),
+                                   B, T, HK, HV, Dk, Dv, _DTYPES[dt], float(scale or 0.0),
+                                   int(bool(use_qk_l2norm)), _ptr(ws), ws.numel(), _stream(stream))
+        _check(rc, "gdn_prefill_gated")
+        return out, final_state, states
     rc = lib.gdn_prefill(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays), _ptr(beta),
                          _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(states),
                          B, T, HK, HV, Dk, Dv, _DTYPES[dt], float(scale or 0.0),
@@ -219,13 +247,15 @@ def prefill(queries, keys, values, decays, beta, initial_state=None, *, scale=No
 
 def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_state=None, *,
                    scale=None, use_qk_l2norm=True, output_states=False, out=None,
-                   final_state=None, states=None, workspace=None, stream=None):
+                   final_state=None, states=None, workspace=None, gate=None, norm_weight=None,
+                   norm_eps=1e-6, stream=None):
     """Chunked prefill over sequences packed back to back (gdn_prefill_varlen).
 
     queries/keys [1, T_total, HK, Dk] (or [T_total, HK, Dk]), values [.., T_total, HV, Dv],
     decays/beta [.., T_total, HV], ``cu_seqlens`` int32 [N+1] on the device,
     initial_state [N, HV, Dk, Dv] or None.  Returns ``(out, final_state [N, HV, Dk, Dv],
-    states)``; out and states keep the leading shape of ``values``.
+    states)``; out and states keep the leading shape of ``values``.  ``gate`` and
+    ``norm_weight`` as in :func:`prefill` (gdn_prefill_varlen_gated).
     """
     _need(queries, "queries")
     dev, dt = queries.device, queries.dtype
@@ -258,6 +288,15 @@ def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_stat
     lib = load_library()
     nbytes = lib.gdn_prefill_workspace_size(T_total, N, HV, Dk, Dv)
     ws = _workspace(workspace, nbytes, dev)
+    if _gated(gate, norm_weight, dt, dev, tuple(values.shape)):
+        rc = lib.gdn_prefill_varlen_gated(
+            _ptr(queries), _ptr(keys), _ptr(values), _ptr(decays), _ptr(beta),
+            _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(states), _ptr(gate),
+            _ptr(norm_weight), float(norm_eps), _ptr(cu_seqlens), N, T_total, HK, HV, Dk, Dv,
+            _DTYPES[dt], float(scale or 0.0), int(bool(use_qk_l2norm)), _ptr(ws), ws.numel(),
+            _stream(stream))
+        _check(rc, "gdn_prefill_varlen_gated")
+        return out, final_state, states
     rc = lib.gdn_prefill_varlen(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays),
                                 _ptr(beta), _ptr(initial_state), _ptr(out), _ptr(final_state),
                                 _ptr(states), _ptr(cu_seqlens), N, T_total, HK, HV, Dk, Dv,

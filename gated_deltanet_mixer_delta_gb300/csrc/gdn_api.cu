@@ -53,10 +53,12 @@ int prefill_common(const void *queries, const void *keys, const void *values,
                    void *out, float *final_state, float *states, const int32_t *cu_seqlens,
                    int N, int T_seq, int64_t T_total, int HK, int HV, int Dk, int Dv,
                    gdn_dtype dtype, float scale, int use_qk_l2norm, void *workspace,
-                   size_t workspace_bytes, void *cuda_stream) {
+                   size_t workspace_bytes, void *cuda_stream, const void *gate_z = nullptr,
+                   const float *norm_weight = nullptr, float norm_eps = 0.f) {
     int rc = check_common(HK, HV, Dk, Dv, dtype, scale);
     if (rc != GDN_OK) return rc;
     if (N < 0 || T_total < 0 || T_seq < 0) return GDN_ERR_INVALID_ARG;
+    if (gate_z && T_total > 0 && !norm_weight) return GDN_ERR_INVALID_ARG;
     if (T_total > INT32_MAX || N > 65535 || HV > 65535) return GDN_ERR_UNSUPPORTED;
     if (N > 0 && !final_state) return GDN_ERR_INVALID_ARG;
     if (T_total > 0 && (!queries || !keys || !values || !decays || !beta || !out))
@@ -64,7 +66,7 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     if (cu_seqlens == nullptr && N > 0 && T_seq > 0 && (int64_t)N * T_seq != T_total)
         return GDN_ERR_INVALID_ARG;
     const void *ptrs[] = {queries, keys, values, decays, beta, initial_state, out,
-                          final_state, states, cu_seqlens};
+                          final_state, states, cu_seqlens, gate_z, norm_weight};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
     // final_state may be initial_state (in place); no other overlap is checked here
@@ -101,6 +103,9 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     }
     cudaError_t e = tc_supported(Dk, Dv, dtype) ? launch_prefill_tc(p, st)
                                                 : launch_prefill_generic(p, dtype, st);
+    // the gated norm runs over the outputs in place, on the same stream
+    if (e == cudaSuccess && gate_z && T_total > 0)
+        e = launch_gated_norm(out, gate_z, norm_weight, out, T_total * HV, Dv, dtype, norm_eps, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -151,6 +156,36 @@ static int decode_common(const void *queries, const void *keys, const void *valu
                                   Dv, dtype, resolve_scale(scale, Dk), use_qk_l2norm ? 1 : 0,
                                   gate_z, norm_weight, norm_eps, (cudaStream_t)cuda_stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_prefill_gated(const void *queries, const void *keys, const void *values,
+                      const float *decays, const float *beta, const float *initial_state,
+                      void *out, float *final_state, float *states, const void *gate_z,
+                      const float *norm_weight, float norm_eps, int B, int T, int HK, int HV,
+                      int Dk, int Dv, gdn_dtype dtype, float scale, int use_qk_l2norm,
+                      void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    if (B < 0 || T < 0) return GDN_ERR_INVALID_ARG;
+    if (!gate_z || !norm_weight || !(norm_eps >= 0.f) || isinf(norm_eps)) return GDN_ERR_INVALID_ARG;
+    return prefill_common(queries, keys, values, decays, beta, initial_state, out, final_state,
+                          states, nullptr, B, T, (int64_t)B * T, HK, HV, Dk, Dv, dtype, scale,
+                          use_qk_l2norm, workspace, workspace_bytes, cuda_stream, gate_z,
+                          norm_weight, norm_eps);
+}
+
+int gdn_prefill_varlen_gated(const void *queries, const void *keys, const void *values,
+                             const float *decays, const float *beta, const float *initial_state,
+                             void *out, float *final_state, float *states, const void *gate_z,
+                             const float *norm_weight, float norm_eps,
+                             const int32_t *cu_seqlens, int N, int T_total, int HK, int HV,
+                             int Dk, int Dv, gdn_dtype dtype, float scale, int use_qk_l2norm,
+                             void *workspace, size_t workspace_bytes, void *cuda_stream) {
+    if (N < 0 || T_total < 0) return GDN_ERR_INVALID_ARG;
+    if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (!gate_z || !norm_weight || !(norm_eps >= 0.f) || isinf(norm_eps)) return GDN_ERR_INVALID_ARG;
+    return prefill_common(queries, keys, values, decays, beta, initial_state, out, final_state,
+                          states, cu_seqlens, N, 0, T_total, HK, HV, Dk, Dv, dtype, scale,
+                          use_qk_l2norm, workspace, workspace_bytes, cuda_stream, gate_z,
+                          norm_weight, norm_eps);
 }
 
 int gdn_decode_step(const void *queries, const void *keys, const void *values,

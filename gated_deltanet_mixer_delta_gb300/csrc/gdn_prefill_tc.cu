@@ -971,15 +971,24 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             tmem_ld32(tmem + lb + TM_QS + 64, o3);
             tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < NV; ++q) o1[q] += o2[q] + o3[q];
+            for (int q = 0; q < NV; q += 2) {               // pairs: one instruction for two
+                const uint64_t r = fadd2(f2pack(o1[q], o1[q + 1]), fadd2(f2pack(o2[q], o2[q + 1]),
+                                                                          f2pack(o3[q], o3[q + 1])));
+                f2unpack(r, o1[q], o1[q + 1]);
+            }
             tmem_ld32(tmem + lb + TM_QS + 96, o2);
             tmem_ld32(tmem + lb + TM_PU, o3);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_OUT]);
+            const uint64_t qd2 = f2pack(qd, qd);
 #pragma unroll
-            for (int q = 0; q < NV; ++q) o1[q] = qd * (o1[q] + o2[q]) + o3[q];
+            for (int q = 0; q < NV; q += 2) {
+                const uint64_t r = ffma2(qd2, fadd2(f2pack(o1[q], o1[q + 1]), f2pack(o2[q], o2[q + 1])),
+                                         f2pack(o3[q], o3[q + 1]));
+                f2unpack(r, o1[q], o1[q + 1]);
+            }
             const int64_t tok = sr.t0 + (int64_t)cc * C + t;
             if (tok < sr.t_end) {
                 __nv_bfloat16 *dst = p.out + ((size_t)tok * p.HV + h) * D + (size_t)vs * NV;

@@ -120,47 +120,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// packed fp32 pairs: one instruction for two lanes of arithmetic
-__device__ __forceinline__ uint64_t f2pack(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t r, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-// silu of a pair: x / (1 + e^{-x}) with the MUFU exponential and reciprocal
-__device__ __forceinline__ uint64_t silu2(uint64_t x) {
-    const uint64_t t = fmul2(x, f2pack(-1.4426950408889634f, -1.4426950408889634f));
-    float t0, t1;
-    f2unpack(t, t0, t1);
-    float e0, e1;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
-    const uint64_t d = fadd2(f2pack(e0, e1), f2pack(1.f, 1.f));
-    float d0, d1;
-    f2unpack(d, d0, d1);
-    float r0, r1;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d0));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d1));
-    return fmul2(x, f2pack(r0, r1));
-}
-
 __device__ __forceinline__ int64_t seq_start(const ProParams &p, int s) {
     return p.cu ? (int64_t)p.cu[s] : (int64_t)s * p.T_seq;
 }

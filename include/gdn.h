@@ -138,6 +138,34 @@ int gdn_prefill_varlen(const void *queries, const void *keys, const void *values
                        void *workspace, size_t workspace_bytes, void *cuda_stream);
 
 /*
+ * gdn_prefill / gdn_prefill_varlen followed by the gated RMS norm of the mixer output
+ * (see gdn_gated_rmsnorm below for the definition), in one call on one stream: `out`
+ * receives norm(y, gate=silu(gate_z)) * norm_weight.  The norm kernel runs over the
+ * prefill's output in place (the faster of the designs measured: forming the norm inside
+ * the prefill's sequential kernel made that kernel's output warps its bottleneck).
+ *   gate_z       [B, T, HV, Dv] (packed: [1, T_total, HV, Dv]) dtype of values
+ *   norm_weight  [Dv] float32;  norm_eps finite and >= 0
+ * Everything else (arguments, states, workspace, errors) as gdn_prefill /
+ * gdn_prefill_varlen; gate_z or norm_weight NULL, or a bad norm_eps, is
+ * GDN_ERR_INVALID_ARG.
+ */
+int gdn_prefill_gated(const void *queries, const void *keys, const void *values,
+                      const float *decays, const float *beta, const float *initial_state,
+                      void *out, float *final_state, float *states,
+                      const void *gate_z, const float *norm_weight, float norm_eps,
+                      int B, int T, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
+                      float scale, int use_qk_l2norm,
+                      void *workspace, size_t workspace_bytes, void *cuda_stream);
+int gdn_prefill_varlen_gated(const void *queries, const void *keys, const void *values,
+                             const float *decays, const float *beta,
+                             const float *initial_state, void *out, float *final_state,
+                             float *states, const void *gate_z, const float *norm_weight,
+                             float norm_eps, const int32_t *cu_seqlens, int N, int T_total,
+                             int HK, int HV, int Dk, int Dv, gdn_dtype dtype, float scale,
+                             int use_qk_l2norm, void *workspace, size_t workspace_bytes,
+                             void *cuda_stream);
+
+/*
  * One decode step ("a decode step's recurrent one", linear_attn value
  * table): one token per sequence, continuing the cache's state in place.
  *

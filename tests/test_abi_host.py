@@ -209,3 +209,23 @@ def _prologue(lib, **kw):
 ])
 def test_prologue_rejects_bad_arguments_on_host(lib, kw, code):
     assert _prologue(lib, **kw) == code
+
+
+def test_gated_prefill_rejects_bad_arguments_on_host(lib):
+    f = lib.gdn_prefill_gated
+    base = [P, P, P, P, P, None, P, P, None, P, P, 1e-6, 1, 64, 2, 4, 128, 128, 0, 0.0, 1, P, BIG,
+            None]
+    a = list(base); a[9] = None
+    assert f(*a) == -1                           # gate required
+    a = list(base); a[10] = None
+    assert f(*a) == -1                           # weight required
+    a = list(base); a[11] = -1.0
+    assert f(*a) == -1
+    a = list(base); a[9] = P + 4
+    assert f(*a) == -3
+    g = lib.gdn_prefill_varlen_gated
+    vbase = [P, P, P, P, P, None, P, P, None, P, P, 1e-6, None, 2, 100, 2, 4, 128, 128, 0, 0.0, 1,
+             P, BIG, None]
+    assert g(*vbase) == -1                       # cu_seqlens required
+    a = list(vbase); a[12] = P; a[10] = P + 8
+    assert g(*a) == -3

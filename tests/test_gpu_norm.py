@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import workloads
-from parity import assert_states_close
+from parity import assert_states_close, oracle_chains
 
 pytestmark = pytest.mark.gpu
 import oracle  # noqa: E402
@@ -109,3 +109,87 @@ def test_fused_decode_norm_matches_oracle(gdn, D, dtype):
     _assert_close(out, ref, RTOL[dtype], extra=1e-3 * gate)
     assert torch.equal(st_gated, st_plain)              # the norm leaves the state step alone
     assert_states_close(st_gated, s_ref, "state")
+
+
+def _norm_bound(y_ref, z, wt, rtol, ytol):
+    """Per element: rtol |ref| plus the rule's output bound ytol on y carried through the
+    norm (|weight silu(z)| ytol / rms(y))."""
+    zz = z.double().cpu().numpy() if hasattr(z, "cpu") else z
+    gate = np.abs(wt.double().cpu().numpy() * zz / (1 + np.exp(-zz)))
+    rms = np.sqrt((y_ref ** 2).mean(-1, keepdims=True))
+    return ytol * gate / np.maximum(rms, 1e-3)
+
+
+@pytest.mark.parametrize("D,dtype", [(128, torch.bfloat16), (32, torch.float32)])
+def test_fused_prefill_norm_matches_oracle(gdn, D, dtype):
+    """gdn_prefill_gated (the prefill, then the norm over its output in place) on the
+    tensor-core and the CUDA-core shapes, against the oracle's norm of the oracle's y; the
+    final state is the ungated prefill's, bit for bit."""
+    B, T, HK, HV = 2, 130, 2, 4
+    d = workloads.draw_inputs(B, T, HK, HV, D, D, dtype, seed=61 + D, init_state_std=0.02)
+    g = torch.Generator().manual_seed(62)
+    z = (torch.randn(B, T, HV, D, generator=g) * 2.0).to(dtype)
+    wt = 1.0 + 0.3 * torch.randn(D, generator=g)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    args = [c[k] for k in ("queries", "keys", "values", "decays", "beta")]
+    out, fin, _ = gdn.prefill(*args, c["initial_state"], gate=z.cuda(), norm_weight=wt.cuda())
+    y, fin0, _ = gdn.prefill(*args, c["initial_state"])
+    torch.cuda.synchronize()
+    assert torch.equal(fin, fin0)
+    y_ref, _, _ = oracle.forward(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                                 d["initial_state"])
+    ref = oracle.gated_rmsnorm(y_ref, z, wt)
+    ytol = 2e-2 if dtype == torch.bfloat16 else 1e-4
+    _assert_close(out, ref, RTOL[dtype], extra=_norm_bound(y_ref, z, wt, RTOL[dtype], ytol))
+
+
+def test_fused_prefill_norm_packed_sequences(gdn):
+    """gdn_prefill_varlen_gated over packed sequences (one shorter than a chunk, one
+    ragged over three chunks, one empty) with initial states, against the oracle."""
+    lens = [10, 0, 150, 64]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    d = workloads.draw_inputs(1, T, 2, 4, 128, 128, torch.bfloat16, 63, init_state_std=0.02,
+                              n_states=len(lens))
+    g = torch.Generator().manual_seed(64)
+    z = torch.randn(1, T, 4, 128, generator=g).to(torch.bfloat16)
+    wt = 1.0 + 0.3 * torch.randn(128, generator=g)
+    c = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    cu_d = torch.from_numpy(cu).cuda()
+    out, fin, _ = gdn.prefill_varlen(c["queries"], c["keys"], c["values"], c["decays"], c["beta"],
+                                     cu_d, c["initial_state"], gate=z.cuda(), norm_weight=wt.cuda())
+    _, fin0, _ = gdn.prefill_varlen(c["queries"], c["keys"], c["values"], c["decays"], c["beta"],
+                                    cu_d, c["initial_state"])
+    torch.cuda.synchronize()
+    assert torch.equal(fin, fin0)
+    y_ref, _, _ = oracle.forward(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                                 d["initial_state"], cu_seqlens=cu)
+    ref = oracle.gated_rmsnorm(y_ref, z, wt)
+    _assert_close(out, ref, RTOL[torch.bfloat16],
+                  extra=_norm_bound(y_ref, z, wt, RTOL[torch.bfloat16], 2e-2))
+
+
+def test_fused_prefill_norm_at_qwen3_next_shape(gdn):
+    """The headline-shaped prompt (4096 tokens, 16/32 heads) through gdn_prefill_gated:
+    sampled value heads against the oracle, and every head bit for bit against the two
+    calls it stands for (prefill, then the norm kernel)."""
+    w = workloads.WORKLOADS["next_prefill_T4096_hk16_hv32_d128"]
+    d = workloads.workload_inputs(w, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(65)
+    z = torch.randn(1, w.T, w.HV, 128, generator=g, device="cuda").to(torch.bfloat16)
+    wt = 1.0 + 0.3 * torch.randn(128, generator=g, device="cuda")
+    args = [d[k] for k in ("queries", "keys", "values", "decays", "beta")]
+    out, fin, _ = gdn.prefill(*args, gate=z, norm_weight=wt)
+    y, fin0, _ = gdn.prefill(*args)
+    unfused = gdn.gated_rmsnorm(y, z, wt)
+    torch.cuda.synchronize()
+    assert torch.equal(fin, fin0)
+    assert torch.equal(out, unfused)
+    chains = oracle_chains({k: v.cpu() if isinstance(v, torch.Tensor) else v for k, v in d.items()},
+                           [(0, h) for h in (0, 17, 31)])
+    zc = z[0].cpu()
+    for (s, h), (o_r, _, _) in chains.items():
+        ref = oracle.gated_rmsnorm(o_r, zc[:, h], wt.cpu())
+        _assert_close(out[0, :, h], ref, RTOL[torch.bfloat16],
+                      extra=_norm_bound(o_r, zc[:, h], wt, RTOL[torch.bfloat16], 2e-2),
+                      what=f"head {h}")
