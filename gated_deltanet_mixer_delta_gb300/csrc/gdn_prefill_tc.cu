@@ -1074,12 +1074,20 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 tmem_ld32(tmem + lb + TM_W + 32, b);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) uu[c] += a[c] + b[c];
+                for (int c = 0; c < NV; c += 2) {       // pairs: one instruction for two
+                    const uint64_t r = fadd2(f2pack(uu[c], uu[c + 1]),
+                                             fadd2(f2pack(a[c], a[c + 1]), f2pack(b[c], b[c + 1])));
+                    f2unpack(r, uu[c], uu[c + 1]);
+                }
                 tmem_ld32(tmem + lb + TM_W + 64, a);
                 tmem_ld32(tmem + lb + TM_W + 96, c2);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) uu[c] += a[c] + c2[c];
+                for (int c = 0; c < NV; c += 2) {
+                    const uint64_t r = fadd2(f2pack(uu[c], uu[c + 1]),
+                                             fadd2(f2pack(a[c], a[c + 1]), f2pack(c2[c], c2[c + 1])));
+                    f2unpack(r, uu[c], uu[c + 1]);
+                }
             }
             // keep this thread's 16 columns, send the other 16 to the partner row (tk, 1 - hf)
             float u16[16], o16[16];
@@ -1163,7 +1171,11 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 tmem_ld32(tmem + lb + TM_S2 + 32, d4);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) ds[c] += d2[c] + d3[c] + d4[c];
+                for (int c = 0; c < NV; c += 2) {
+                    const uint64_t r = fadd2(fadd2(f2pack(ds[c], ds[c + 1]), f2pack(d2[c], d2[c + 1])),
+                                             fadd2(f2pack(d3[c], d3[c + 1]), f2pack(d4[c], d4[c + 1])));
+                    f2unpack(r, ds[c], ds[c + 1]);
+                }
             }
             if (STATES) {
                 const uint8_t *ktile = sb + kBK + (i >> 6) * 8192;
@@ -1195,7 +1207,10 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 }
             }
 #pragma unroll
-            for (int c = 0; c < NV; ++c) S[c] = gl * S[c] + ds[c];
+            for (int c = 0; c < NV; c += 2) {
+                const uint64_t r = ffma2(f2pack(gl, gl), f2pack(S[c], S[c + 1]), f2pack(ds[c], ds[c + 1]));
+                f2unpack(r, S[c], S[c + 1]);
+            }
             store_row_hilo128(sm + OFF_S, i, S);     // Q S of this chunk is done (QSD above)
             fence_async_smem();
             tc_fence_before();
