@@ -111,7 +111,9 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16 &hi, __nv_bflo
 __device__ __forceinline__ void split2_bf16(float a, float b, uint32_t &hi, uint32_t &lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    float ra, rb;                                   // (a - hi, b - hi) in one instruction
+    f2unpack(ffma2(f2pack(-1.f, -1.f), f2pack(hf.x, hf.y), f2pack(a, b)), ra, rb);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(ra, rb);
     hi = *reinterpret_cast<const uint32_t *>(&h);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
@@ -1109,10 +1111,10 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float4 x4 = *reinterpret_cast<const float4 *>(src + xchg_off(tk, c));
-                    u16[4 * c] += x4.x;
-                    u16[4 * c + 1] += x4.y;
-                    u16[4 * c + 2] += x4.z;
-                    u16[4 * c + 3] += x4.w;
+                    const uint64_t r0 = fadd2(f2pack(u16[4 * c], u16[4 * c + 1]), f2pack(x4.x, x4.y));
+                    const uint64_t r1 = fadd2(f2pack(u16[4 * c + 2], u16[4 * c + 3]), f2pack(x4.z, x4.w));
+                    f2unpack(r0, u16[4 * c], u16[4 * c + 1]);
+                    f2unpack(r1, u16[4 * c + 2], u16[4 * c + 3]);
                 }
             }
             // columns 16 hf .. 16 hf + 15 of token tk: Z_hi, Z_lo (chunks 2 hf, 2 hf + 1 of
@@ -1123,7 +1125,9 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = 8 * q + 2 * e;
-                    split2_bf16(kd * u16[c], kd * u16[c + 1], zh[e], zl[e]);
+                    float z0, z1;
+                    f2unpack(fmul2(f2pack(kd, kd), f2pack(u16[c], u16[c + 1])), z0, z1);
+                    split2_bf16(z0, z1, zh[e], zl[e]);
                     const __nv_bfloat162 u2v = __floats2bfloat162_rn(u16[c], u16[c + 1]);
                     uh[e] = *reinterpret_cast<const uint32_t *>(&u2v);
                 }
