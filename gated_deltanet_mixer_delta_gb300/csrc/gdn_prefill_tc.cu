@@ -226,9 +226,9 @@ __device__ __forceinline__ void tmem_row_split(uint32_t taddr, float (&x)[32]) {
 // block is read by solve_tile and replaced by apply_tile; a barrier separates the two.
 template <int N, int RT>
 __device__ __forceinline__ void solve_tile(const float *sAT, float *sX, int r0, int c0, int tr, int tc) {
-    float acc[RT][4];
+    uint64_t acc[RT][2];                                // column pairs (0, 1), (2, 3)
 #pragma unroll
-    for (int a = 0; a < RT; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+    for (int a = 0; a < RT; ++a) acc[a][0] = acc[a][1] = 0;
 #pragma unroll
     for (int m4 = 0; m4 < N; m4 += 4) {
         float4 a4[RT];
@@ -237,23 +237,29 @@ __device__ __forceinline__ void solve_tile(const float *sAT, float *sX, int r0, 
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
             const float4 t4 = lds4(sAT + (c0 + m4 + mm) * LDA + c0 + 4 * tc);
+            const uint64_t t01 = f2pack(t4.x, t4.y), t23 = f2pack(t4.z, t4.w);
 #pragma unroll
             for (int a = 0; a < RT; ++a) {
                 const float av = f4get(a4[a], mm);
-                acc[a][0] += av * t4.x; acc[a][1] += av * t4.y;
-                acc[a][2] += av * t4.z; acc[a][3] += av * t4.w;
+                const uint64_t aa = f2pack(av, av);
+                acc[a][0] = ffma2(aa, t01, acc[a][0]);
+                acc[a][1] = ffma2(aa, t23, acc[a][1]);
             }
         }
     }
 #pragma unroll
-    for (int a = 0; a < RT; ++a)
-        sts4(sX + (tr + 8 * a) * LDX + 4 * tc, acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    for (int a = 0; a < RT; ++a) {
+        float x0, x1, x2, x3;
+        f2unpack(acc[a][0], x0, x1);
+        f2unpack(acc[a][1], x2, x3);
+        sts4(sX + (tr + 8 * a) * LDX + 4 * tc, x0, x1, x2, x3);
+    }
 }
 template <int N, int RT>
 __device__ __forceinline__ void apply_tile(float *sAT, const float *sX, int r0, int c0, int tr, int tc) {
-    float acc[RT][4];
+    uint64_t acc[RT][2];                                // column pairs (0, 1), (2, 3)
 #pragma unroll
-    for (int a = 0; a < RT; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+    for (int a = 0; a < RT; ++a) acc[a][0] = acc[a][1] = 0;
 #pragma unroll
     for (int m4 = 0; m4 < N; m4 += 4) {
         float4 t4[RT];
@@ -262,17 +268,23 @@ __device__ __forceinline__ void apply_tile(float *sAT, const float *sX, int r0, 
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
             const float4 x4 = lds4(sX + (m4 + mm) * LDX + 4 * tc);
+            const uint64_t x01 = f2pack(x4.x, x4.y), x23 = f2pack(x4.z, x4.w);
 #pragma unroll
             for (int a = 0; a < RT; ++a) {
                 const float tv = f4get(t4[a], mm);
-                acc[a][0] += tv * x4.x; acc[a][1] += tv * x4.y;
-                acc[a][2] += tv * x4.z; acc[a][3] += tv * x4.w;
+                const uint64_t tt = f2pack(tv, tv);
+                acc[a][0] = ffma2(tt, x01, acc[a][0]);
+                acc[a][1] = ffma2(tt, x23, acc[a][1]);
             }
         }
     }
 #pragma unroll
-    for (int a = 0; a < RT; ++a)
-        sts4(sAT + (r0 + tr + 8 * a) * LDA + c0 + 4 * tc, -acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
+    for (int a = 0; a < RT; ++a) {
+        float x0, x1, x2, x3;
+        f2unpack(acc[a][0], x0, x1);
+        f2unpack(acc[a][1], x2, x3);
+        sts4(sAT + (r0 + tr + 8 * a) * LDA + c0 + 4 * tc, -x0, -x1, -x2, -x3);
+    }
 }
 
 // x (32 columns of a row of T) times diag(col) as hi/lo images (row t, chunks 4 half ..)
@@ -282,7 +294,8 @@ __device__ __forceinline__ void store_scaled_row(const float (&tv)[32], const fl
 #pragma unroll
     for (int q = 0; q < 32; q += 4) {
         const float4 c4 = lds4(col + half * 32 + q);
-        x[q] = tv[q] * c4.x; x[q + 1] = tv[q + 1] * c4.y; x[q + 2] = tv[q + 2] * c4.z; x[q + 3] = tv[q + 3] * c4.w;
+        f2unpack(fmul2(f2pack(tv[q], tv[q + 1]), f2pack(c4.x, c4.y)), x[q], x[q + 1]);
+        f2unpack(fmul2(f2pack(tv[q + 2], tv[q + 3]), f2pack(c4.z, c4.w)), x[q + 2], x[q + 3]);
     }
     store_half_row_hilo(img_hi, img_lo, t, half * 4, x);
 }
