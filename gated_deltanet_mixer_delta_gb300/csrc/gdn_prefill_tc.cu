@@ -489,16 +489,25 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
             const float *G2 = vG2(i);
             const float G2t = G2[trow], at = vB(i)[trow] * rkt;
             float av[32], pv[32];
+            const uint64_t G2t2 = f2pack(G2t, G2t), at2 = f2pack(at, at), pt2 = f2pack(pt, pt);
 #pragma unroll
             for (int q4 = 0; q4 < 32; q4 += 4) {
                 const float4 g4 = lds4(G2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
                 const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
+                for (int qq = 0; qq < 4; qq += 2) {             // column pairs
                     const int q = q4 + qq, jj = tcb * 32 + q;
-                    const float e = (jj <= trow && jj < len) ? ex2_fast(G2t - gv[qq]) * rv[qq] : 0.f;
-                    av[q] = (live && jj < trow) ? at * e * gr[q] : 0.f;
-                    pv[q] = pt * e * qk[q];
+                    float d0, d1;                               // G_t - G_j (log2 units)
+                    f2unpack(ffma2(f2pack(-1.f, -1.f), f2pack(gv[qq], gv[qq + 1]), G2t2), d0, d1);
+                    // the exponent is selected before any product (past t it may be inf)
+                    const float e0 = (jj <= trow && jj < len) ? ex2_fast(d0) : 0.f;
+                    const float e1 = (jj + 1 <= trow && jj + 1 < len) ? ex2_fast(d1) : 0.f;
+                    const uint64_t e2 = fmul2(f2pack(e0, e1), f2pack(rv[qq], rv[qq + 1]));
+                    float a0, a1;
+                    f2unpack(fmul2(fmul2(at2, e2), f2pack(gr[q], gr[q + 1])), a0, a1);
+                    av[q] = (live && jj < trow) ? a0 : 0.f;
+                    av[q + 1] = (live && jj + 1 < trow) ? a1 : 0.f;
+                    f2unpack(fmul2(fmul2(pt2, e2), f2pack(qk[q], qk[q + 1])), pv[q], pv[q + 1]);
                 }
             }
             float *sA = sAT + i * C * LDA;
