@@ -930,7 +930,10 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             for (int cc = 0; cc < nch; ++cc) {
                 // P U_hi (outputs only: one bf16 term) once U is formed and the output
                 // warps have read the previous chunk's
-                if (!wait(B_E1DONE, cc & 1) || (cc >= 1 && !wait(B_OUT, (cc - 1) & 1))) break;
+                // polled without parking: the tensor pipe runs in order, and P U issued late
+                // would sit in front of the next chunk's -W S
+                if (*s_err || !mbar_wait_spin(&bars[B_E1DONE], cc & 1)) { fail(); break; }
+                if (cc >= 1 && !wait(B_OUT, (cc - 1) & 1)) break;
                 issued = true;
                 tc_fence_after();
                 {

@@ -62,6 +62,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of a phase (the thread is never parked).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete; gives up after `limit_ns`
 // and returns false (the caller records a timeout and stops waiting).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
@@ -71,6 +83,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     while (!mbar_try_wait_sleep(bar, parity, 20000u))
         if (globaltimer_ns() - t0 > limit_ns) return false;
     return true;
+}
+
+// The same for a phase expected within a few thousand cycles: polls without parking the
+// thread (waking a parked thread costs hundreds of cycles) for up to `spins` tests first.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, int spins = 4096) {
+    for (int i = 0; i < spins; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait(bar, parity);
 }
 
 // ---------------------------------------------------------------- TMA / bulk copies
