@@ -206,7 +206,7 @@ def bench_prefill(gdn, w, iters, warmup, states=False, T_override=None, gated=Fa
         nbytes += T_total * HV * D * elt + D * 4             # the gate z and the gain
     flops = prefill_flops(T_total, HV, D)
     res = dict(tokens=T_total, ms=statistics.mean(times), ms_min=min(times), bytes=nbytes,
-               flops=flops, launches_per_call=(3 if w.n_seqs else 2))
+               flops=flops, launches_per_call=(3 if w.n_seqs else 2) + (2 if states else 0))
     del q, k, v, g, b, s0, out, fin, st, ws, d, gk
     torch.cuda.empty_cache()
     return res
@@ -464,8 +464,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline and decode only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
-                    help="comma list of prologue, gated_norm, decode_gated_norm: time just those "
-                         "steps and print one line each (profiling; not the bench line)")
+                    help="comma list of prologue, gated_norm, decode_gated_norm, states: time just "
+                         "those steps and print one line each (profiling; not the bench line)")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="override the headline prefill length (profiling a case larger than L2)")
     args = ap.parse_args()
@@ -490,7 +490,9 @@ def main():
         runs = {"prologue": lambda: bench_prologue(gdn, head_w, args.steps, args.warmup),
                 "gated_norm": lambda: bench_gated_norm(gdn, head_w, args.steps, args.warmup),
                 "decode_gated_norm": lambda: bench_decode_gated(gdn, W["decode_B256_hk16_hv32_d128"],
-                                                                args.steps, args.warmup)}
+                                                                args.steps, args.warmup),
+                "states": lambda: bench_prefill(gdn, W["states_B4_T1024_hk16_hv32_d128"], args.steps,
+                                                args.warmup, states=True)}
         for name in args.only.split(","):
             r = runs[name]()
             if rank == 0:

@@ -22,10 +22,13 @@
 //           chunk loop, warp-specialised (256 threads): a TMA producer warp, a warp that
 //           issues the products off the chain's critical path, two output warps, and an
 //           epilogue warpgroup that holds the fp32 state slice in registers (thread i =
-//           key row i), forms U, Z = kd U and the new state (and the per-token states
-//           when asked), and issues the products on the critical path itself.  Hi/lo
-//           operand pairs are stacked along M or N so that one instruction covers several
-//           terms.
+//           key row i), forms U, Z = kd U and the new state, and issues the products
+//           on the critical path itself.  Hi/lo operand pairs are stacked along M or N so
+//           that one instruction covers several terms.
+//  states -- only when per-token states are asked for: the chain leaves each chunk's U
+//           rows and its carried state in the states tensor, and one CTA per (chunk,
+//           value head, value slice), all independent, replays the recurrence over the
+//           chunk's tokens from there (then a small kernel copies the final states).
 // All waits are bounded; a timeout sets GDN_ERR_TIMEOUT in the status word and the CTA
 // drains and exits.
 #include <string.h>
@@ -58,6 +61,7 @@ constexpr int kRecBytes = REC_F + 8 * C * 4;                // 58 KiB
 enum { SC_QD = 0, SC_KD, SC_RK, SC_ALPHA, SC_MISC };
 
 struct Params {
+    const __nv_bfloat16 *k;      // keys [T_total][HK][128] (read by the states kernel)
     const float *g, *beta, *s0;
     __nv_bfloat16 *out;
     float *s_final, *states;
@@ -710,8 +714,7 @@ constexpr int OFF_S = OFF_B + 2 * kStageB;                 // [S_hi | S_lo] [128
 constexpr int OFF_Z = OFF_S + 16384;                       // [Z_hi | Z_lo] [64 tokens][128B] MN-major
 constexpr int OFF_U = OFF_Z + 8192;                        // U_hi [64 tokens][64B] MN-major
 constexpr int OFF_X = OFF_U + 4096;                        // fp32 [2][64][16] half-row exchange
-                                                           // (16-byte chunks XOR-swizzled), then
-                                                           // U rows [64][32] for the states
+                                                           // (16-byte chunks XOR-swizzled)
 constexpr int OFF_BAR = OFF_X + C * NV * 4;
 constexpr int kChainSmem = OFF_BAR + 256 + 1024;
 static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0 && kAV % 1024 == 0 && kBQ % 1024 == 0,
@@ -760,13 +763,10 @@ __device__ __forceinline__ bool wg_and(bool v) {
     return r != 0;
 }
 
-// 8 fp32 values to global memory in one 32-byte streaming store (a whole sector);
-// dst must be 32-byte aligned
-__device__ __forceinline__ void st_cs_v8(float *dst, float a0, float a1, float a2, float a3, float a4,
-                                         float a5, float a6, float a7) {
-    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-                 :: "l"(dst), "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
-                 : "memory");
+// 4 fp32 values to global memory in one 16-byte streaming store; dst 16-byte aligned
+__device__ __forceinline__ void st_cs_v4(float *dst, float a0, float a1, float a2, float a3) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(dst), "f"(a0), "f"(a1), "f"(a2), "f"(a3) : "memory");
 }
 
 // 32 fp32 values -> one 128-byte row [hi | lo] of a 128B-swizzled bf16 image
@@ -1161,17 +1161,20 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 *reinterpret_cast<uint4 *>(sm + OFF_Z + sw128_offset(tk, 64 + ch * 16)) = make_uint4(zl[0], zl[1], zl[2], zl[3]);
                 *reinterpret_cast<uint4 *>(sm + OFF_U + sw64_offset(tk, ch * 16)) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
             }
-            if (STATES) {
-                // U rows [64][32] for the per-token states, once every exchange read is done
-                named_sync(1, 128);
+            if (STATES && tk < len - 1) {
+                // U rows 0 .. len-2 of the chunk (fp32, this slice's columns) for the states
+                // kernel, parked in the slot of the chunk's first token: row t at float t * D
+                // (the states kernel reads them before it writes that slot)
+                float *dst = p.states + ((size_t)tok0 * p.HV + h) * (D * D) + (size_t)tk * D +
+                             (size_t)vs * NV + hf * 16;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<float4 *>(xf + tk * NV + hf * 16 + 4 * c) =
+                    *reinterpret_cast<float4 *>(dst + 4 * c) =
                         make_float4(u16[4 * c], u16[4 * c + 1], u16[4 * c + 2], u16[4 * c + 3]);
             }
             fence_async_smem();
             tc_fence_before();
-            named_sync(1, 128);                 // Z, U (and the U rows for the states) complete
+            named_sync(1, 128);                 // Z and U complete
             if (lead) mbar_arrive(&bars[B_E1DONE]);
             if (lane == 0 && (warp == 2 || warp == 3)) {
                 // K^T [Z_hi | Z_lo]: A = key tile read MN-major; k-steps 0-1 / 2-3
@@ -1206,35 +1209,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     f2unpack(r, ds[c], ds[c + 1]);
                 }
             }
-            if (STATES) {
-                const uint8_t *ktile = sb + kBK + (i >> 6) * 8192;
-                const uint32_t kbyte = (uint32_t)(i & 63) * 2;
-                float rs[NV];
-#pragma unroll
-                for (int c = 0; c < NV; ++c) rs[c] = S[c];
-                for (int t = 0; t < len; ++t) {
-                    const float kt = __bfloat162float(
-                        *reinterpret_cast<const __nv_bfloat16 *>(ktile + sw128_offset(t, kbyte)));
-                    const float al = F[SC_ALPHA * C + t], f = F[SC_RK * C + t] * kt;
-                    float *dst = p.states + (((size_t)(tok0 + t) * p.HV + h) * D + i) * D + (size_t)vs * NV;
-                    const bool last = (t == len - 1);
-#pragma unroll
-                    for (int c = 0; c < NV; c += 4) {
-                        const float4 u4 = *reinterpret_cast<const float4 *>(xf + t * NV + c);
-                        rs[c] = al * rs[c] + f * u4.x;
-                        rs[c + 1] = al * rs[c + 1] + f * u4.y;
-                        rs[c + 2] = al * rs[c + 2] + f * u4.z;
-                        rs[c + 3] = al * rs[c + 3] + f * u4.w;
-                    }
-                    // the state after the chunk's last token is the carried chunk-form state
-                    float o[NV];
-#pragma unroll
-                    for (int c = 0; c < NV; ++c) o[c] = last ? gl * S[c] + ds[c] : rs[c];
-#pragma unroll
-                    for (int c = 0; c < NV; c += 8)
-                        st_cs_v8(dst + c, o[c], o[c + 1], o[c + 2], o[c + 3], o[c + 4], o[c + 5], o[c + 6], o[c + 7]);
-                }
-            }
 #pragma unroll
             for (int c = 0; c < NV; c += 2) {
                 const uint64_t r = ffma2(f2pack(gl, gl), f2pack(S[c], S[c + 1]), f2pack(ds[c], ds[c + 1]));
@@ -1250,13 +1224,23 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 issued = true;
             }
             __syncwarp();
+            if (STATES) {
+                // the state after the chunk's last token is the carried chunk-form state
+                float *dst = p.states + ((size_t)(tok0 + len - 1) * p.HV + h) * (D * D) + (size_t)i * D +
+                             (size_t)vs * NV;
+#pragma unroll
+                for (int q = 0; q < NV / 4; ++q)
+                    reinterpret_cast<float4 *>(dst)[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2],
+                                                                     S[4 * q + 3]);
+            }
         }
         if (lane == 0) {
             if (issued) mma_commit(&bars[B_DRAIN]);
             else mbar_arrive(&bars[B_DRAIN]);
         }
-        // final state slice
-        if (!*s_err) {
+        // final state slice (with per-token states, a later kernel copies it from the last
+        // token's state once nothing reads the initial state any more: they may alias)
+        if (!STATES && !*s_err) {
 #pragma unroll
             for (int q = 0; q < NV / 4; ++q)
                 reinterpret_cast<float4 *>(p.s_final + sbase)[q] =
@@ -1268,6 +1252,117 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     __syncthreads();
     if (warp == 4) tmem_dealloc(tmem, kTmemCols);
 }
+// ------------------------------------------------------------------ per-token states
+// One CTA per (chunk, value head, 32-wide value slice), all independent.  It replays the
+// recurrence S_t = alpha_t S_{t-1} + (rk_t k_t) u_t^T over the chunk's tokens but the last
+// one, from the state before the chunk, with the chunk-form U rows: the same u_t as the
+// token-by-token rule.  The chain kernel left in the states tensor the carried state after
+// every chunk's last token (the state before chunk c > 0 of a sequence is the last
+// per-token state of chunk c - 1; before the first chunk it is the initial state, or
+// zero) and the chunk's U rows in the slot of its first token, columns of this slice;
+// this CTA is the only reader of those rows and reads them all before it overwrites the
+// slot.  Thread (r, cg) owns value columns 4 cg .. 4 cg + 3 of key rows r + 32 m, so a
+// warp stores four whole 128-byte row segments per instruction.
+constexpr int kStThreads = 256;
+
+__global__ void __launch_bounds__(kStThreads)
+states_kernel(Params p) {
+    __shared__ float sF[C][D];                    // rk_t k_t[i]
+    __shared__ __align__(16) float sU[C][NV];     // u_t, this slice's columns
+    __shared__ float sAl[C];                      // alpha_t
+    if (p.status[kStatusWord] != GDN_OK) return;
+    const int m = blockIdx.x, h = blockIdx.y, vs = blockIdx.z;
+    int cc;
+    int64_t t0;
+    int len;
+    int s;
+    if (p.cu_seqlens) {
+        if (m >= p.status[kChunkCountWord]) return;
+        s = p.chunk_seq[m];
+        cc = m - p.chunk_first[s];
+        t0 = p.cu_seqlens[s] + (int64_t)cc * C;
+        len = (int)min((int64_t)C, (int64_t)p.cu_seqlens[s + 1] - t0);
+    } else {
+        const int cps = (p.T_seq + C - 1) / C;
+        if (cps == 0 || m >= p.N * cps) return;
+        s = m / cps;
+        cc = m - s * cps;
+        t0 = (int64_t)s * p.T_seq + (int64_t)cc * C;
+        len = min(C, p.T_seq - cc * C);
+    }
+    const int n = len - 1;                        // tokens whose states are written here
+    if (n <= 0) return;
+    const int j = h / (p.HV / p.HK);
+    const int tid = threadIdx.x;
+    const size_t slot = (size_t)D * D;            // floats per (token, value head)
+    const float *F = reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(p.rec) +
+                                                     ((size_t)m * p.HV + h) * kRecBytes + REC_F);
+    const float *park = p.states + ((size_t)t0 * p.HV + h) * slot + (size_t)vs * NV;
+    for (int e = tid; e < n * (NV / 4); e += kStThreads) {
+        const int t = e >> 3, c4 = e & 7;
+        *reinterpret_cast<float4 *>(&sU[t][4 * c4]) =
+            *reinterpret_cast<const float4 *>(park + (size_t)t * D + 4 * c4);
+    }
+    for (int e = tid; e < n * (D / 8); e += kStThreads) {
+        const int t = e >> 4, c8 = e & 15;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(p.k + ((size_t)(t0 + t) * p.HK + j) * D + 8 * c8);
+        const float rk = F[SC_RK * C + t];
+        const __nv_bfloat16 *kb = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sF[t][8 * c8 + q] = rk * __bfloat162float(kb[q]);
+    }
+    if (tid < n) sAl[tid] = F[SC_ALPHA * C + tid];
+    const int cg = tid & 7, r = tid >> 3;
+    const float *src = cc > 0 ? p.states + ((size_t)(t0 - 1) * p.HV + h) * slot
+                     : p.s0 ? p.s0 + ((size_t)s * p.HV + h) * slot : nullptr;
+    float S[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (src) v4 = *reinterpret_cast<const float4 *>(src + (size_t)(r + 32 * q) * D + vs * NV + 4 * cg);
+        S[q][0] = v4.x; S[q][1] = v4.y; S[q][2] = v4.z; S[q][3] = v4.w;
+    }
+    __syncthreads();                              // every U row is read before the slot is rewritten
+    float *dst = p.states + ((size_t)t0 * p.HV + h) * slot + (size_t)vs * NV + 4 * cg;
+    for (int t = 0; t < n; ++t, dst += (size_t)p.HV * slot) {
+        const float al = sAl[t];
+        const float4 u = *reinterpret_cast<const float4 *>(&sU[t][4 * cg]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float f = sF[t][r + 32 * q];
+            S[q][0] = al * S[q][0] + f * u.x;
+            S[q][1] = al * S[q][1] + f * u.y;
+            S[q][2] = al * S[q][2] + f * u.z;
+            S[q][3] = al * S[q][3] + f * u.w;
+            st_cs_v4(dst + (size_t)(r + 32 * q) * D, S[q][0], S[q][1], S[q][2], S[q][3]);
+        }
+    }
+}
+
+// Final states when per-token states are written: the last token's state (the carried
+// chunk-form state), or the initial state (zero without one) for an empty sequence.  It
+// runs after the states kernel, the last reader of the initial states, so a final state
+// buffer that aliases the initial one is safe.
+__global__ void __launch_bounds__(256)
+final_from_states_kernel(Params p) {
+    if (p.status[kStatusWord] != GDN_OK) return;
+    const int h = blockIdx.x, s = blockIdx.y;
+    int64_t t0, t_end;
+    if (p.cu_seqlens) {
+        t0 = p.cu_seqlens[s];
+        t_end = p.cu_seqlens[s + 1];
+    } else {
+        t0 = (int64_t)s * p.T_seq;
+        t_end = t0 + p.T_seq;
+    }
+    const size_t slot = (size_t)D * D;
+    const float4 *src = t_end > t0 ? reinterpret_cast<const float4 *>(p.states + ((size_t)(t_end - 1) * p.HV + h) * slot)
+                      : p.s0 ? reinterpret_cast<const float4 *>(p.s0 + ((size_t)s * p.HV + h) * slot)
+                             : nullptr;
+    float4 *dst = reinterpret_cast<float4 *>(p.s_final + ((size_t)s * p.HV + h) * slot);
+    for (int e = threadIdx.x; e < D * D / 4; e += 256) dst[e] = src ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // ================================================================== host side
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1321,7 +1416,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     }
     Params p;
     memset(&p, 0, sizeof p);
-    p.g = pp.g; p.beta = pp.beta; p.s0 = pp.s0;
+    p.k = (const __nv_bfloat16 *)pp.k; p.g = pp.g; p.beta = pp.beta; p.s0 = pp.s0;
     p.out = (__nv_bfloat16 *)pp.out; p.s_final = pp.s_final; p.states = pp.states;
     p.cu_seqlens = pp.cu_seqlens; p.N = pp.N; p.T_seq = pp.T_seq; p.T_total = pp.T_total;
     p.HK = pp.HK; p.HV = pp.HV; p.scale = pp.scale; p.l2norm = pp.l2norm;
@@ -1373,6 +1468,14 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if ((e = cudaLaunchKernelEx(&cfg, kern, mk, mq, mv, p)) != cudaSuccess) return e;
+        if (pp.states) {
+            if (pp.max_chunks > 0) {
+                states_kernel<<<dim3(pp.max_chunks, pp.HV, D / NV), kStThreads, 0, st>>>(p);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
+            final_from_states_kernel<<<dim3(pp.HV, pp.N), 256, 0, st>>>(p);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }

@@ -75,6 +75,30 @@ def test_prefill_per_token_states(gdn, D, dtype):
     _check_vs_oracle(gdn, d, states=True)
 
 
+@pytest.mark.parametrize("T", [1, 2, 64, 65, 66, 129])
+def test_prefill_per_token_states_chunk_tails(gdn, T):
+    """Last chunks of 1 and 2 tokens (the state of a chunk's last token is the carried
+    one; the tokens before it are replayed from the chunk's U rows), whole chunks, with
+    and without an initial state."""
+    d = _inputs(2, T, 2, 4, 128, torch.bfloat16, seed=300 + T, s0=(T % 2 == 0))
+    _check_vs_oracle(gdn, d, states=True)
+
+
+def test_prefill_per_token_states_in_place_cache(gdn):
+    """Per-token states with final_state = initial_state: every per-token state still
+    starts from the initial state, and the cache ends as the last token's state."""
+    d = _cuda(_inputs(2, 150, 2, 4, 128, torch.bfloat16, seed=5, s0=True))
+    ref_out, ref_fin, ref_st = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"],
+                                           d["beta"], d["initial_state"].clone(),
+                                           output_states=True)
+    cache = d["initial_state"].clone()
+    out, fin, st = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                               cache, final_state=cache, output_states=True)
+    assert fin.data_ptr() == cache.data_ptr()
+    assert torch.equal(out, ref_out) and torch.equal(st, ref_st) and torch.equal(cache, ref_fin)
+    assert torch.equal(st[:, -1], cache)
+
+
 def test_prefill_zero_length_returns_initial_state(gdn):
     d = _cuda(_inputs(2, 0, 2, 4, 128, torch.bfloat16, seed=3, s0=True))
     out, fin, _ = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
