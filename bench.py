@@ -467,7 +467,8 @@ def main():
                     help="comma list of prologue, gated_norm, decode_gated_norm, states: time just "
                          "those steps and print one line each (profiling; not the bench line)")
     ap.add_argument("--prefill-T", type=int, default=0,
-                    help="override the headline prefill length (profiling a case larger than L2)")
+                    help="override the headline prefill length (profiling a case larger than L2); "
+                         "with --only states, the per-token-state workload's length")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -492,7 +493,8 @@ def main():
                 "decode_gated_norm": lambda: bench_decode_gated(gdn, W["decode_B256_hk16_hv32_d128"],
                                                                 args.steps, args.warmup),
                 "states": lambda: bench_prefill(gdn, W["states_B4_T1024_hk16_hv32_d128"], args.steps,
-                                                args.warmup, states=True)}
+                                                args.warmup, states=True,
+                                                T_override=args.prefill_T or None)}
         for name in args.only.split(","):
             r = runs[name]()
             if rank == 0:
