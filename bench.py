@@ -585,6 +585,11 @@ def main():
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic, "peak_source": peak_src,
                      "algorithmic_bytes": head["bytes"], "flops": head["flops"]},
+        # the same call against the tensor pipe (HBM binds: this figure is context)
+        "roofline_tensor": {"bound": "tensor", "achieved": head["flops"] / (head["ms"] * 1e-3) / 1e12,
+                            "peak": P["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": head["flops"] / (head["ms"] * 1e-3) / 1e12 / P["bf16_tflops"],
+                            "peak_source": peak_src + " (bf16 burst)"},
         "decode": {"workload": "decode_B256_hk16_hv32_d128", "value": 1e3 / dec_ms * ws,
                    "unit": "steps/s", "ms_per_step": dec_ms,
                    "roofline": {"bound": "hbm", "kernel": "decode_kernel",

@@ -763,6 +763,13 @@ __device__ __forceinline__ bool wg_and(bool v) {
     return r != 0;
 }
 
+// 8 fp32 values to global memory in one 32-byte store (a whole sector); dst 32-byte aligned
+__device__ __forceinline__ void st_v8(float *dst, const float *x) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(dst), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+                    "f"(x[7])
+                 : "memory");
+}
 // 4 fp32 values to global memory in one 16-byte streaming store; dst 16-byte aligned
 __device__ __forceinline__ void st_cs_v4(float *dst, float a0, float a1, float a2, float a3) {
     asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};"
@@ -1053,6 +1060,9 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             for (int q = 0; q < NV; ++q) S[q] = 0.f;
         }
         float *xf = reinterpret_cast<float *>(sm + OFF_X);
+        // whole 32-byte sectors for the values left in the states tensor when its base
+        // allows (every offset written below is a multiple of 64 bytes)
+        const bool states32 = STATES && ((uintptr_t)p.states & 31u) == 0;
         // Up to four (barrier, parity) pairs, a negative barrier index being skipped: warp w
         // polls pair w (all its threads), then one barrier reduction over the warpgroup
         // joins them and makes the outcome uniform (a timeout anywhere stops every thread);
@@ -1167,10 +1177,15 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 // (the states kernel reads them before it writes that slot)
                 float *dst = p.states + ((size_t)tok0 * p.HV + h) * (D * D) + (size_t)tk * D +
                              (size_t)vs * NV + hf * 16;
+                if (states32) {
+                    st_v8(dst, u16);
+                    st_v8(dst + 8, u16 + 8);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<float4 *>(dst + 4 * c) =
-                        make_float4(u16[4 * c], u16[4 * c + 1], u16[4 * c + 2], u16[4 * c + 3]);
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<float4 *>(dst + 4 * c) =
+                            make_float4(u16[4 * c], u16[4 * c + 1], u16[4 * c + 2], u16[4 * c + 3]);
+                }
             }
             fence_async_smem();
             tc_fence_before();
@@ -1228,10 +1243,15 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 // the state after the chunk's last token is the carried chunk-form state
                 float *dst = p.states + ((size_t)(tok0 + len - 1) * p.HV + h) * (D * D) + (size_t)i * D +
                              (size_t)vs * NV;
+                if (states32) {
 #pragma unroll
-                for (int q = 0; q < NV / 4; ++q)
-                    reinterpret_cast<float4 *>(dst)[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2],
-                                                                     S[4 * q + 3]);
+                    for (int q = 0; q < NV / 8; ++q) st_v8(dst + 8 * q, S + 8 * q);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NV / 4; ++q)
+                        reinterpret_cast<float4 *>(dst)[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2],
+                                                                         S[4 * q + 3]);
+                }
             }
         }
         if (lane == 0) {

@@ -84,6 +84,21 @@ def test_prefill_per_token_states_chunk_tails(gdn, T):
     _check_vs_oracle(gdn, d, states=True)
 
 
+def test_prefill_per_token_states_16_byte_aligned_buffer(gdn):
+    """A states buffer that is 16- but not 32-byte aligned (the ABI asks for 16) takes the
+    16-byte store path and gives the same bits."""
+    d = _cuda(_inputs(1, 150, 2, 4, 128, torch.bfloat16, seed=6, s0=True))
+    _, ref_fin, ref_st = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"],
+                                     d["beta"], d["initial_state"], output_states=True)
+    flat = torch.empty(ref_st.numel() + 4, dtype=torch.float32, device="cuda")
+    st = flat[4:].view(ref_st.shape)
+    assert st.data_ptr() % 32 == 16
+    _, fin, st2 = gdn.prefill(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                              d["initial_state"], states=st)
+    assert st2.data_ptr() == st.data_ptr()
+    assert torch.equal(st, ref_st) and torch.equal(fin, ref_fin)
+
+
 def test_prefill_per_token_states_in_place_cache(gdn):
     """Per-token states with final_state = initial_state: every per-token state still
     starts from the initial state, and the cache ends as the last token's state."""
