@@ -1384,17 +1384,17 @@ final_from_states_kernel(Params p) {
 }
 
 // ================================================================== host side
+// the driver's tensor-map encoder, looked up once per process (a function-local static
+// is initialised exactly once even when several host threads launch at the same time)
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         cudaDriverEntryPointQueryResult q;
         void *f = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 

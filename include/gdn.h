@@ -95,7 +95,8 @@ typedef enum {
  *   final_state     [B, HV, Dk, Dv]  float32; may equal initial_state (the
  *                                    cache continued in place); other overlap
  *                                    is not allowed
- *   states          [B, T, HV, Dk, Dv] float32 or NULL
+ *   states          [B, T, HV, Dk, Dv] float32 or NULL (16-byte alignment
+ *                   suffices; at 32 bytes the kernels write whole sectors)
  *   scale           multiplier of the normalised queries; <= 0 -> Dk^-1/2
  *   use_qk_l2norm   1: l2-normalise queries and keys in the kernel (the
  *                   model's convention); 0: use them as given
