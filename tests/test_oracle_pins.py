@@ -300,6 +300,64 @@ def test_matches_independent_one_chunk_solve(oracle_mod, T, Dk, Dv, g_scale):
     np.testing.assert_allclose(sf[0, 0], ST, rtol=0, atol=1e-10)
 
 
+def _chunked(q, k, v, g, beta, s0, scale, C=64, single_stage=False):
+    """The chunk form over chunks of C tokens, carrying the state between chunks (the
+    algebra of the tensor-core prefill).  Per chunk, with G the decay prefix restarted at
+    the chunk, gamma = e^G, T = (I + A)^{-1}, Ut = T diag(beta) V, W = T diag(beta gamma) K^:
+        U = Ut - W S,  O = diag(gamma) Q~ S + P U,  S' = gamma_C S + (diag(e^{G_C-G}) K^)^T U.
+    single_stage: the same through S' = M S + N and O = R S + P Ut with
+    M = gamma_C I - Kd^T W, N = Kd^T Ut, R = diag(gamma) Q~ - P W.
+    Also returns every token's state, replayed from the state before its chunk with the
+    chunk's U rows: S_t = e^{g_t} S_{t-1} + k^_t u_t^T."""
+    Tn, Dk = q.shape
+    qn, kn = _l2n(q) * scale, _l2n(k)
+    S = s0.copy()
+    O = np.zeros_like(v)
+    states = np.zeros((Tn, Dk, v.shape[1]))
+    for c0 in range(0, Tn, C):
+        sl = slice(c0, min(Tn, c0 + C))
+        n = sl.stop - sl.start
+        G = np.cumsum(g[sl])
+        gam = np.exp(G)
+        D = np.exp(G[:, None] - G[None, :])
+        A = beta[sl][:, None] * D * (kn[sl] @ kn[sl].T) * np.tril(np.ones((n, n)), -1)
+        Tinv = np.linalg.inv(np.eye(n) + A)
+        Ut = Tinv @ (beta[sl][:, None] * v[sl])
+        W = Tinv @ ((beta[sl] * gam)[:, None] * kn[sl])
+        P = D * (qn[sl] @ kn[sl].T) * np.tril(np.ones((n, n)))
+        Kd = np.exp(G[-1] - G)[:, None] * kn[sl]
+        U = Ut - W @ S
+        Sp = S.copy()
+        for t in range(n):
+            Sp = np.exp(g[sl][t]) * Sp + np.outer(kn[sl][t], U[t])
+            states[sl.start + t] = Sp
+        if single_stage:
+            M = gam[-1] * np.eye(Dk) - Kd.T @ W
+            R = gam[:, None] * qn[sl] - P @ W
+            O[sl] = R @ S + P @ Ut
+            S = M @ S + Kd.T @ Ut
+        else:
+            O[sl] = gam[:, None] * (qn[sl] @ S) + P @ U
+            S = gam[-1] * S + Kd.T @ U
+    return O, S, states
+
+
+@pytest.mark.parametrize("single_stage", [False, True])
+@pytest.mark.parametrize("T,g_scale", [(150, 0.05), (129, 1.0), (64, 0.5)])
+def test_matches_chunked_form_over_several_chunks(oracle_mod, T, g_scale, single_stage):
+    """Chunks of 64 carrying the state (tails of 22 and 1 tokens), the per-token states
+    replayed from each chunk's U rows, and the single-stage rewrite of the state update
+    and outputs: all equal the token-by-token rule."""
+    rng = _rng(40 + T)
+    q, k, v, g, beta, s0 = _rand_case(rng, 1, T, 1, 1, 16, 12, s0=True, g_scale=g_scale)
+    o, sf, st = oracle_mod.forward(q, k, v, g, beta, initial_state=s0, want_states=True)
+    O, ST, states = _chunked(q[0, :, 0], k[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0],
+                             s0[0, 0], 16 ** -0.5, single_stage=single_stage)
+    np.testing.assert_allclose(O, o[0, :, 0], rtol=0, atol=1e-10)
+    np.testing.assert_allclose(ST, sf[0, 0], rtol=0, atol=1e-10)
+    np.testing.assert_allclose(states, st[0, :, 0], rtol=0, atol=1e-10)
+
+
 def test_per_token_states_are_the_running_state(oracle_mod):
     """states[t] is the state after token t: o_t = states[t]^T q~_t and the last one is
     the final state."""
