@@ -113,6 +113,32 @@ def test_prefill_rejects_bad_arguments_on_host(lib, kw, code):
     assert _prefill(lib, **kw) == code
 
 
+def _noalloc(lib, **kw):
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn = lib.gdn_prefill_noalloc
+    fn.restype = i
+    fn.argtypes = [vp] * 9 + [i] * 7 + [f, i, vp]
+    a = dict(q=P, k=P, v=P, g=P, b=P, s0=None, out=P, fin=P, st=None, B=1, T=64, HK=2, HV=4,
+             Dk=128, Dv=128, dtype=0, scale=0.0, l2=1, stream=None)
+    a.update(kw)
+    return fn(a["q"], a["k"], a["v"], a["g"], a["b"], a["s0"], a["out"], a["fin"], a["st"],
+              a["B"], a["T"], a["HK"], a["HV"], a["Dk"], a["Dv"], a["dtype"], a["scale"],
+              a["l2"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(HV=3), -1), (dict(B=-1), -1), (dict(Dk=96, Dv=96), -2), (dict(dtype=5), -2),
+    (dict(q=P + 4), -3), (dict(st=P + 8), -3), (dict(fin=None), -1),
+    # the fixed scratch (64 MiB) holds 1129 records of 58 KiB: 32 value heads x 36 chunks
+    # of 64 tokens fit, x 128 chunks do not
+    (dict(T=128 * 64, HK=16, HV=32), -4), (dict(B=4, T=36 * 64, HK=16, HV=32), -4),
+])
+def test_noalloc_rejects_bad_arguments_and_oversized_shapes_on_host(lib, kw, code):
+    """gdn_prefill_noalloc checks its arguments and its scratch limit before it looks up
+    the scratch array or enqueues anything."""
+    assert _noalloc(lib, **kw) == code
+
+
 def test_varlen_rejects_bad_arguments_on_host(lib):
     f = lib.gdn_prefill_varlen
     args = [P, P, P, P, P, None, P, P, None, P, 2, 100, 2, 4, 128, 128, 0, 0.0, 1, P, BIG, None]
