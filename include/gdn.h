@@ -37,7 +37,9 @@
  * Conventions of every entry point:
  *   - Every pointer argument that names a tensor is a DEVICE pointer of the
  *     current CUDA device, 16-byte aligned.  The caller owns every buffer; the
- *     library allocates no device memory and keeps no state between calls.
+ *     library allocates no device memory and keeps no state between calls
+ *     (the one exception is gdn_prefill_noalloc's fixed scratch array, a
+ *     static part of the library's device image, described there).
  *   - Work is enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default
  *     stream) and runs asynchronously; the call returns after enqueueing.
  *   - A negative return is an error detected before anything was enqueued
