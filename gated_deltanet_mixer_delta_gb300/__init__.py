@@ -5,7 +5,8 @@ Qwen3.5 / Qwen3-Next hybrid models (qwen3_5_text page, Notes -> "The DeltaNet
 mixer"; qwen3_next page, Notes -> "The DeltaNet mixer fuses its projections per
 key head").  This module only marshals arguments: it checks tensors, allocates
 outputs with PyTorch when the caller passes none, and calls the C ABI of
-``include/gdn.h`` on the current CUDA stream.  Every step of the computation
+``include/gdn.h`` on the current CUDA stream (or on the ``stream`` given, which
+then also owns every tensor the binding allocates).  Every step of the computation
 runs in the library's CUDA kernels; there is no other implementation to fall
 back to, and a missing library is an error.
 
@@ -15,6 +16,7 @@ Layouts (the pages' linear_attn value table):
     states         [B, T, HV, Dk, Dv] float32 (state after every token)
 """
 import ctypes
+import functools
 import os
 
 import torch
@@ -173,6 +175,21 @@ def selftest_wait_timeout(limit_ns, device=None, stream=None):
     return int(s[0]), int(s[1])
 
 
+def _on_stream(fn):
+    """Run ``fn`` with its ``stream`` argument, when one is given, as torch's current
+    stream.  Every tensor the binding allocates (outputs the caller did not pass, a
+    default workspace) then belongs to the stream that the library's kernels use, so the
+    caching allocator cannot hand a freed temporary to other work while those kernels
+    still read or write it."""
+    @functools.wraps(fn)
+    def run(*args, stream=None, **kwargs):
+        if stream is None:
+            return fn(*args, stream=None, **kwargs)
+        with torch.cuda.stream(stream):
+            return fn(*args, stream=stream, **kwargs)
+    return run
+
+
 def _gated(gate, norm_weight, dtype, device, shape):
     """Checks the gated-norm arguments; True when they are given."""
     if (gate is None) != (norm_weight is None):
@@ -193,6 +210,7 @@ def _workspace(workspace, nbytes, device):
     return workspace
 
 
+@_on_stream
 def prefill(queries, keys, values, decays, beta, initial_state=None, *, scale=None,
             use_qk_l2norm=True, output_states=False, out=None, final_state=None, states=None,
             workspace=None, gate=None, norm_weight=None, norm_eps=1e-6, stream=None):
@@ -245,6 +263,7 @@ def prefill(queries, keys, values, decays, beta, initial_state=None, *, scale=No
     return out, final_state, states
 
 
+@_on_stream
 def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_state=None, *,
                    scale=None, use_qk_l2norm=True, output_states=False, out=None,
                    final_state=None, states=None, workspace=None, gate=None, norm_weight=None,
@@ -306,6 +325,7 @@ def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_stat
     return out, final_state, states
 
 
+@_on_stream
 def decode_step(queries, keys, values, decays, beta, state, *, scale=None, use_qk_l2norm=True,
                 out=None, gate=None, norm_weight=None, norm_eps=1e-6, stream=None):
     """One decode step (gdn_decode_step): queries/keys [B, HK, Dk], values [B, HV, Dv],
@@ -346,6 +366,7 @@ def decode_step(queries, keys, values, decays, beta, state, *, scale=None, use_q
     return out
 
 
+@_on_stream
 def gated_rmsnorm(y, gate, norm_weight, *, eps=1e-6, out=None, stream=None):
     """Gated RMS norm of the mixer output (gdn_gated_rmsnorm): y, gate [..., Dv] (bf16 or
     float32, same dtype), norm_weight [Dv] float32.  Returns
@@ -370,6 +391,7 @@ def gated_rmsnorm(y, gate, norm_weight, *, eps=1e-6, out=None, stream=None):
 LAYOUTS = {"qkv": 0, "qkvz": 1}
 
 
+@_on_stream
 def conv_gate_prologue(proj, proj_b, proj_a, conv_weight, A_log, dt_bias, *, HK, HV, Dk, Dv,
                        layout="qkv", conv_state=None, conv_state_out=None, cu_seqlens=None,
                        stream=None):
