@@ -538,3 +538,17 @@ def test_regroup_matches_the_hand_listed_layout(oracle_mod):
     q, k, v, z, b, a = oracle_mod.regroup_qkvz(qkvz, ba, HK=2, HV=4, Dk=2, Dv=2)
     for name, got in zip("qkvzba", (q, k, v, z, b, a)):
         np.testing.assert_array_equal(got[0].reshape(G[name].shape), G[name])
+
+
+def test_split_matches_the_hand_listed_layout(oracle_mod):
+    """tests/golden/split_qkv_hk2_hv4_dk2_dv3.txt: the channels each of q, k, v takes out of
+    the conv output, listed by hand from the page's cat(q, k, v) (q heads, then k heads,
+    then v heads, each head contiguous).  Value heads wider than key heads, so a reshape
+    with the head and width axes swapped, a v taken before k, or a width taken from the
+    wrong field all move some channel."""
+    G = _parse_golden(os.path.join(GOLDEN, "split_qkv_hk2_hv4_dk2_dv3.txt"))
+    y = np.arange(20, dtype=float)[None, :]
+    q, k, v = oracle_mod.split_qkv(y, HK=2, HV=4, Dk=2, Dv=3)
+    assert q.shape == (1, 2, 2) and k.shape == (1, 2, 2) and v.shape == (1, 4, 3)
+    for name, got in zip("qkv", (q, k, v)):
+        np.testing.assert_array_equal(got[0], G[name])
