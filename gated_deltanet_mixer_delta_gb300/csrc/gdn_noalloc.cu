@@ -11,7 +11,7 @@
 // and output buffer.  Nothing here calls cudaMalloc, cudaFree or an allocating
 // library routine.
 #include <math.h>
-#include <mutex>
+#include <atomic>
 #include <string.h>
 
 #include "gdn_internal.cuh"
@@ -22,22 +22,22 @@ constexpr size_t kScratchBytes = (size_t)64 << 20;     // 64 MiB per device
 __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void *g_scratch_addr[kMaxDevices];
-cudaError_t g_setup_err[kMaxDevices];
+std::atomic<void *> g_scratch_addr[kMaxDevices];
 
 // Device address of g_scratch on the current device.  In host code the array's name
-// is only a host-side stand-in, so the address is asked for once per device (with
-// that device current) and cached.
+// is only a host-side stand-in, so the address is asked for with that device current.
+// Only a successful lookup is kept: a lookup that failed (made during a stream capture,
+// or with an error left by earlier work) is tried again on the next call.
 int scratch_for_current_device(void **addr) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
-    std::call_once(g_once[dev], [dev] {
-        g_setup_err[dev] = cudaGetSymbolAddress(&g_scratch_addr[dev], g_scratch);
-    });
-    if (g_setup_err[dev] != cudaSuccess || g_scratch_addr[dev] == nullptr) return GDN_ERR_CUDA;
-    *addr = g_scratch_addr[dev];
+    void *a = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (a == nullptr) {
+        if (cudaGetSymbolAddress(&a, g_scratch) != cudaSuccess || a == nullptr) return GDN_ERR_CUDA;
+        g_scratch_addr[dev].store(a, std::memory_order_release);
+    }
+    *addr = a;
     return GDN_OK;
 }
 
@@ -101,4 +101,18 @@ extern "C" int gdn_prefill_noalloc(const void *queries, const void *keys, const 
     p.rec_floats = tc ? tc_record_bytes() / sizeof(float) : record_floats(Dk, Dv);
     cudaError_t e = tc ? launch_prefill_tc(p, st) : launch_prefill_generic(p, dtype, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" int gdn_prefill_noalloc_status(void *cuda_stream, int *status) {
+    using namespace gdn;
+    if (!status) return GDN_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    int rc = scratch_for_current_device(&scratch);
+    if (rc != GDN_OK) return rc;
+    int32_t v = 0;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    if (cudaMemcpyAsync(&v, scratch, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ERR_CUDA;
+    *status = v;
+    return GDN_OK;
 }

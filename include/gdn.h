@@ -288,11 +288,15 @@ int gdn_decode_step_gated(const void *queries, const void *keys, const void *val
  *     library holds its 64 MiB until the process exits.
  *   - The first call on each device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream capture.
+ *     A lookup that fails is not cached: the next call tries again.
  *   - All calls share the one array and it keeps the last call's contents; the call
  *     clears the status word it reads, everything else is written before it is read.
  *     Calls whose GPU work overlaps (two streams, two host threads) race on it: order
  *     them on one stream or serialise them.
- *   - gdn_workspace_status() does not apply (there is no caller workspace).
+ *   - Errors found on the device (a bounded wait that timed out) go to the status word
+ *     at the start of the array; read it with gdn_prefill_noalloc_status() before the
+ *     next call clears it.  gdn_workspace_status() does not apply (there is no caller
+ *     workspace).
  * No cudaMalloc, cudaFree or allocating library routine is called.
  */
 int gdn_prefill_noalloc(const void *queries, const void *keys, const void *values,
@@ -300,6 +304,15 @@ int gdn_prefill_noalloc(const void *queries, const void *keys, const void *value
                         void *out, float *final_state, float *states,
                         int B, int T, int HK, int HV, int Dk, int Dv, gdn_dtype dtype,
                         float scale, int use_qk_l2norm, void *cuda_stream);
+
+/*
+ * The device status word of the last gdn_prefill_noalloc on the current device: GDN_OK
+ * or the GDN_ERR_* code its kernels recorded (GDN_ERR_TIMEOUT for a bounded wait that
+ * gave up).  Enqueues a 4-byte copy on `cuda_stream` (the stream the prefill ran on) and
+ * waits for that stream.  Returns GDN_OK, GDN_ERR_INVALID_ARG for a null `status`, or
+ * GDN_ERR_CUDA when the copy fails.  Allocates nothing.
+ */
+int gdn_prefill_noalloc_status(void *cuda_stream, int *status);
 
 /*
  * Layout of the recurrent state buffer [batch, value_heads, key_dim,

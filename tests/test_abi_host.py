@@ -129,14 +129,38 @@ def _noalloc(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(HV=3), -1), (dict(B=-1), -1), (dict(Dk=96, Dv=96), -2), (dict(dtype=5), -2),
     (dict(q=P + 4), -3), (dict(st=P + 8), -3), (dict(fin=None), -1),
-    # the fixed scratch (64 MiB) holds 1129 records of 58 KiB: 32 value heads x 36 chunks
-    # of 64 tokens fit, x 128 chunks do not
+    # the fixed scratch (64 MiB) holds 1129 records of 58 KiB after its header and chunk
+    # table: 32 value heads x 35 chunks of 64 tokens fit, x 36 do not
     (dict(T=128 * 64, HK=16, HV=32), -4), (dict(B=4, T=36 * 64, HK=16, HV=32), -4),
+    (dict(T=35 * 64 + 1, HK=16, HV=32), -4),
 ])
 def test_noalloc_rejects_bad_arguments_and_oversized_shapes_on_host(lib, kw, code):
     """gdn_prefill_noalloc checks its arguments and its scratch limit before it looks up
     the scratch array or enqueues anything."""
     assert _noalloc(lib, **kw) == code
+
+
+def test_noalloc_scratch_limit_boundary_on_host(lib):
+    """B = 1, T = 2240 at 32 value heads (35 chunks, 1120 records) is the largest
+    128 x 128 bf16 prompt the scratch takes: it passes the size check and only then
+    needs a device (here none: GDN_ERR_CUDA); one token more is rejected with
+    GDN_ERR_WORKSPACE before any device call."""
+    assert _noalloc(lib, T=2240, HK=16, HV=32) not in (-4,)
+    assert _noalloc(lib, T=2241, HK=16, HV=32) == -4
+
+
+def test_noalloc_status_reader_arguments_on_host(lib):
+    """gdn_prefill_noalloc_status rejects a null result pointer; without a device the
+    copy itself fails with GDN_ERR_CUDA rather than returning a stale value."""
+    fn = lib.gdn_prefill_noalloc_status
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert fn(None, None) == -1
+    st = ctypes.c_int(12345)
+    rc = fn(None, ctypes.byref(st))
+    import torch
+    if not torch.cuda.is_available():
+        assert rc == -5 and st.value == 12345
 
 
 def test_varlen_rejects_bad_arguments_on_host(lib):

@@ -31,7 +31,17 @@ def gdn():
     lib.gdn_prefill_noalloc.restype = i
     lib.gdn_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                         f, i, vp]
+    lib.gdn_prefill_noalloc_status.restype = i
+    lib.gdn_prefill_noalloc_status.argtypes = [vp, vp]
     return m
+
+
+def _status(gdn):
+    st = ctypes.c_int(-99)
+    rc = gdn.abi().gdn_prefill_noalloc_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
+                                               ctypes.byref(st))
+    assert rc == 0, rc
+    return st.value
 
 
 def _noalloc(gdn, d, states=False):
@@ -72,11 +82,27 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row(gdn):
     assert_states_close(s1, r1[2].double().cpu().numpy(), "call 1 states")
     assert_out_close(o2, r2[0].double().cpu().numpy(), torch.float32, "call 2 out")
     assert_states_close(f2, r2[1].double().cpu().numpy(), "call 2 final state")
+    assert _status(gdn) == 0
     # the first call again, after the second one reused the scratch array
     o3, f3, _ = _noalloc(gdn, d1)
     torch.cuda.synchronize()
     assert_out_close(o3, r1[0].double().cpu().numpy(), torch.bfloat16, "call 3 out")
     assert_states_close(f3, r1[1].double().cpu().numpy(), "call 3 final state")
+    assert _status(gdn) == 0
+
+
+def test_noalloc_empty_prompts_carry_the_initial_state(gdn):
+    """B = 2 sequences of T = 0 tokens: no chunk runs, the final state is the initial
+    state (and zero without one), as with gdn_prefill."""
+    d = _cuda(workloads.draw_inputs(2, 0, 2, 4, 128, 128, torch.bfloat16, 73, init_state_std=0.02))
+    _, fin, _ = _noalloc(gdn, d)
+    torch.cuda.synchronize()
+    assert torch.equal(fin, d["initial_state"])
+    d0 = dict(d, initial_state=None)
+    _, fin0, _ = _noalloc(gdn, d0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(fin0) == 0
+    assert _status(gdn) == 0
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(gdn):
