@@ -393,6 +393,181 @@ class OracleSample:
         return (self.n / self.w.HV) * self.T / el
 
 
+def oracle_chain_rate(w, target_s=6.0, want_states=False):
+    """The fp64 oracle on whole (sequence, value head) chains of workload w, as many as
+    run in about `target_s` seconds on the host cores (packed batches use their own
+    sequences).  Returns (tokens/s with all value heads of a token counted once, cores,
+    description of the sample)."""
+    import concurrent.futures as cf
+    import oracle
+    d = workloads.workload_inputs(w, device="cpu")
+    cores = oracle.default_threads()
+    r = w.HV // w.HK
+    if w.n_seqs:
+        cu = [int(x) for x in d["cu_seqlens"].tolist()]
+        spans = [(0, cu[i], cu[i + 1]) for i in range(w.n_seqs)]
+    else:
+        spans = [(b, 0, d["queries"].shape[1]) for b in range(w.B)]
+    order = [(s, h) for h in range(w.HV) for s in range(len(spans))]  # spread over sequences
+
+    def one(sh):
+        s, h = sh
+        b, a, e = spans[s]
+        s0 = d.get("initial_state")
+        oracle.chain(d["queries"][b, a:e, h // r], d["keys"][b, a:e, h // r], d["values"][b, a:e, h],
+                     d["decays"][b, a:e, h], d["beta"][b, a:e, h],
+                     initial_state=None if s0 is None else s0[s, h], want_states=want_states)
+        return e - a
+
+    t0 = time.perf_counter()
+    first = one(order[0])
+    t_one = max(time.perf_counter() - t0, 1e-6)
+    per_token = t_one / max(first, 1)
+    budget = target_s * cores / per_token                  # chain-tokens in the budget
+    chosen, tok = [], 0
+    for sh in order[1:]:
+        n = spans[sh[0]][2] - spans[sh[0]][1]
+        if chosen and tok + n > budget:
+            break
+        chosen.append(sh)
+        tok += n
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        done = sum(ex.map(one, chosen)) if chosen else 0
+    el = time.perf_counter() - t0
+    if not chosen:
+        done, el = first, t_one
+    desc = (f"{len(chosen) or 1} (sequence, value head) chains ({done} chain-tokens) of {w.name}"
+            f"{' with per-token states' if want_states else ''}, fp64, {cores} threads")
+    return (done / w.HV) / el, cores, desc
+
+
+def oracle_decode_rate(w, target_s=6.0, n_seq=32):
+    """The fp64 oracle's decode step on `n_seq` of the workload's sequences (all value
+    heads), consecutive steps carrying the state; the rate is scaled to steps of the full
+    batch (sequences are independent, so a step's work is proportional to the batch)."""
+    import oracle
+    d = workloads.decode_inputs(w, steps=16, device="cpu")
+    cores = oracle.default_threads()
+    n_seq = min(n_seq, w.B)
+    st = d["initial_state"][:n_seq].contiguous()
+    names = ("queries", "keys", "values", "decays", "beta")
+    step = lambda i, st: oracle.decode_step(*(d[n][i][:n_seq].contiguous() for n in names), st,
+                                            n_threads=cores)[1]
+    t0 = time.perf_counter()
+    st = step(0, st)
+    t1 = max(time.perf_counter() - t0, 1e-6)
+    k = max(1, min(15, int(target_s / t1)))
+    t0 = time.perf_counter()
+    for i in range(k):
+        st = step(1 + i, st)
+    el = time.perf_counter() - t0
+    return (k / el) * n_seq / w.B, cores, (f"{k} consecutive decode steps of {n_seq} of the {w.B} sequences "
+                                           f"of {w.name} (all heads; rate scaled to the full batch), "
+                                           f"fp64, {cores} threads")
+
+
+def oracle_norm_rate(w, target_s=4.0):
+    """The oracle's gated RMS norm over rows of workload w's output shape; rows/s."""
+    import oracle
+    gen = torch.Generator().manual_seed(5)
+    rows = w.T * w.HV
+    y = torch.randn(rows, w.Dv, generator=gen).to(w.dtype)
+    z = torch.randn(rows, w.Dv, generator=gen).to(w.dtype)
+    wt = 1.0 + 0.3 * torch.randn(w.Dv, generator=gen)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.gated_rmsnorm(y, z, wt)
+        n += 1
+        el = time.perf_counter() - t0
+        if el > target_s or n >= 50:
+            break
+    return n * rows / el, 1, f"{n} passes over {rows} rows of {w.Dv} ({w.name} outputs), fp64, 1 thread"
+
+
+def oracle_prologue_rate(w, target_s=4.0):
+    """The oracle's regroup of Qwen3-Next's fused projections, conv + SiLU and gates over
+    one prompt of workload w; tokens/s."""
+    import oracle
+    gen = torch.Generator().manual_seed(6)
+    HK, HV, D, T = w.HK, w.HV, w.Dk, w.T
+    r = HV // HK
+    C = 2 * HK * D + HV * D
+    proj = torch.randn(1, T, HK * (2 * D + 2 * r * D), generator=gen).to(w.dtype)
+    ba = torch.randn(1, T, 2 * HV, generator=gen).to(w.dtype)
+    cw = torch.randn(C, 4, generator=gen) * 0.5
+    al = torch.randn(HV, generator=gen) * 0.5
+    db = torch.randn(HV, generator=gen) * 0.5
+    import numpy as np
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        q, k, v, z, b, a = oracle.regroup_qkvz(proj, ba, HK, HV, D, D)
+        x = np.concatenate([q.reshape(1, T, -1), k.reshape(1, T, -1), v.reshape(1, T, -1)], axis=-1)
+        oracle.conv_gate(x, b, a, cw, al, db)
+        n += 1
+        el = time.perf_counter() - t0
+        if el > target_s or n >= 20:
+            break
+    return n * T / el, 1, f"{n} prompts of {T} tokens of {w.name} (fused layout), fp64, 1 thread"
+
+
+def oracle_decode_gated_rate(w, target_s=6.0, n_seq=32):
+    """The oracle's decode step followed by the gated RMS norm of its output, on `n_seq`
+    sequences; steps/s scaled to the full batch."""
+    import oracle
+    d = workloads.decode_inputs(w, steps=16, device="cpu")
+    cores = oracle.default_threads()
+    n_seq = min(n_seq, w.B)
+    st = d["initial_state"][:n_seq].contiguous()
+    gen = torch.Generator().manual_seed(4)
+    z = torch.randn(n_seq, w.HV, w.Dv, generator=gen).to(w.dtype)
+    wt = 1.0 + 0.3 * torch.randn(w.Dv, generator=gen)
+    names = ("queries", "keys", "values", "decays", "beta")
+
+    def step(i, st):
+        o, st = oracle.decode_step(*(d[n][i][:n_seq].contiguous() for n in names), st, n_threads=cores)
+        oracle.gated_rmsnorm(o, z, wt)
+        return st
+
+    t0 = time.perf_counter()
+    st = step(0, st)
+    t1 = max(time.perf_counter() - t0, 1e-6)
+    k = max(1, min(15, int(target_s / t1)))
+    t0 = time.perf_counter()
+    for i in range(k):
+        st = step(1 + i, st)
+    el = time.perf_counter() - t0
+    return (k / el) * n_seq / w.B, cores, (f"{k} consecutive gated decode steps of {n_seq} of the {w.B} "
+                                           f"sequences of {w.name} (rate scaled to the full batch), fp64, "
+                                           f"{cores} threads")
+
+
+def oracle_prefill_gated_rate(w, target_s=6.0):
+    """The oracle's prefill of whole chains of workload w followed by the gated RMS norm of
+    their outputs; tokens/s with all value heads of a token counted once."""
+    import oracle
+    d = workloads.workload_inputs(w, device="cpu")
+    cores = oracle.default_threads()
+    gen = torch.Generator().manual_seed(7)
+    zf = torch.randn(w.T, w.Dv, generator=gen).to(w.dtype)
+    wt = 1.0 + 0.3 * torch.randn(w.Dv, generator=gen)
+    t0 = time.perf_counter()
+    o, _, _ = oracle.forward(*(d[k][:1] for k in ("queries", "keys", "values", "decays", "beta")),
+                             chains=[0], n_threads=1)
+    one = max(time.perf_counter() - t0, 1e-6)
+    n = max(1, min(w.HV, int(target_s * cores / one)))
+    t0 = time.perf_counter()
+    o, _, _ = oracle.forward(d["queries"], d["keys"], d["values"], d["decays"], d["beta"],
+                             chains=list(range(n)), n_threads=cores)
+    for h in range(n):
+        oracle.gated_rmsnorm(o[0, :, h], zf, wt)
+    el = time.perf_counter() - t0
+    return (n / w.HV) * w.T / el, cores, (f"{n} value-head chains x {w.T} tokens of {w.name}, each output "
+                                          f"then gated-normed, fp64, {cores} threads")
+
+
 # ---------------------------------------------------------------- main
 def dist_setup(backend="nccl"):
     """One process per GPU (torchrun): rank, local rank and world size from the env."""
@@ -464,8 +639,9 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline and decode only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
-                    help="comma list of prologue, gated_norm, decode_gated_norm, states: time just "
-                         "those steps and print one line each (profiling; not the bench line)")
+                    help="comma list of prologue, gated_norm, decode_gated_norm, states, headline, "
+                         "varlen, long, hv48, hv16: time just those steps and print one line each "
+                         "(profiling; not the bench line)")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="override the headline prefill length (profiling a case larger than L2); "
                          "with --only states, the per-token-state workload's length")
@@ -494,7 +670,16 @@ def main():
                                                                 args.steps, args.warmup),
                 "states": lambda: bench_prefill(gdn, W["states_B4_T1024_hk16_hv32_d128"], args.steps,
                                                 args.warmup, states=True,
-                                                T_override=args.prefill_T or None)}
+                                                T_override=args.prefill_T or None),
+                "headline": lambda: bench_prefill(gdn, head_w, args.steps, args.warmup),
+                "varlen": lambda: bench_prefill(gdn, W["varlen8_512to8192_hk16_hv32_d128"], args.steps,
+                                                args.warmup),
+                "long": lambda: bench_prefill(gdn, W["long_prefill_B2_T65536_hk16_hv32_d128"],
+                                              args.steps, args.warmup),
+                "hv48": lambda: bench_prefill(gdn, W["qwen35_27b_prefill_T4096_hk16_hv48_d128"],
+                                              args.steps, args.warmup),
+                "hv16": lambda: bench_prefill(gdn, W["qwen35_0p8b_prefill_T4096_hk16_hv16_d128"],
+                                              args.steps, args.warmup)}
         for name in args.only.split(","):
             r = runs[name]()
             if rank == 0:
@@ -512,6 +697,7 @@ def main():
 
     # end to end right after the headline, before the larger workloads churn memory
     e2e = bench_e2e(gdn, head_w, max(5, min(args.steps, 20)), 2)
+    e2e_s = max_over_ranks(e2e["s"], ws)
 
     subs = {}
     if not args.quick:
@@ -521,11 +707,12 @@ def main():
                               ("prefill_hv48", "qwen35_27b_prefill_T4096_hk16_hv48_d128", {}),
                               ("prefill_hv16", "qwen35_0p8b_prefill_T4096_hk16_hv16_d128", {})):
             r = bench_prefill(gdn, W[name], max(3, min(args.steps, 5)), 3, **kw)
-            subs[key] = dict(workload=name, tokens=r["tokens"], ms=r["ms"],
-                             tokens_per_s=r["tokens"] / (r["ms"] * 1e-3),
-                             roofline={"bound": "hbm", "achieved": r["bytes"] / (r["ms"] * 1e-3) / 1e9,
+            r_ms = max_over_ranks(r["ms"], ws)
+            subs[key] = dict(workload=name, tokens=r["tokens"], ms=r_ms,
+                             tokens_per_s=ws * r["tokens"] / (r_ms * 1e-3),
+                             roofline={"bound": "hbm", "achieved": r["bytes"] / (r_ms * 1e-3) / 1e9,
                                        "peak": hbm, "unit": "GB/s",
-                                       "frac": r["bytes"] / (r["ms"] * 1e-3) / 1e9 / hbm,
+                                       "frac": r["bytes"] / (r_ms * 1e-3) / 1e9 / hbm,
                                        "algorithmic_bytes": r["bytes"]})
         dg = bench_decode_gated(gdn, W["decode_B256_hk16_hv32_d128"], max(args.steps, 20),
                                 args.warmup)
@@ -565,6 +752,25 @@ def main():
         sample = OracleSample(head_w)
         cpu = {"value": sample.run(), "unit": "tokens/s", "cores": sample.cores, "kind": "oracle",
                "sample": sample.desc}
+        # the oracle on the other rows: a bounded sample of each workload
+        rate, cores, desc = oracle_decode_rate(W["decode_B256_hk16_hv32_d128"])
+        dec["cpu_baseline"] = {"value": rate, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                               "sample": desc}
+        for key, wants in (("varlen", False), ("long_prefill", False), ("states", True),
+                           ("prefill_hv48", False), ("prefill_hv16", False)):
+            if key in subs:
+                rate, cores, desc = oracle_chain_rate(W[subs[key]["workload"]], want_states=wants)
+                subs[key]["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores,
+                                             "kind": "oracle", "sample": desc}
+        for key, fn, unit in (("decode_gated_norm", lambda: oracle_decode_gated_rate(
+                                    W["decode_B256_hk16_hv32_d128"]), "steps/s"),
+                              ("prefill_gated_norm", lambda: oracle_prefill_gated_rate(head_w), "tokens/s"),
+                              ("prologue", lambda: oracle_prologue_rate(head_w), "tokens/s"),
+                              ("gated_norm", lambda: oracle_norm_rate(head_w), "rows/s")):
+            if key in subs:
+                rate, cores, desc = fn()
+                subs[key]["cpu_baseline"] = {"value": rate, "unit": unit, "cores": cores,
+                                             "kind": "oracle", "sample": desc}
 
     if rank != 0:
         return
@@ -593,12 +799,13 @@ def main():
         "decode": {"workload": "decode_B256_hk16_hv32_d128", "value": 1e3 / dec_ms * ws,
                    "unit": "steps/s", "ms_per_step": dec_ms,
                    "roofline": {"bound": "hbm", "kernel": "decode_kernel",
-                                "achieved": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9,
+                                "achieved": dec["bytes"] / (dec_ms * 1e-3) / 1e9,
                                 "peak": hbm, "unit": "GB/s",
-                                "frac": dec["bytes"] / (dec["ms"] * 1e-3) / 1e9 / hbm,
+                                "frac": dec["bytes"] / (dec_ms * 1e-3) / 1e9 / hbm,
                                 "traffic": measured_traffic("decode_kernel_B256.md", "gdn_decode.cu"),
-                                "algorithmic_bytes": dec["bytes"]}},
-        "e2e": {"value": e2e["tokens"] / e2e["s"] * ws, "unit": "tokens/s",
+                                "algorithmic_bytes": dec["bytes"]},
+                   "cpu_baseline": dec.get("cpu_baseline")},
+        "e2e": {"value": e2e["tokens"] / e2e_s * ws, "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": args.steps * head["launches_per_call"],
         "clocks": clk,
