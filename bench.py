@@ -18,6 +18,7 @@ CUDA-event times on the launching stream.  ``--impl reference`` times the fp64
 CPU oracle on the host cores instead (bounded sample of the same workload).
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -186,7 +187,7 @@ def bench_prefill(gdn, w, iters, warmup, states=False, T_override=None, gated=Fa
     out = torch.empty_like(v)
     fin = torch.empty(N, HV, D, D, dtype=torch.float32, device=dev)
     st = torch.empty(*v.shape[:-1], D, D, dtype=torch.float32, device=dev) if states else None
-    ws = torch.empty(gdn.workspace_size(T_total, N, HV, D, D), dtype=torch.uint8, device=dev)
+    ws = torch.empty(gdn.workspace_size(T_total, N, HV, D, D, dtype=q.dtype), dtype=torch.uint8, device=dev)
     gk = {}
     if gated:
         gen = torch.Generator(device="cuda").manual_seed(7)
@@ -319,7 +320,7 @@ def bench_e2e(gdn, w, iters, warmup):
     fin_h = [torch.empty(B, w.HV, w.Dk, w.Dv, dtype=torch.float32).pin_memory() for _ in range(nb)]
     out_d = [torch.empty_like(out_h[0], device="cuda") for _ in range(nb)]
     fin_d = [torch.empty_like(fin_h[0], device="cuda") for _ in range(nb)]
-    ws = torch.empty(gdn.workspace_size(B * T, B, w.HV, w.Dk, w.Dv), dtype=torch.uint8,
+    ws = torch.empty(gdn.workspace_size(B * T, B, w.HV, w.Dk, w.Dv, dtype=w.dtype), dtype=torch.uint8,
                      device="cuda")
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(nb)]
@@ -640,8 +641,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
                     help="comma list of prologue, gated_norm, decode_gated_norm, states, headline, "
-                         "varlen, long, hv48, hv16: time just those steps and print one line each "
-                         "(profiling; not the bench line)")
+                         "varlen, long, hv48, hv16, f32, tiny: time just those steps and print one "
+                         "line each (profiling; not the bench line)")
     ap.add_argument("--prefill-T", type=int, default=0,
                     help="override the headline prefill length (profiling a case larger than L2); "
                          "with --only states, the per-token-state workload's length")
@@ -679,7 +680,12 @@ def main():
                 "hv48": lambda: bench_prefill(gdn, W["qwen35_27b_prefill_T4096_hk16_hv48_d128"],
                                               args.steps, args.warmup),
                 "hv16": lambda: bench_prefill(gdn, W["qwen35_0p8b_prefill_T4096_hk16_hv16_d128"],
-                                              args.steps, args.warmup)}
+                                              args.steps, args.warmup),
+                # the CUDA-core prefill: fp32 inputs at the headline shape, and the tiny case
+                "f32": lambda: bench_prefill(gdn, dataclasses.replace(head_w, dtype=torch.float32,
+                                                                      name=head_w.name + "_f32"),
+                                             args.steps, args.warmup),
+                "tiny": lambda: bench_prefill(gdn, W["tiny_T64_H2_d32_f32"], args.steps, args.warmup)}
         for name in args.only.split(","):
             r = runs[name]()
             if rank == 0:

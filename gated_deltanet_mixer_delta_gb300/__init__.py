@@ -96,6 +96,8 @@ def load_library(build_if_missing: bool = False):
     lib.gdn_state_layout.argtypes = [i, i, i, i, ctypes.POINTER(_StateLayout)]
     lib.gdn_prefill_workspace_size.restype = sz
     lib.gdn_prefill_workspace_size.argtypes = [ctypes.c_int64, i, i, i, i]
+    lib.gdn_prefill_workspace_size_for.restype = sz
+    lib.gdn_prefill_workspace_size_for.argtypes = [ctypes.c_int64, i, i, i, i, i]
     lib.gdn_workspace_status.restype = i
     lib.gdn_workspace_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     lib.gdn_status_string.restype = ctypes.c_char_p
@@ -150,8 +152,13 @@ def state_layout(batch, HV, Dk, Dv):
                 shape=tuple(lay.shape), alignment=lay.alignment)
 
 
-def workspace_size(T_total, n_seqs, HV, Dk, Dv) -> int:
-    return int(load_library().gdn_prefill_workspace_size(T_total, n_seqs, HV, Dk, Dv))
+def workspace_size(T_total, n_seqs, HV, Dk, Dv, dtype=None) -> int:
+    """Workspace bytes of a prefill: for `dtype` (torch.bfloat16 / torch.float32) exactly
+    what that path needs, without it enough for either."""
+    lib = load_library()
+    if dtype is None:
+        return int(lib.gdn_prefill_workspace_size(T_total, n_seqs, HV, Dk, Dv))
+    return int(lib.gdn_prefill_workspace_size_for(T_total, n_seqs, HV, Dk, Dv, _DTYPES[dtype]))
 
 
 def workspace_status(workspace, stream=None) -> int:
@@ -245,7 +252,7 @@ def prefill(queries, keys, values, decays, beta, initial_state=None, *, scale=No
     if states is not None:
         _need(states, "states", torch.float32, dev, (B, T, HV, Dk, Dv))
     lib = load_library()
-    nbytes = lib.gdn_prefill_workspace_size(B * T, B, HV, Dk, Dv)
+    nbytes = lib.gdn_prefill_workspace_size_for(B * T, B, HV, Dk, Dv, _DTYPES[dt])
     ws = _workspace(workspace, nbytes, dev)
     if _gated(gate, norm_weight, dt, dev, (B, T, HV, Dv)):
         rc = lib.gdn_prefill_gated(_ptr(queries), _ptr(keys), _ptr(values), _ptr(decays),
@@ -305,7 +312,7 @@ def prefill_varlen(queries, keys, values, decays, beta, cu_seqlens, initial_stat
     if states is not None:
         _need(states, "states", torch.float32, dev, (*lead, HV, Dk, Dv))
     lib = load_library()
-    nbytes = lib.gdn_prefill_workspace_size(T_total, N, HV, Dk, Dv)
+    nbytes = lib.gdn_prefill_workspace_size_for(T_total, N, HV, Dk, Dv, _DTYPES[dt])
     ws = _workspace(workspace, nbytes, dev)
     if _gated(gate, norm_weight, dt, dev, tuple(values.shape)):
         rc = lib.gdn_prefill_varlen_gated(

@@ -22,11 +22,23 @@ static size_t table_bytes(int max_chunks, int n_seqs) {
     return round_up(sizeof(int32_t) * ((size_t)max_chunks + 2 * (size_t)n_seqs + 1), 256);
 }
 
-size_t prefill_workspace_bytes(int64_t T_total, int n_seqs, int HV, int Dk, int Dv) {
+// bytes of one record of the path a shape and dtype take: the tensor-core path's operand
+// images, or the CUDA-core path's fp32 record
+static size_t record_bytes_for(int Dk, int Dv, gdn_dtype dtype) {
+    return tc_supported(Dk, Dv, dtype) ? tc_record_bytes() : record_floats(Dk, Dv) * sizeof(float);
+}
+
+size_t prefill_workspace_bytes_for(int64_t T_total, int n_seqs, int HV, int Dk, int Dv, gdn_dtype dtype) {
     // sized for the packed bound, which also covers equal-length batches
     const int mc = max_chunks_for(T_total, n_seqs, true, 0);
-    return kWsHeader + table_bytes(mc, n_seqs) +
-           (size_t)mc * HV * record_floats(Dk, Dv) * sizeof(float);
+    return kWsHeader + table_bytes(mc, n_seqs) + (size_t)mc * HV * record_bytes_for(Dk, Dv, dtype);
+}
+
+size_t prefill_workspace_bytes(int64_t T_total, int n_seqs, int HV, int Dk, int Dv) {
+    // without a dtype: enough for either path
+    const size_t a = prefill_workspace_bytes_for(T_total, n_seqs, HV, Dk, Dv, GDN_BF16);
+    const size_t b = prefill_workspace_bytes_for(T_total, n_seqs, HV, Dk, Dv, GDN_F32);
+    return a > b ? a : b;
 }
 
 }  // namespace gdn
@@ -72,7 +84,7 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     // final_state may be initial_state (in place); no other overlap is checked here
     if (!workspace) return GDN_ERR_WORKSPACE;
     if ((uintptr_t)workspace & 255u) return GDN_ERR_MISALIGNED;
-    if (workspace_bytes < prefill_workspace_bytes(T_total, N, HV, Dk, Dv)) return GDN_ERR_WORKSPACE;
+    if (workspace_bytes < prefill_workspace_bytes_for(T_total, N, HV, Dk, Dv, dtype)) return GDN_ERR_WORKSPACE;
 
     cudaStream_t st = (cudaStream_t)cuda_stream;
     const bool packed = cu_seqlens != nullptr;
@@ -93,7 +105,7 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     p.chunk_first = p.chunk_seq + mc;
     p.seq_order = p.chunk_first + N + 1;
     p.rec = (float *)(ws + kWsHeader + table_bytes(mc, N));
-    p.rec_floats = record_floats(Dk, Dv);
+    p.rec_floats = record_bytes_for(Dk, Dv, dtype) / sizeof(float);
 
     if (N == 0) {
         // nothing to run; leave a clean status word
@@ -271,6 +283,12 @@ int gdn_state_layout(int batch, int HV, int Dk, int Dv, gdn_state_layout_t *layo
 size_t gdn_prefill_workspace_size(int64_t T_total, int n_seqs, int HV, int Dk, int Dv) {
     if (T_total < 0 || n_seqs < 0 || HV <= 0 || !dim_ok(Dk) || !dim_ok(Dv)) return 0;
     return prefill_workspace_bytes(T_total, n_seqs, HV, Dk, Dv);
+}
+
+size_t gdn_prefill_workspace_size_for(int64_t T_total, int n_seqs, int HV, int Dk, int Dv, gdn_dtype dtype) {
+    if (T_total < 0 || n_seqs < 0 || HV <= 0 || !dim_ok(Dk) || Dv != Dk) return 0;
+    if (dtype != GDN_BF16 && dtype != GDN_F32) return 0;
+    return prefill_workspace_bytes_for(T_total, n_seqs, HV, Dk, Dv, dtype);
 }
 
 int gdn_workspace_status(const void *workspace, void *cuda_stream, int *status) {

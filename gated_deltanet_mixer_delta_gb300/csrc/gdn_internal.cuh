@@ -52,6 +52,7 @@ inline size_t record_floats(int Dk, int Dv) {
 }
 
 size_t prefill_workspace_bytes(int64_t T_total, int n_seqs, int HV, int Dk, int Dv);
+size_t prefill_workspace_bytes_for(int64_t T_total, int n_seqs, int HV, int Dk, int Dv, gdn_dtype dtype);
 int max_chunks_for(int64_t T_total, int n_seqs, bool packed, int T_seq);
 
 // Launchers (return cudaError_t of the launches).

@@ -333,10 +333,20 @@ int gdn_state_layout(int batch, int HV, int Dk, int Dv, gdn_state_layout_t *layo
 
 /*
  * Bytes of device workspace gdn_prefill / gdn_prefill_varlen need for
- * `T_total` tokens in `n_seqs` sequences (B for gdn_prefill).  Host-only.
- * Returns 0 for invalid sizes.
+ * `T_total` tokens in `n_seqs` sequences (B for gdn_prefill), whatever the dtype
+ * (the larger of the two paths' needs).  Host-only.  Returns 0 for invalid sizes.
  */
 size_t gdn_prefill_workspace_size(int64_t T_total, int n_seqs, int HV, int Dk, int Dv);
+
+/*
+ * The same for a given dtype: exactly what the path that shape and dtype take needs
+ * (128 x 128 bf16 heads take the tensor-core path, 58 KiB per (chunk, value head);
+ * the other shapes and fp32 the CUDA-core path, 4 * (64 (Dk + Dv + 64) + 320) bytes).
+ * A workspace of this size is accepted by calls with that dtype.  Host-only.
+ * Returns 0 for invalid sizes or dtype.
+ */
+size_t gdn_prefill_workspace_size_for(int64_t T_total, int n_seqs, int HV, int Dk, int Dv,
+                                      gdn_dtype dtype);
 
 /*
  * Read the device status word a prefill wrote into `workspace`: GDN_OK, or

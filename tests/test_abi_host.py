@@ -10,6 +10,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
@@ -81,6 +82,33 @@ def test_workspace_size(lib):
     assert gdn.workspace_size(0, 0, 32, 128, 128) > 0
     assert gdn.workspace_size(10, 1, 32, 96, 96) == 0
     assert gdn.workspace_size(-1, 1, 32, 128, 128) == 0
+
+
+def test_workspace_size_for_each_path(lib):
+    """With a dtype the size is exactly what that path needs: 58 KiB records of operand
+    images for 128 x 128 bf16 heads (tensor cores), fp32 records of 64 (Dk + Dv + 64) + 320
+    floats otherwise; without one, the larger of the two."""
+    import gated_deltanet_mixer_delta_gb300 as gdn
+    T, N, HV = 4096, 1, 32
+    bf = gdn.workspace_size(T, N, HV, 128, 128, dtype=torch.bfloat16)
+    f32 = gdn.workspace_size(T, N, HV, 128, 128, dtype=torch.float32)
+    both = gdn.workspace_size(T, N, HV, 128, 128)
+    chunks = T // 64 + N                          # the packed bound on chunks
+    assert f32 - bf == chunks * HV * (4 * (64 * (128 + 128 + 64) + 320) - 59392)
+    assert both == max(bf, f32) == f32
+    # 32 x 32 heads take the CUDA-core path whatever the dtype
+    assert gdn.workspace_size(T, N, HV, 32, 32, dtype=torch.bfloat16) == \
+        gdn.workspace_size(T, N, HV, 32, 32, dtype=torch.float32)
+    assert lib.gdn_prefill_workspace_size_for(10, 1, 32, 128, 128, 7) == 0
+
+
+def test_prefill_checks_the_workspace_of_its_own_path_on_host(lib):
+    """The host check asks for the dtype's exact size: one byte less is rejected, and an
+    fp32 call does not accept the smaller bf16 size."""
+    import gated_deltanet_mixer_delta_gb300 as gdn
+    bf = gdn.workspace_size(64, 1, 4, 128, 128, dtype=torch.bfloat16)
+    assert _prefill(lib, wsb=bf - 1) == -4
+    assert _prefill(lib, wsb=bf, dtype=1) == -4
 
 
 def test_status_strings(lib):
