@@ -17,7 +17,8 @@ int max_chunks_for(int64_t T_total, int n_seqs, bool packed, int T_seq) {
     return (int)((T_total + kChunk - 1) / kChunk + n_seqs);
 }
 
-// header | chunk_seq[max_chunks] | chunk_first[N+1] | seq_order[N] | records[max_chunks][HV]
+// header | chain flags[N*HV*kChainSlices] | chunk_seq[max_chunks] | chunk_first[N+1] |
+// seq_order[N] | records[max_chunks][HV]
 static size_t table_bytes(int max_chunks, int n_seqs) {
     return round_up(sizeof(int32_t) * ((size_t)max_chunks + 2 * (size_t)n_seqs + 1), 256);
 }
@@ -31,7 +32,8 @@ static size_t record_bytes_for(int Dk, int Dv, gdn_dtype dtype) {
 size_t prefill_workspace_bytes_for(int64_t T_total, int n_seqs, int HV, int Dk, int Dv, gdn_dtype dtype) {
     // sized for the packed bound, which also covers equal-length batches
     const int mc = max_chunks_for(T_total, n_seqs, true, 0);
-    return kWsHeader + table_bytes(mc, n_seqs) + (size_t)mc * HV * record_bytes_for(Dk, Dv, dtype);
+    return kWsHeader + chain_flag_bytes(n_seqs, HV) + table_bytes(mc, n_seqs) +
+           (size_t)mc * HV * record_bytes_for(Dk, Dv, dtype);
 }
 
 size_t prefill_workspace_bytes(int64_t T_total, int n_seqs, int HV, int Dk, int Dv) {
@@ -72,6 +74,7 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     if (N < 0 || T_total < 0 || T_seq < 0) return GDN_ERR_INVALID_ARG;
     if (gate_z && T_total > 0 && !norm_weight) return GDN_ERR_INVALID_ARG;
     if (T_total > INT32_MAX || N > 65535 || HV > 65535) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)N * HV * kChainSlices > INT32_MAX) return GDN_ERR_UNSUPPORTED;   // chain numbers
     if (N > 0 && !final_state) return GDN_ERR_INVALID_ARG;
     if (T_total > 0 && (!queries || !keys || !values || !decays || !beta || !out))
         return GDN_ERR_INVALID_ARG;
@@ -100,11 +103,13 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     p.scale = resolve_scale(scale, Dk);
     p.l2norm = use_qk_l2norm ? 1 : 0;
     p.max_chunks = mc;
+    const size_t flag_bytes = chain_flag_bytes(N, HV);
     p.status = (int32_t *)ws;
-    p.chunk_seq = (int32_t *)(ws + kWsHeader);
+    p.chain_flags = (int32_t *)(ws + kWsHeader);
+    p.chunk_seq = (int32_t *)(ws + kWsHeader + flag_bytes);
     p.chunk_first = p.chunk_seq + mc;
     p.seq_order = p.chunk_first + N + 1;
-    p.rec = (float *)(ws + kWsHeader + table_bytes(mc, N));
+    p.rec = (float *)(ws + kWsHeader + flag_bytes + table_bytes(mc, N));
     p.rec_floats = record_bytes_for(Dk, Dv, dtype) / sizeof(float);
 
     if (N == 0) {

@@ -58,6 +58,7 @@ extern "C" int gdn_prefill_noalloc(const void *queries, const void *keys, const 
     if (dtype != GDN_BF16 && dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
     if (isnan(scale) || isinf(scale)) return GDN_ERR_INVALID_ARG;
     if (B > 65535 || HV > 65535 || (int64_t)B * T > INT32_MAX) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)B * HV * kChainSlices > INT32_MAX) return GDN_ERR_UNSUPPORTED;   // chain numbers
     const int64_t T_total = (int64_t)B * T;
     if (B > 0 && !final_state) return GDN_ERR_INVALID_ARG;
     if (T_total > 0 && (!queries || !keys || !values || !decays || !beta || !out))
@@ -72,15 +73,16 @@ extern "C" int gdn_prefill_noalloc(const void *queries, const void *keys, const 
     const bool tc = tc_supported(Dk, Dv, dtype);
     const size_t rec_bytes = tc ? tc_record_bytes() : record_floats(Dk, Dv) * sizeof(float);
     const size_t table = round256(sizeof(int32_t) * ((size_t)mc + B + 1));
-    const size_t need = kWsHeader + table + (size_t)mc * HV * rec_bytes;
+    const size_t flag_bytes = chain_flag_bytes(B, HV);
+    const size_t need = kWsHeader + flag_bytes + table + (size_t)mc * HV * rec_bytes;
     if (need > kScratchBytes) return GDN_ERR_WORKSPACE;     // beyond the fixed maximum
 
     void *scratch = nullptr;
     int rc = scratch_for_current_device(&scratch);
     if (rc != GDN_OK) return rc;
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    // the array keeps the previous call's contents: start from a clean status word
-    if (cudaMemsetAsync(scratch, 0, kWsHeader, st) != cudaSuccess) return GDN_ERR_CUDA;
+    // the array keeps the previous call's contents: start from clean status and flag words
+    if (cudaMemsetAsync(scratch, 0, kWsHeader + flag_bytes, st) != cudaSuccess) return GDN_ERR_CUDA;
     if (B == 0) return GDN_OK;
 
     char *ws = (char *)scratch;
@@ -95,9 +97,10 @@ extern "C" int gdn_prefill_noalloc(const void *queries, const void *keys, const 
     p.l2norm = use_qk_l2norm ? 1 : 0;
     p.max_chunks = mc;
     p.status = (int32_t *)ws;
-    p.chunk_seq = (int32_t *)(ws + kWsHeader);
+    p.chain_flags = (int32_t *)(ws + kWsHeader);
+    p.chunk_seq = (int32_t *)(ws + kWsHeader + flag_bytes);
     p.chunk_first = p.chunk_seq + mc;
-    p.rec = (float *)(ws + kWsHeader + table);
+    p.rec = (float *)(ws + kWsHeader + flag_bytes + table);
     p.rec_floats = tc ? tc_record_bytes() / sizeof(float) : record_floats(Dk, Dv);
     cudaError_t e = tc ? launch_prefill_tc(p, st) : launch_prefill_generic(p, dtype, st);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

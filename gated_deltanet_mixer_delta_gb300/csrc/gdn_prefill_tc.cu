@@ -19,7 +19,10 @@
 //           W^T = K^T T'^T on the tensor core, P; writes -W (hi/lo), T'' (hi/lo) and P
 //           as operand images, and the per-token factors.
 //  chain -- one CTA per (sequence, value head, 32-wide value slice), the sequential
-//           chunk loop, warp-specialised (256 threads): a TMA producer warp, a warp that
+//           chunk loop (or, when an equal-length batch has more of these chains than the
+//           GPU has SMs, one persistent CTA per SM running a stream of chain segments
+//           whose states pass between CTAs), warp-specialised (256 threads): a TMA
+//           producer warp, a warp that
 //           issues the products off the chain's critical path, two output warps, and an
 //           epilogue warpgroup that holds the fp32 state slice in registers (thread i =
 //           key row i), forms U, Z = kd U and the new state, and issues the products
@@ -73,6 +76,10 @@ struct Params {
     int max_chunks;
     int32_t *status, *chunk_seq, *chunk_first, *seq_order;
     float *rec;                  // [chunks][HV] records of kRecBytes
+    // the chain kernel's work-unit stream: a unit is a run of at most seg_len consecutive
+    // chunks of one of the n_chains (sequence, value head, value slice) chains
+    int32_t *chain_flags;        // [n_chains] segments of the chain whose end state is out
+    int seg_len, n_chains, n_units;
 };
 
 // ------------------------------------------------------------------ shared helpers
@@ -715,7 +722,8 @@ constexpr int OFF_Z = OFF_S + 16384;                       // [Z_hi | Z_lo] [64 
 constexpr int OFF_U = OFF_Z + 8192;                        // U_hi [64 tokens][64B] MN-major
 constexpr int OFF_X = OFF_U + 4096;                        // fp32 [2][64][16] half-row exchange
                                                            // (16-byte chunks XOR-swizzled)
-constexpr int OFF_BAR = OFF_X + C * NV * 4;
+constexpr int OFF_BAR = OFF_X + C * NV * 4;                // barriers, TMEM slot, error flag
+constexpr int OFF_DESC = OFF_BAR + 128;                    // chunk descriptors [4][8] int32
 constexpr int kChainSmem = OFF_BAR + 256 + 1024;
 static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0 && kAV % 1024 == 0 && kBQ % 1024 == 0,
               "swizzled operands need 1 KiB alignment");
@@ -792,7 +800,77 @@ __device__ __forceinline__ void store_row_hilo128(uint8_t *img, int row, const f
 // are XOR-swizzled so that eight consecutive rows hit eight different bank groups
 __device__ __forceinline__ int xchg_off(int t, int c) { return t * 16 + ((c ^ ((t >> 1) & 3)) << 2); }
 
-template <bool STATES>
+// Work units (equal-length batches whose chains outnumber the SMs).  A chain is one
+// (sequence, value head, 32-wide value slice); its chunks are cut into segments of at
+// most seg_len chunks, and the units are numbered segment-major (segment 0 of every
+// chain, then segment 1, ...), so that the CTAs, one per SM, share the work evenly
+// instead of running whole waves of chains.  CTA b takes unit b first; later units are
+// claimed in order from an atomic counter by running CTAs, so a unit's predecessor (the
+// previous segment of its chain) was taken earlier by a CTA that has started.  A
+// segment's end state goes through global memory (the final-state slice, or with
+// per-token states the slot of its last token) and a flag word per chain.
+struct Unit {
+    SeqRange sr;
+    int s, h, vs, seg, c0, c1;      // chunks c0 .. c1 - 1 of the sequence
+};
+
+__device__ __forceinline__ bool unit_of(const Params &p, int u, Unit &w) {
+    constexpr int SL = D / NV;
+    int c = u, seg = 0;
+    if (!p.cu_seqlens) {
+        seg = u / p.n_chains;
+        c = u - seg * p.n_chains;
+    }
+    const int per_seq = p.HV * SL;
+    const int z = c / per_seq, rem = c - z * per_seq;
+    w.h = rem / SL;
+    w.vs = rem - w.h * SL;
+    w.s = p.cu_seqlens ? p.seq_order[z] : z;
+    if (!seq_range(p, w.s, w.sr)) return false;
+    w.seg = seg;
+    w.c0 = min(w.sr.count, seg * p.seg_len);
+    w.c1 = min(w.sr.count, w.c0 + p.seg_len);
+    return true;
+}
+
+// Descriptor of one chunk of a chain CTA's stream, written by the producer before it
+// arms the chunk's ring barriers (whose phase then publishes it to the other warps).
+enum { DW_TOK = 0, DW_LEN, DW_CHAIN, DW_SEG, DW_HEAD, DW_SLICE, kDescWords = 8 };
+enum { DF_FIRST = 1, DF_LAST = 2, DF_END = 4, DF_STOP = 8 };   // DW_LEN bits 8 and up
+constexpr int kDescSlots = 4;
+static_assert(8 * B_COUNT + 8 <= OFF_DESC - OFF_BAR && OFF_DESC - OFF_BAR + kDescSlots * kDescWords * 4 <= 256,
+              "barrier area");
+static_assert(D / NV == kChainSlices, "chain flag words per value head");
+
+// Flag words between CTAs: the writer publishes after a barrier that follows every
+// participating thread's stores (the fence makes them visible at GPU scope first); the
+// reader acquires before a barrier that precedes the other threads' loads.
+__device__ __forceinline__ void flag_release(int32_t *f, int32_t v) {
+    asm volatile("fence.acq_rel.gpu;\n\tst.relaxed.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t flag_acquire(const int32_t *f) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// wait until *f >= want; gives up (false) after limit_ns
+__device__ __forceinline__ bool flag_wait(const int32_t *f, int32_t want, uint64_t limit_ns = 1000000000ull) {
+    if (flag_acquire(f) >= want) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(128);
+        if (flag_acquire(f) >= want) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// UNITS == false: one CTA per chain, launched as a (value slice, value head, sequence)
+// grid, packed batches' chains longest first (the hardware starts the CTAs in order).
+// UNITS == true: the persistent work-unit stream above (equal-length batches whose chains
+// outnumber the SMs).  The per-chunk work is the same code; only the loops around it and
+// the source of a chunk's coordinates differ, and each schedule compiles only its own
+// loops (the kernel's speed depends on the size of its loop code: instruction fetch).
+template <bool STATES, bool UNITS>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
              const __grid_constant__ CUtensorMap mapV, Params p) {
@@ -802,16 +880,21 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 8 * B_COUNT);
     volatile int *s_err = reinterpret_cast<volatile int *>(sm + OFF_BAR + 8 * B_COUNT + 4);
+    int32_t *descs = reinterpret_cast<int32_t *>(sm + OFF_DESC);
 
-    const int vs = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // packed batches: the longest sequences first (the chunk-table kernel ranked them)
     if (p.cu_seqlens && p.status[kStatusWord] != GDN_OK) return;
-    const int s = p.cu_seqlens ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
-    SeqRange sr;
-    if (!seq_range(p, s, sr)) return;
-    const int j = h / (p.HV / p.HK);
-    const int nch = sr.count;
+    // the CTA's own chain (UNITS == false)
+    int vs = 0, h = 0, s = 0, j = 0, nch = 0;
+    SeqRange sr{};
+    if constexpr (!UNITS) {
+        vs = blockIdx.x;
+        h = blockIdx.y;
+        s = p.cu_seqlens ? p.seq_order[blockIdx.z] : (int)blockIdx.z;
+        if (!seq_range(p, s, sr)) return;
+        j = h / (p.HV / p.HK);
+        nch = sr.count;
+    }
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -829,7 +912,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         mbar_init(&bars[B_DRAIN], 8);
         *s_err = 0;
         fence_mbar_init();
-        if (nch > 0) {
+        if (UNITS ? p.n_units > 0 : nch > 0) {
             prefetch_tensormap(&mapK);
             prefetch_tensormap(&mapQ);
             prefetch_tensormap(&mapV);
@@ -852,6 +935,7 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     };
     auto ring_a = [&](int cc) { return sm + OFF_A + (cc & 1) * kStageA; };
     auto ring_b = [&](int cc) { return sm + OFF_B + (cc & 1) * kStageB; };
+    auto desc = [&](int cc) { return descs + (cc & (kDescSlots - 1)) * kDescWords; };
     const uint32_t s_img = smem_u32(sm + OFF_S), z_img = smem_u32(sm + OFF_Z);
 
     // -W S of chunk cc from the state of chunk cc - 1, k-steps 4(w-1) .. 4(w-1)+3, issued
@@ -890,40 +974,123 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 mma_commit(&bars[B_D1]);
                 return true;
             };
+            // the loads of chunk cc: ring A (the record's first 48 KiB and the value slice of
+            // value head hh, slice vv), ring B (key and query tiles of key head jj, P and the
+            // factor rows)
+            auto load_a = [&](int cc, const uint8_t *rec, int tok, int hh, int vv) {
+                uint8_t *sa = ring_a(cc);
+                uint64_t *fa = &bars[B_FULLA0 + (cc & 1)];
+                mbar_arrive_expect_tx(fa, kStageA);
+                bulk_load(sa + kAW, rec, REC_P, fa);
+                tma_load_3d(sa + kAV, &mapV, fa, vv * NV, hh, tok);
+            };
+            auto load_b = [&](int cc, const uint8_t *rec, int tok, int jj) {
+                uint8_t *sb = ring_b(cc);
+                uint64_t *fb = &bars[B_FULLB0 + (cc & 1)];
+                mbar_arrive_expect_tx(fb, kStageB);
+                tma_load_3d(sb + kBK, &mapK, fb, 0, jj, tok);
+                tma_load_3d(sb + kBK + 8192, &mapK, fb, 64, jj, tok);
+                tma_load_3d(sb + kBQ, &mapQ, fb, 0, jj, tok);
+                tma_load_3d(sb + kBQ + 8192, &mapQ, fb, 64, jj, tok);
+                bulk_load(sb + kBP, rec + REC_P, kStageB - kBP, fb);
+            };
             bool issued = false;
             // the records come from the prep grid, which may still be running
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            // iteration cc: (once -W S of chunk cc - 2 is done) T'' V of chunk cc - 1, then
-            // the loads of chunk cc; the last iteration only issues T'' V of chunk nch - 1.
-            // T'' V of chunk 0 waits for its inputs, so it follows the loads of chunk 1.
-            for (int cc = 0; cc <= nch; ++cc) {
-                const int st = cc & 1, u = cc >> 1;
-                if (cc >= 2 && !wait(B_EMPTYA0 + st, (u - 1) & 1)) break;
-                if (cc >= 2 || (cc == 1 && nch == 1)) {
-                    if (!issue_tv(cc - 1)) break;
-                    issued = true;
+            if constexpr (!UNITS) {
+                // iteration cc: (once -W S of chunk cc - 2 is done) T'' V of chunk cc - 1, then
+                // the loads of chunk cc; the last iteration only issues T'' V of chunk nch - 1.
+                // T'' V of chunk 0 waits for its inputs, so it follows the loads of chunk 1.
+                for (int cc = 0; cc <= nch; ++cc) {
+                    const int st = cc & 1, u = cc >> 1;
+                    if (cc >= 2 && !wait(B_EMPTYA0 + st, (u - 1) & 1)) break;
+                    if (cc >= 2 || (cc == 1 && nch == 1)) {
+                        if (!issue_tv(cc - 1)) break;
+                        issued = true;
+                    }
+                    if (cc == nch) break;
+                    const int tok = (int)(sr.t0 + (int64_t)cc * C);
+                    const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.rec) +
+                                         ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes;
+                    load_a(cc, rec, tok, h, vs);
+                    if (u >= 1 && !wait(B_EMPTYB0 + st, (u - 1) & 1)) break;
+                    load_b(cc, rec, tok, j);
+                    if (cc == 1) {
+                        if (!issue_tv(0)) break;
+                        issued = true;
+                    }
                 }
-                if (cc == nch) break;
-                const int tok = (int)(sr.t0 + (int64_t)cc * C);
-                const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.rec) +
-                                     ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes;
-                uint8_t *sa = ring_a(cc);
-                uint64_t *fa = &bars[B_FULLA0 + st];
-                mbar_arrive_expect_tx(fa, kStageA);
-                bulk_load(sa + kAW, rec, REC_P, fa);
-                tma_load_3d(sa + kAV, &mapV, fa, vs * NV, h, tok);
-                if (u >= 1 && !wait(B_EMPTYB0 + st, (u - 1) & 1)) break;
-                uint8_t *sb = ring_b(cc);
-                uint64_t *fb = &bars[B_FULLB0 + st];
-                mbar_arrive_expect_tx(fb, kStageB);
-                tma_load_3d(sb + kBK, &mapK, fb, 0, j, tok);
-                tma_load_3d(sb + kBK + 8192, &mapK, fb, 64, j, tok);
-                tma_load_3d(sb + kBQ, &mapQ, fb, 0, j, tok);
-                tma_load_3d(sb + kBQ + 8192, &mapQ, fb, 64, j, tok);
-                bulk_load(sb + kBP, rec + REC_P, kStageB - kBP, fb);
-                if (cc == 1) {
-                    if (!issue_tv(0)) break;
-                    issued = true;
+            } else {
+                Unit w;
+                int k = 0, nk = 0;          // chunk k of the nk chunks of the current unit
+                // the first unit of CTA b is unit b (a chain's first segment: no
+                // predecessor); later ones come from the counter, after the grid's first round
+                int next_u = blockIdx.x;
+                // per unit: key head, chain number; per chunk (advanced after its loads):
+                // first token and record
+                int jj = 0, chain = 0, tok = 0;
+                const uint8_t *rec = nullptr;
+                const size_t rec_step = (size_t)p.HV * kRecBytes;
+                // iteration cc (once -W S of chunk cc - 2 is done): the next chunk of the
+                // stream (of the current unit, else of the next unit claimed that has chunks)
+                // or the end of the stream, published in the chunk's descriptor, and T'' V of
+                // chunk cc - 1
+                for (int cc = 0;; ++cc) {
+                    const int st = cc & 1, u = cc >> 1;
+                    if (cc >= 2 && !wait(B_EMPTYA0 + st, (u - 1) & 1)) break;
+                    bool stop = false;
+                    while (k >= nk) {
+                        const int un = next_u >= 0 ? next_u
+                                     : p.n_units <= (int)gridDim.x ? p.n_units   // all were first ones
+                                     : (int)gridDim.x + atomicAdd(&p.status[kClaimWord], 1);
+                        next_u = -1;
+                        if (un >= p.n_units || !unit_of(p, un, w)) { stop = true; break; }
+                        k = 0;
+                        nk = w.c1 - w.c0;
+                        jj = w.h / (p.HV / p.HK);
+                        chain = (w.s * p.HV + w.h) * (D / NV) + w.vs;
+                        tok = (int)(w.sr.t0 + (int64_t)w.c0 * C);
+                        rec = reinterpret_cast<const uint8_t *>(p.rec) +
+                              ((size_t)(w.sr.first + w.c0) * p.HV + w.h) * kRecBytes;
+                    }
+                    int32_t *d = desc(cc);
+                    if (stop) {
+                        // an armed phase with no data: the other warps read the end marker
+                        d[DW_LEN] = DF_STOP << 8;
+                        mbar_arrive(&bars[B_FULLA0 + st]);
+                    } else {
+                        const int len = (int)min((int64_t)C, w.sr.t_end - tok);
+                        const int fl = (k == 0 ? DF_FIRST : 0) | (k == nk - 1 ? DF_LAST : 0) |
+                                       (w.c0 + k == w.sr.count - 1 ? DF_END : 0);
+                        d[DW_TOK] = tok;
+                        d[DW_LEN] = len | (fl << 8);
+                        d[DW_CHAIN] = chain;
+                        d[DW_SEG] = w.seg;
+                        d[DW_HEAD] = w.h;
+                        d[DW_SLICE] = w.vs;
+                        load_a(cc, rec, tok, w.h, w.vs);
+                    }
+                    // T'' V of chunk cc - 1 goes ahead of ring B's wait (which ends only with
+                    // the state update of chunk cc - 2), so that it runs before -W S of chunk
+                    // cc - 1
+                    if (cc >= 2 || (cc == 1 && stop)) {
+                        if (!issue_tv(cc - 1)) break;
+                        issued = true;
+                    }
+                    if (u >= 1 && !wait(B_EMPTYB0 + st, (u - 1) & 1)) break;
+                    if (stop) {
+                        mbar_arrive(&bars[B_FULLB0 + st]);
+                        break;
+                    }
+                    load_b(cc, rec, tok, jj);
+                    ++k;
+                    tok += C;
+                    rec += rec_step;
+                    // T'' V of chunk 0 waits for its inputs, so it follows the loads of chunk 1
+                    if (cc == 1) {
+                        if (!issue_tv(0)) break;
+                        issued = true;
+                    }
                 }
             }
             if (issued) mma_commit(&bars[B_DRAIN]);
@@ -934,12 +1101,16 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         if (lane == 0) {
             constexpr uint32_t id_o = instr_desc(128, NV, kFmtBF16, 0, 1);
             bool issued = false;
-            for (int cc = 0; cc < nch; ++cc) {
+            for (int cc = 0; UNITS || cc < nch; ++cc) {
                 // P U_hi (outputs only: one bf16 term) once U is formed and the output
                 // warps have read the previous chunk's
                 // polled without parking: the tensor pipe runs in order, and P U issued late
-                // would sit in front of the next chunk's -W S
+                // would sit in front of the next chunk's -W S.  At the end of a stream the
+                // epilogue completes one more phase, and the chunk's descriptor says so.
                 if (*s_err || !mbar_wait_spin(&bars[B_E1DONE], cc & 1)) { fail(); break; }
+                if constexpr (UNITS) {
+                    if (desc(cc)[DW_LEN] & (DF_STOP << 8)) break;
+                }
                 if (cc >= 1 && !wait(B_OUT, (cc - 1) & 1)) break;
                 issued = true;
                 tc_fence_after();
@@ -962,13 +1133,35 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         const int t = tid - 192;
         const uint32_t lb = lane_base(warp);
         bool issued = false;
-        for (int cc = 0; cc < nch; ++cc) {
+        for (int cc = 0; UNITS || cc < nch; ++cc) {
+            // this thread's token, whether it is in the sequence, the value head and slice
+            int64_t tok;
+            bool live;
+            int hh, vv;
+            if constexpr (UNITS) {
+                // ring B's phase publishes the chunk's descriptor (or the end of the stream)
+                bool ok = !*s_err && mbar_wait(&bars[B_FULLB0 + (cc & 1)], (cc >> 1) & 1);
+                if (!ok) fail();
+                if (!__all_sync(0xffffffffu, ok)) break;
+                const int32_t *d = desc(cc);
+                const int dlen = d[DW_LEN];
+                if (dlen & (DF_STOP << 8)) break;
+                tok = (int64_t)d[DW_TOK] + t;
+                live = t < (dlen & 255);
+                hh = d[DW_HEAD];
+                vv = d[DW_SLICE];
+            } else {
+                tok = sr.t0 + (int64_t)cc * C + t;
+                live = tok < sr.t_end;
+                hh = h;
+                vv = vs;
+            }
             // Q S of chunk cc, k-steps 4 (warp - 6) .. + 3: A = [any; Q] read from 8 KiB
             // before the query tile so that the live rows land in TMEM lanes 64-127.  The
             // state operand it reads was written before -W S of chunk cc was issued and is
             // rewritten only after QSD; both output warps have read Q S of chunk cc - 1 (OUT).
             if (lane == 0) {
-                bool ok2 = wait(B_D1, cc & 1) && wait(B_FULLB0 + (cc & 1), (cc >> 1) & 1) &&
+                bool ok2 = wait(B_D1, cc & 1) && (UNITS || wait(B_FULLB0 + (cc & 1), (cc >> 1) & 1)) &&
                            (cc == 0 || wait(B_OUT, (cc - 1) & 1));
                 if (ok2) {
                     tc_fence_after();
@@ -988,14 +1181,16 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 }
             }
             __syncwarp();
+            if constexpr (!UNITS) {
+                bool ok = !*s_err && mbar_wait(&bars[B_FULLB0 + (cc & 1)], (cc >> 1) & 1);
+                if (!ok) fail();
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
             // the chunk's query factor, then release ring B's factor rows
-            bool ok = !*s_err && mbar_wait(&bars[B_FULLB0 + (cc & 1)], (cc >> 1) & 1);
-            if (!ok) fail();
-            if (!__all_sync(0xffffffffu, ok)) break;
             const float qd = reinterpret_cast<const float *>(ring_b(cc) + kBF)[SC_QD * C + t];
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_EMPTYB0 + (cc & 1)]);
-            ok = !*s_err && mbar_wait(&bars[B_QSD], cc & 1) && mbar_wait(&bars[B_DO], cc & 1);
+            bool ok = !*s_err && mbar_wait(&bars[B_QSD], cc & 1) && mbar_wait(&bars[B_DO], cc & 1);
             if (!ok) fail();
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
@@ -1023,9 +1218,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                                          f2pack(o3[q], o3[q + 1]));
                 f2unpack(r, o1[q], o1[q + 1]);
             }
-            const int64_t tok = sr.t0 + (int64_t)cc * C + t;
-            if (tok < sr.t_end) {
-                __nv_bfloat16 *dst = p.out + ((size_t)tok * p.HV + h) * D + (size_t)vs * NV;
+            if (live) {
+                __nv_bfloat16 *dst = p.out + ((size_t)tok * p.HV + hh) * D + (size_t)vv * NV;
 #pragma unroll
                 for (int q = 0; q < NV; q += 8) {
                     uint32_t w[4];
@@ -1048,17 +1242,6 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
         const uint32_t lb = lane_base(warp);
         const int tk = i & 63, hf = i >> 6;        // token, column half handled in E1
         float S[NV];
-        const size_t sbase = (((size_t)s * p.HV + h) * D + i) * D + (size_t)vs * NV;
-        if (p.s0) {
-#pragma unroll
-            for (int q = 0; q < NV / 4; ++q) {
-                const float4 v4 = reinterpret_cast<const float4 *>(p.s0 + sbase)[q];
-                S[4 * q] = v4.x; S[4 * q + 1] = v4.y; S[4 * q + 2] = v4.z; S[4 * q + 3] = v4.w;
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < NV; ++q) S[q] = 0.f;
-        }
         float *xf = reinterpret_cast<float *>(sm + OFF_X);
         // whole 32-byte sectors for the values left in the states tensor when its base
         // allows (every offset written below is a multiple of 64 bytes)
@@ -1075,31 +1258,81 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
             if (ok && b >= 0 && !mbar_wait(&bars[b], par)) { fail(); ok = false; }
             return wg_and(ok);
         };
-        store_row_hilo128(sm + OFF_S, i, S);
-        fence_async_smem();
-        named_sync(1, 128);
-        int nch_run = nch;
-        bool issued = false;                // this lane has issued tensor-core work
-        if (nch > 0) {
-            if (!wg_wait4(B_FULLA0, 0, -1, 0, -1, 0, -1, 0)) nch_run = 0;
-            else if (lane == 0 && (warp == 1 || warp == 2)) {
-                issue_ws(warp, 0);
-                issued = true;
+        // row i of a chain's slice in a [N][HV][D][D] fp32 state tensor (chains are numbered
+        // (sequence, value head, slice)-major)
+        auto slice_row = [&](int chain) -> size_t {
+            return ((size_t)(chain / (D / NV)) * D + i) * D + (size_t)(chain % (D / NV)) * NV;
+        };
+        // the lead's end-state flag not yet published (the next segment of its chain waits)
+        int32_t *pend = nullptr;
+        int32_t pend_v = 0;
+        // The state slice at the start of the unit of descriptor d: the initial state (zero
+        // without one) for a chain's first segment, else the end state of the previous
+        // segment once its CTA has published it (this CTA's own pending flag goes out first
+        // if that means waiting); then its bf16 hi/lo operand image.
+        auto unit_state = [&](const int32_t *d) -> bool {
+            const int seg = d[DW_SEG];
+            bool ok = !*s_err;
+            if (lead && ok && seg > 0) {
+                const int32_t *f = p.chain_flags + d[DW_CHAIN];
+                if (flag_acquire(f) < seg) {
+                    if (pend) { flag_release(pend, pend_v); pend = nullptr; }
+                    if (!flag_wait(f, seg)) { fail(); ok = false; }
+                }
             }
-            __syncwarp();
-        }
-        for (int cc = 0; cc < nch_run; ++cc) {
+            if (!wg_and(ok)) return false;
+            const float *src = nullptr;
+            if (seg == 0) src = p.s0 ? p.s0 + slice_row(d[DW_CHAIN]) : nullptr;
+            else if (STATES)
+                src = p.states + ((size_t)(d[DW_TOK] - 1) * p.HV + d[DW_HEAD]) * (D * D) + (size_t)i * D +
+                      (size_t)d[DW_SLICE] * NV;
+            else src = p.s_final + slice_row(d[DW_CHAIN]);
+            if (src) {
+#pragma unroll
+                for (int q = 0; q < NV / 4; ++q) {
+                    const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(src) + q);
+                    S[4 * q] = v4.x; S[4 * q + 1] = v4.y; S[4 * q + 2] = v4.z; S[4 * q + 3] = v4.w;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < NV; ++q) S[q] = 0.f;
+            }
+            store_row_hilo128(sm + OFF_S, i, S);
+            fence_async_smem();
+            tc_fence_before();
+            named_sync(1, 128);
+            return true;
+        };
+        bool issued = false;                // this lane has issued tensor-core work
+        // the state after a chunk's last token, with per-token states: the carried
+        // chunk-form state
+        auto state_out = [&](float *dst) {
+            if (states32) {
+#pragma unroll
+                for (int q = 0; q < NV / 8; ++q) st_v8(dst + 8 * q, S + 8 * q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < NV / 4; ++q)
+                    reinterpret_cast<float4 *>(dst)[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2],
+                                                                     S[4 * q + 3]);
+            }
+        };
+        // One chunk of the chain: E1 (U, Z = kd U, K^T Z) and E2 (the new state); then,
+        // unless the chunk ends its unit, the next state operand, -W S of the next chunk
+        // (issue_next) and, with per-token states, the carried state.  (tok0, len, hh, vv):
+        // the chunk's first token and length, value head and value slice; wait_next: ring A
+        // of the next chunk is armed (data, or the end of a stream).  Returns 0 (next chunk),
+        // 1 (the chunk ends its unit: the state is in S), -1 (a wait gave up).
+        auto chunk = [&](int cc, int64_t tok0, int len, int hh, int vv, bool wait_next, bool unit_end,
+                         bool issue_next) -> int {
             const int st = cc & 1;
             uint8_t *sb = ring_b(cc);
             const float *F = reinterpret_cast<const float *>(sb + kBF);
-            const int64_t tok0 = sr.t0 + (int64_t)cc * C;
-            const int len = (int)min((int64_t)C, sr.t_end - tok0);
             // ---- E1: U = rows 0-63 + rows 64-127 of (-W S + T'' V), Z = kd U; the previous
-            // chunk's P U_hi must have read the U_hi image.  Ring A of the next chunk is
-            // checked here too, for the -W S issued after the state update.
+            // chunk's P U_hi must have read the U_hi image
             if (!wg_wait4(B_D1, cc & 1, B_FULLB0 + st, (cc >> 1) & 1, cc >= 1 ? B_DO : -1, (cc - 1) & 1,
-                          cc + 1 < nch ? B_FULLA0 + (st ^ 1) : -1, ((cc + 1) >> 1) & 1))
-                break;
+                          -1, 0))
+                return -1;
             if (lead) mbar_arrive(&bars[B_EMPTYA0 + st]);   // ring A of chunk cc is consumed
             tc_fence_after();
             const float kd = F[SC_KD * C + tk], gl = F[SC_MISC * C + 0];
@@ -1175,8 +1408,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 // U rows 0 .. len-2 of the chunk (fp32, this slice's columns) for the states
                 // kernel, parked in the slot of the chunk's first token: row t at float t * D
                 // (the states kernel reads them before it writes that slot)
-                float *dst = p.states + ((size_t)tok0 * p.HV + h) * (D * D) + (size_t)tk * D +
-                             (size_t)vs * NV + hf * 16;
+                float *dst = p.states + ((size_t)tok0 * p.HV + hh) * (D * D) + (size_t)tk * D +
+                             (size_t)vv * NV + hf * 16;
                 if (states32) {
                     st_v8(dst, u16);
                     st_v8(dst + 8, u16 + 8);
@@ -1206,8 +1439,13 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 issued = true;
             }
             __syncwarp();
-            // ---- E2: new state (thread i = key row i)
-            if (!wg_wait4(B_D2, cc & 1, B_QSD, cc & 1, -1, 0, -1, 0)) break;
+            // ---- E2: new state (thread i = key row i).  Ring A of the next chunk is checked
+            // here, for the -W S issued after the update: its loads start only once E1 of this
+            // chunk has released the other stage, and waiting for them in E1 would put their
+            // latency on the chain.
+            if (!wg_wait4(B_D2, cc & 1, B_QSD, cc & 1, wait_next ? B_FULLA0 + (st ^ 1) : -1, ((cc + 1) >> 1) & 1,
+                          -1, 0))
+                return -1;
             tc_fence_after();
             float ds[NV];
             {
@@ -1229,42 +1467,118 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 const uint64_t r = ffma2(f2pack(gl, gl), f2pack(S[c], S[c + 1]), f2pack(ds[c], ds[c + 1]));
                 f2unpack(r, S[c], S[c + 1]);
             }
+            if (unit_end) return 1;
             store_row_hilo128(sm + OFF_S, i, S);     // Q S of this chunk is done (QSD above)
             fence_async_smem();
             tc_fence_before();
             named_sync(1, 128);                 // the new state operand is complete
             if (lead) mbar_arrive(&bars[B_EMPTYB0 + st]);   // (with the P U commit)
-            if (cc + 1 < nch && lane == 0 && (warp == 1 || warp == 2)) {
+            if (issue_next && lane == 0 && (warp == 1 || warp == 2)) {
                 issue_ws(warp, cc + 1);
                 issued = true;
             }
             __syncwarp();
-            if (STATES) {
-                // the state after the chunk's last token is the carried chunk-form state
-                float *dst = p.states + ((size_t)(tok0 + len - 1) * p.HV + h) * (D * D) + (size_t)i * D +
-                             (size_t)vs * NV;
-                if (states32) {
+            if (STATES)
+                state_out(p.states + ((size_t)(tok0 + len - 1) * p.HV + hh) * (D * D) + (size_t)i * D +
+                          (size_t)vv * NV);
+            return 0;
+        };
+        if constexpr (!UNITS) {
+            const size_t sbase = (((size_t)s * p.HV + h) * D + i) * D + (size_t)vs * NV;
+            if (p.s0) {
 #pragma unroll
-                    for (int q = 0; q < NV / 8; ++q) st_v8(dst + 8 * q, S + 8 * q);
-                } else {
+                for (int q = 0; q < NV / 4; ++q) {
+                    const float4 v4 = reinterpret_cast<const float4 *>(p.s0 + sbase)[q];
+                    S[4 * q] = v4.x; S[4 * q + 1] = v4.y; S[4 * q + 2] = v4.z; S[4 * q + 3] = v4.w;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < NV; ++q) S[q] = 0.f;
+            }
+            store_row_hilo128(sm + OFF_S, i, S);
+            fence_async_smem();
+            named_sync(1, 128);
+            int nch_run = nch;
+            if (nch > 0) {
+                if (!wg_wait4(B_FULLA0, 0, -1, 0, -1, 0, -1, 0)) nch_run = 0;
+                else if (lane == 0 && (warp == 1 || warp == 2)) {
+                    issue_ws(warp, 0);
+                    issued = true;
+                }
+                __syncwarp();
+            }
+            for (int cc = 0; cc < nch_run; ++cc) {
+                const int64_t tok0 = sr.t0 + (int64_t)cc * C;
+                const int len = (int)min((int64_t)C, sr.t_end - tok0);
+                if (chunk(cc, tok0, len, h, vs, cc + 1 < nch, false, cc + 1 < nch) < 0) break;
+            }
+            if (lane == 0) {
+                if (issued) mma_commit(&bars[B_DRAIN]);
+                else mbar_arrive(&bars[B_DRAIN]);
+            }
+            // final state slice (with per-token states, a later kernel copies it from the last
+            // token's state once nothing reads the initial state any more: they may alias)
+            if (!STATES && !*s_err) {
+#pragma unroll
+                for (int q = 0; q < NV / 4; ++q)
+                    reinterpret_cast<float4 *>(p.s_final + sbase)[q] =
+                        make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+            }
+        } else {
+            // ring A of the first chunk: its descriptor says what the stream holds
+            bool run = wg_wait4(B_FULLA0, 0, -1, 0, -1, 0, -1, 0);
+            int cc = 0;
+            while (run) {
+                // ---- the start of a unit (chunk cc, whose ring A has been seen armed): its
+                // state, then -W S of its first chunk; the previous unit's end state is
+                // published once that is on its way (or before any wait for another CTA)
+                const int32_t *d0 = desc(cc);
+                if ((d0[DW_LEN] & (DF_STOP << 8)) || !unit_state(d0)) break;
+                if (lane == 0 && (warp == 1 || warp == 2)) {
+                    issue_ws(warp, cc);
+                    issued = true;
+                }
+                __syncwarp();
+                if (pend) { flag_release(pend, pend_v); pend = nullptr; }
+                // ---- the chunks of the unit (its descriptors stay in place for the whole
+                // chunk: slot cc % 4 is rewritten for chunk cc + 4, after E1 of chunk cc + 2);
+                // the last one returns after its state update
+                int r;
+                for (;; ++cc) {
+                    const int32_t *dc = desc(cc);
+                    const int dl = dc[DW_LEN];
+                    r = chunk(cc, dc[DW_TOK], dl & 255, dc[DW_HEAD], dc[DW_SLICE], true, (dl >> 8) & DF_LAST, true);
+                    if (r != 0) break;
+                }
+                if (r < 0) break;                   // a wait gave up
+                // ---- the end of the unit (chunk cc): its end state goes out (the slot of
+                // its last token, or the final-state slice: the final state, or the start of
+                // the chain's next segment); then every thread's row is out and its reads of
+                // ring B are done.  Ring A of chunk cc + 1 was seen in E2 of chunk cc.
+                const int32_t *de = desc(cc);
+                if (STATES)
+                    state_out(p.states + ((size_t)(de[DW_TOK] + (de[DW_LEN] & 255) - 1) * p.HV + de[DW_HEAD]) *
+                                             (D * D) + (size_t)i * D + (size_t)de[DW_SLICE] * NV);
+                else {
 #pragma unroll
                     for (int q = 0; q < NV / 4; ++q)
-                        reinterpret_cast<float4 *>(dst)[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2],
-                                                                         S[4 * q + 3]);
+                        reinterpret_cast<float4 *>(p.s_final + slice_row(de[DW_CHAIN]))[q] =
+                            make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
                 }
+                named_sync(1, 128);
+                if (lead) mbar_arrive(&bars[B_EMPTYB0 + (cc & 1)]);
+                if (lead && !(de[DW_LEN] & (DF_END << 8))) {
+                    pend = p.chain_flags + de[DW_CHAIN];
+                    pend_v = de[DW_SEG] + 1;
+                }
+                ++cc;
             }
-        }
-        if (lane == 0) {
-            if (issued) mma_commit(&bars[B_DRAIN]);
-            else mbar_arrive(&bars[B_DRAIN]);
-        }
-        // final state slice (with per-token states, a later kernel copies it from the last
-        // token's state once nothing reads the initial state any more: they may alias)
-        if (!STATES && !*s_err) {
-#pragma unroll
-            for (int q = 0; q < NV / 4; ++q)
-                reinterpret_cast<float4 *>(p.s_final + sbase)[q] =
-                    make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+            if (lead && pend) flag_release(pend, pend_v);
+            if (lead && !*s_err) mbar_arrive(&bars[B_E1DONE]);   // the end of the stream, for warp 4
+            if (lane == 0) {
+                if (issued) mma_commit(&bars[B_DRAIN]);
+                else mbar_arrive(&bars[B_DRAIN]);
+            }
         }
         if (lead) mbar_wait(&bars[B_DRAIN], 0);   // every MMA of the CTA has finished
     }
@@ -1416,6 +1730,47 @@ static bool make_map(CUtensorMap *m, const void *base, int heads, int64_t T_tota
 
 }  // namespace tc
 
+namespace tc {
+
+struct ChainPlan {
+    int n_chains, seg_len, n_units, grid;
+};
+
+// The work-unit stream of an equal-length batch: while its chains fit on the SMs, one
+// unit per chain (and the fixed-chain kernel runs instead); otherwise segments of seg_len
+// chunks, chosen to minimise the estimated makespan ceil(units / SMs) * (seg_len +
+// kUnitCost) in chunk periods, kUnitCost standing for the hand-off of a segment's state
+// between CTAs; one CTA per SM at most (its shared memory and TMEM allow no more).
+constexpr double kUnitCost = 0.5;
+
+static ChainPlan plan_chain(const PrefillParams &pp, int n_sm) {
+    ChainPlan c;
+    c.n_chains = pp.N * pp.HV * (D / NV);
+    if (n_sm < 1) n_sm = 1;
+    const int n = (pp.T_seq + C - 1) / C;
+    c.seg_len = n > 0 ? n : 1;
+    if (n > 1 && c.n_chains > n_sm) {
+        double best = -1.0;
+        for (int r = 1; r <= n; ++r) {
+            const int L = (n + r - 1) / r;
+            if (r > 1 && L == (n + r - 2) / (r - 1)) continue;   // the same segment length
+            const int rr = (n + L - 1) / L;
+            const double waves = ((double)c.n_chains * rr + n_sm - 1) / n_sm;
+            const double cost = (double)(int64_t)waves * (L + kUnitCost);
+            if (best < 0.0 || cost < best) {
+                best = cost;
+                c.seg_len = L;
+            }
+        }
+    }
+    c.n_units = n > 0 ? c.n_chains * ((n + c.seg_len - 1) / c.seg_len) : 0;
+    c.grid = c.n_units < n_sm ? c.n_units : n_sm;
+    if (c.grid < 1) c.grid = 1;
+    return c;
+}
+
+}  // namespace tc
+
 size_t tc_record_bytes() { return (size_t)tc::kRecBytes; }
 
 bool tc_supported(int Dk, int Dv, gdn_dtype dtype) {
@@ -1430,9 +1785,12 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     if (pp.cu_seqlens) {
         if ((e = launch_chunk_table(pp, st)) != cudaSuccess) return e;
     } else {
-        // both kernels only ever move the status word from GDN_OK to an error code, so it
-        // starts clean here (a reused workspace may hold the last call's error)
-        if ((e = cudaMemsetAsync(pp.status, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return e;
+        // the kernels only ever move the status word from GDN_OK to an error code, so it
+        // starts clean here (a reused workspace may hold the last call's error), with the
+        // work-unit stream's claim counter and hand-off flags (right after the header)
+        const size_t clear = (size_t)((const char *)pp.chain_flags - (const char *)pp.status) +
+                             chain_flag_bytes(pp.N, pp.HV);
+        if ((e = cudaMemsetAsync(pp.status, 0, clear, st)) != cudaSuccess) return e;
     }
     Params p;
     memset(&p, 0, sizeof p);
@@ -1442,6 +1800,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     p.HK = pp.HK; p.HV = pp.HV; p.scale = pp.scale; p.l2norm = pp.l2norm;
     p.max_chunks = pp.max_chunks; p.status = pp.status; p.chunk_seq = pp.chunk_seq;
     p.chunk_first = pp.chunk_first; p.seq_order = pp.seq_order; p.rec = pp.rec;
+    p.chain_flags = pp.chain_flags;
     CUtensorMap mk, mq, mv;
     if (pp.T_total > 0) {
         if (!make_map(&mk, pp.k, pp.HK, pp.T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1469,7 +1828,22 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (pp.N > 0) {
-        auto kern = pp.states ? chain_kernel<true> : chain_kernel<false>;
+        // the work-unit stream only where an equal-length batch's chains are cut into
+        // segments; otherwise one CTA per chain (packed batches: longest first, in the
+        // order the hardware starts the CTAs)
+        ChainPlan plan = {0, 1, 0, 1};
+        if (!pp.cu_seqlens) {
+            int dev = 0, n_sm = 0;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+            if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+            plan = plan_chain(pp, n_sm);
+        }
+        const bool units = plan.n_units > plan.n_chains;
+        p.n_chains = plan.n_chains;
+        p.seg_len = plan.seg_len;
+        p.n_units = plan.n_units;
+        auto kern = units ? (pp.states ? chain_kernel<true, true> : chain_kernel<false, true>)
+                          : (pp.states ? chain_kernel<true, false> : chain_kernel<false, false>);
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kChainSmem)) != cudaSuccess)
             return e;
@@ -1478,7 +1852,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         // grid before the first record copy
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(D / NV, pp.HV, pp.N);
+        cfg.gridDim = units ? dim3(plan.grid) : dim3(D / NV, pp.HV, pp.N);
         cfg.blockDim = dim3(kChainThreads);
         cfg.dynamicSmemBytes = kChainSmem;
         cfg.stream = st;

@@ -136,6 +136,8 @@ def _prefill(lib, **kw):
     (dict(q=P + 4), -3), (dict(out=P + 8), -3), (dict(st=P + 2), -3),
     (dict(ws=None), -4), (dict(wsb=100), -4), (dict(ws=P + 16), -3),
     (dict(q=None), -1), (dict(fin=None), -1), (dict(scale=float("nan")), -1),
+    # (sequence, value head, value slice) chains are numbered in 32 bits
+    (dict(B=40000, T=1, HK=16000, HV=16000), -2),
 ])
 def test_prefill_rejects_bad_arguments_on_host(lib, kw, code):
     assert _prefill(lib, **kw) == code
@@ -160,7 +162,7 @@ def _noalloc(lib, **kw):
     # the fixed scratch (64 MiB) holds 1129 records of 58 KiB after its header and chunk
     # table: 32 value heads x 35 chunks of 64 tokens fit, x 36 do not
     (dict(T=128 * 64, HK=16, HV=32), -4), (dict(B=4, T=36 * 64, HK=16, HV=32), -4),
-    (dict(T=35 * 64 + 1, HK=16, HV=32), -4),
+    (dict(T=35 * 64 + 1, HK=16, HV=32), -4), (dict(B=40000, T=1, HK=16000, HV=16000), -2),
 ])
 def test_noalloc_rejects_bad_arguments_and_oversized_shapes_on_host(lib, kw, code):
     """gdn_prefill_noalloc checks its arguments and its scratch limit before it looks up
