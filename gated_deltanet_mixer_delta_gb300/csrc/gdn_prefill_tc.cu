@@ -80,6 +80,9 @@ struct Params {
     // chunks of one of the n_chains (sequence, value head, value slice) chains
     int32_t *chain_flags;        // [n_chains] segments of the chain whose end state is out
     int seg_len, n_chains, n_units;
+    int states_overlap;          // the states kernel takes each segment as the stream ends it
+    int final_direct;            // with per-token states, the stream writes the final states
+                                 // too (final_state does not alias initial_state)
 };
 
 // ------------------------------------------------------------------ shared helpers
@@ -922,6 +925,9 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the stream's dependent grid (the states kernel, which takes each segment as it is
+    // published) may be scheduled once every CTA of this grid has started
+    if constexpr (UNITS) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     auto fail = [&](void) {
         *s_err = 1;
@@ -1556,9 +1562,18 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 // the chain's next segment); then every thread's row is out and its reads of
                 // ring B are done.  Ring A of chunk cc + 1 was seen in E2 of chunk cc.
                 const int32_t *de = desc(cc);
-                if (STATES)
+                if (STATES) {
                     state_out(p.states + ((size_t)(de[DW_TOK] + (de[DW_LEN] & 255) - 1) * p.HV + de[DW_HEAD]) *
                                              (D * D) + (size_t)i * D + (size_t)de[DW_SLICE] * NV);
+                    // the chain's final state, when nothing later reads the initial state
+                    // through the same buffer
+                    if (p.final_direct && (de[DW_LEN] & (DF_END << 8))) {
+#pragma unroll
+                        for (int q = 0; q < NV / 4; ++q)
+                            reinterpret_cast<float4 *>(p.s_final + slice_row(de[DW_CHAIN]))[q] =
+                                make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+                    }
+                }
                 else {
 #pragma unroll
                     for (int q = 0; q < NV / 4; ++q)
@@ -1567,7 +1582,8 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 }
                 named_sync(1, 128);
                 if (lead) mbar_arrive(&bars[B_EMPTYB0 + (cc & 1)]);
-                if (lead && !(de[DW_LEN] & (DF_END << 8))) {
+                // (with per-token states also a chain's last segment: the states kernel waits)
+                if (lead && (STATES || !(de[DW_LEN] & (DF_END << 8)))) {
                     pend = p.chain_flags + de[DW_CHAIN];
                     pend_v = de[DW_SEG] + 1;
                 }
@@ -1604,8 +1620,33 @@ states_kernel(Params p) {
     __shared__ float sF[C][D];                    // rk_t k_t[i]
     __shared__ __align__(16) float sU[C][NV];     // u_t, this slice's columns
     __shared__ float sAl[C];                      // alpha_t
+    __shared__ int s_ok;
+    // beside the chain's work-unit stream, the last CTA (started last) waits for the whole
+    // stream grid first: this grid then ends only after it, so later work in the stream
+    // finds every output and state in place
+    if (p.states_overlap && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (p.status[kStatusWord] != GDN_OK) return;
-    const int m = blockIdx.x, h = blockIdx.y, vs = blockIdx.z;
+    int m = blockIdx.x, h = blockIdx.y, vs = blockIdx.z;
+    if (p.states_overlap) {
+        // running beside the chain's work-unit stream: CTAs in the order the stream ends
+        // its segments (segment-major, then chain, then chunk); each waits until the
+        // segment holding its chunk is published (its U rows and the carried state before
+        // it are then in the states tensor)
+        const int cps = (p.T_seq + C - 1) / C, L = p.seg_len;
+        const int q = blockIdx.x, per_seg = p.n_chains * L;
+        const int seg = q / per_seg, rem = q - seg * per_seg;
+        const int chain = rem / L, cc0 = seg * L + (rem - (rem / L) * L);
+        if (cc0 >= cps) return;
+        vs = chain % (D / NV);
+        h = (chain / (D / NV)) % p.HV;
+        m = (chain / (D / NV) / p.HV) * cps + cc0;
+        if (threadIdx.x == 0) {
+            s_ok = flag_wait(p.chain_flags + chain, seg + 1);
+            if (!s_ok) set_error(p, GDN_ERR_TIMEOUT);
+        }
+        __syncthreads();
+        if (!s_ok) return;
+    }
     int cc;
     int64_t t0;
     int len;
@@ -1629,6 +1670,9 @@ states_kernel(Params p) {
     const int j = h / (p.HV / p.HK);
     const int tid = threadIdx.x;
     const size_t slot = (size_t)D * D;            // floats per (token, value head)
+    // the chunk's factor rows (written by the prep grid: complete and visible once the
+    // chain, which waited for it before its first record, published the segment) and its
+    // U rows (this slice's columns)
     const float *F = reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(p.rec) +
                                                      ((size_t)m * p.HV + h) * kRecBytes + REC_F);
     const float *park = p.states + ((size_t)t0 * p.HV + h) * slot + (size_t)vs * NV;
@@ -1743,6 +1787,26 @@ struct ChainPlan {
 // between CTAs; one CTA per SM at most (its shared memory and TMEM allow no more).
 constexpr double kUnitCost = 0.5;
 
+// Beside the states kernel (per-token states of an equal-length batch): segments of
+// kOverlapSeg chunks, so that the first states CTAs find work early, and about a sixth of
+// the SMs for the stream.  A stream CTA ends a chunk per ~2.5 us; a states CTA writes a
+// chunk's states (1 MiB a 32-wide slice) in ~100 us, five to an SM, so ~17 stream CTAs keep
+// 135 SMs of states CTAs busy; more take SMs from the writes the call is bound by (measured
+// at B = 4, T = 1024: 16 CTAs starve the writes, 25 give 90.7% of HBM, 38 give 87.5%).
+constexpr int kOverlapSeg = 4;
+
+static ChainPlan plan_overlap(const PrefillParams &pp, int n_sm) {
+    ChainPlan c;
+    c.n_chains = pp.N * pp.HV * (D / NV);
+    const int n = (pp.T_seq + C - 1) / C;
+    c.seg_len = n < kOverlapSeg ? (n > 0 ? n : 1) : kOverlapSeg;
+    c.n_units = n > 0 ? c.n_chains * ((n + c.seg_len - 1) / c.seg_len) : 0;
+    const int g = (n_sm + 5) / 6;
+    c.grid = c.n_units < g ? c.n_units : g;
+    if (c.grid < 1) c.grid = 1;
+    return c;
+}
+
 static ChainPlan plan_chain(const PrefillParams &pp, int n_sm) {
     ChainPlan c;
     c.n_chains = pp.N * pp.HV * (D / NV);
@@ -1831,17 +1895,23 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         // the work-unit stream only where an equal-length batch's chains are cut into
         // segments; otherwise one CTA per chain (packed batches: longest first, in the
         // order the hardware starts the CTAs)
+        // With per-token states (equal-length batches) the stream runs on half the SMs and
+        // the states kernel beside it on the other half, taking each segment as the stream
+        // publishes it: the states are bound by HBM writes, the stream by its latency.
+        const bool overlap = pp.states && !pp.cu_seqlens && pp.max_chunks > 0;
         ChainPlan plan = {0, 1, 0, 1};
         if (!pp.cu_seqlens) {
             int dev = 0, n_sm = 0;
             if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
             if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-            plan = plan_chain(pp, n_sm);
+            plan = overlap ? plan_overlap(pp, n_sm) : plan_chain(pp, n_sm);
         }
-        const bool units = plan.n_units > plan.n_chains;
+        const bool units = overlap || plan.n_units > plan.n_chains;
         p.n_chains = plan.n_chains;
         p.seg_len = plan.seg_len;
         p.n_units = plan.n_units;
+        p.states_overlap = overlap ? 1 : 0;
+        p.final_direct = overlap && pp.s_final != pp.s0 ? 1 : 0;
         auto kern = units ? (pp.states ? chain_kernel<true, true> : chain_kernel<false, true>)
                           : (pp.states ? chain_kernel<true, false> : chain_kernel<false, false>);
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1863,12 +1933,31 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         cfg.numAttrs = 1;
         if ((e = cudaLaunchKernelEx(&cfg, kern, mk, mq, mv, p)) != cudaSuccess) return e;
         if (pp.states) {
-            if (pp.max_chunks > 0) {
+            if (overlap) {
+                // a programmatic dependent of the stream: its CTAs start once every stream
+                // CTA has, on the SMs the stream leaves free
+                const int n = (pp.T_seq + C - 1) / C;
+                const int64_t ctas = (int64_t)((n + plan.seg_len - 1) / plan.seg_len) * plan.n_chains * plan.seg_len;
+                if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+                cudaLaunchConfig_t sc;
+                memset(&sc, 0, sizeof sc);
+                sc.gridDim = dim3((unsigned)ctas);
+                sc.blockDim = dim3(kStThreads);
+                sc.stream = st;
+                cudaLaunchAttribute sa[1];
+                sa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                sa[0].val.programmaticStreamSerializationAllowed = 1;
+                sc.attrs = sa;
+                sc.numAttrs = 1;
+                if ((e = cudaLaunchKernelEx(&sc, states_kernel, p)) != cudaSuccess) return e;
+            } else if (pp.max_chunks > 0) {
                 states_kernel<<<dim3(pp.max_chunks, pp.HV, D / NV), kStThreads, 0, st>>>(p);
                 if ((e = cudaGetLastError()) != cudaSuccess) return e;
             }
-            final_from_states_kernel<<<dim3(pp.HV, pp.N), 256, 0, st>>>(p);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if (!p.final_direct) {
+                final_from_states_kernel<<<dim3(pp.HV, pp.N), 256, 0, st>>>(p);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
         }
     }
     return cudaSuccess;
