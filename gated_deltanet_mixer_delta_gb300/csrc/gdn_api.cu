@@ -17,8 +17,8 @@ int max_chunks_for(int64_t T_total, int n_seqs, bool packed, int T_seq) {
     return (int)((T_total + kChunk - 1) / kChunk + n_seqs);
 }
 
-// header | chain flags[N*HV*kChainSlices] | chunk_seq[max_chunks] | chunk_first[N+1] |
-// seq_order[N] | records[max_chunks][HV]
+// header | chain flags[N*HV*kChainSlices] | ready flags[max_chunks][HV] |
+// chunk_seq[max_chunks] | chunk_first[N+1] | seq_order[N] | records[max_chunks][HV]
 static size_t table_bytes(int max_chunks, int n_seqs) {
     return round_up(sizeof(int32_t) * ((size_t)max_chunks + 2 * (size_t)n_seqs + 1), 256);
 }
@@ -32,7 +32,7 @@ static size_t record_bytes_for(int Dk, int Dv, gdn_dtype dtype) {
 size_t prefill_workspace_bytes_for(int64_t T_total, int n_seqs, int HV, int Dk, int Dv, gdn_dtype dtype) {
     // sized for the packed bound, which also covers equal-length batches
     const int mc = max_chunks_for(T_total, n_seqs, true, 0);
-    return kWsHeader + chain_flag_bytes(n_seqs, HV) + table_bytes(mc, n_seqs) +
+    return kWsHeader + chain_flag_bytes(n_seqs, HV) + ready_flag_bytes(mc, HV) + table_bytes(mc, n_seqs) +
            (size_t)mc * HV * record_bytes_for(Dk, Dv, dtype);
 }
 
@@ -103,9 +103,10 @@ int prefill_common(const void *queries, const void *keys, const void *values,
     p.scale = resolve_scale(scale, Dk);
     p.l2norm = use_qk_l2norm ? 1 : 0;
     p.max_chunks = mc;
-    const size_t flag_bytes = chain_flag_bytes(N, HV);
+    const size_t flag_bytes = chain_flag_bytes(N, HV) + ready_flag_bytes(mc, HV);
     p.status = (int32_t *)ws;
     p.chain_flags = (int32_t *)(ws + kWsHeader);
+    p.ready = (int32_t *)(ws + kWsHeader + chain_flag_bytes(N, HV));
     p.chunk_seq = (int32_t *)(ws + kWsHeader + flag_bytes);
     p.chunk_first = p.chunk_seq + mc;
     p.seq_order = p.chunk_first + N + 1;

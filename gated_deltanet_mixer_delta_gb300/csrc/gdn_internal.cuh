@@ -16,14 +16,23 @@ constexpr float kL2Eps = 1e-6f;       // l2norm(x) = x / sqrt(sum x^2 + eps)
 // Workspace header: status words, then one flag word per chain of the tensor-core path,
 // then the chunk table of a packed batch.
 constexpr size_t kWsHeader = 256;     // int32 status[64]: [0] status, [1] number of chunks,
-                                      // [2] work units claimed by the chain kernel
-enum { kStatusWord = 0, kChunkCountWord = 1, kClaimWord = 2 };
+                                      // [2] work units claimed by the chain kernel, [3] prep
+                                      // items claimed below the limit, [4] prep CTAs that stay
+                                      // beside the chain, [5] prep items claimed past the limit
+enum { kStatusWord = 0, kChunkCountWord = 1, kClaimWord = 2, kPrepClaimWord = 3, kPrepStayWord = 4,
+       kPrepClaimPastWord = 5 };
 // value slices per (sequence, value head) chain of the tensor-core prefill
 constexpr int kChainSlices = 4;
 // bytes of the chain flag words (one per (sequence, value head, value slice)), 256-aligned;
 // zero before the chain kernel runs, like the status words
 inline size_t chain_flag_bytes(int n_seqs, int HV) {
     return ((size_t)n_seqs * HV * kChainSlices * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+// bytes of the record-ready flags (one per (chunk, value head)), 256-aligned: with the
+// prep running beside the chain, the chain takes a record once its flag is set
+inline size_t ready_flag_bytes(int max_chunks, int HV) {
+    return ((size_t)max_chunks * HV * sizeof(int32_t) + 255) / 256 * 256;
 }
 
 // Everything a prefill launch needs; passed by value to the kernels.
@@ -46,6 +55,7 @@ struct PrefillParams {
     int32_t *chunk_first;         // [N + 1] first chunk of each sequence (packed batches)
     int32_t *seq_order;           // [N] sequences by decreasing chunk count (packed batches)
     int32_t *chain_flags;         // [N * HV * kChainSlices] (tensor-core chain hand-offs)
+    int32_t *ready;               // [max_chunks * HV] record-ready flags (tensor-core path)
     float *rec;                   // per (chunk, value head) records of the prep pass
     size_t rec_floats;            // floats per record
 };

@@ -73,7 +73,7 @@ extern "C" int gdn_prefill_noalloc(const void *queries, const void *keys, const 
     const bool tc = tc_supported(Dk, Dv, dtype);
     const size_t rec_bytes = tc ? tc_record_bytes() : record_floats(Dk, Dv) * sizeof(float);
     const size_t table = round256(sizeof(int32_t) * ((size_t)mc + B + 1));
-    const size_t flag_bytes = chain_flag_bytes(B, HV);
+    const size_t flag_bytes = chain_flag_bytes(B, HV) + ready_flag_bytes(mc, HV);
     const size_t need = kWsHeader + flag_bytes + table + (size_t)mc * HV * rec_bytes;
     if (need > kScratchBytes) return GDN_ERR_WORKSPACE;     // beyond the fixed maximum
 
@@ -98,6 +98,7 @@ extern "C" int gdn_prefill_noalloc(const void *queries, const void *keys, const 
     p.max_chunks = mc;
     p.status = (int32_t *)ws;
     p.chain_flags = (int32_t *)(ws + kWsHeader);
+    p.ready = (int32_t *)(ws + kWsHeader + chain_flag_bytes(B, HV));
     p.chunk_seq = (int32_t *)(ws + kWsHeader + flag_bytes);
     p.chunk_first = p.chunk_seq + mc;
     p.rec = (float *)(ws + kWsHeader + flag_bytes + table);

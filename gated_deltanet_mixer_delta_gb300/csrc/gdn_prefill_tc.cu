@@ -83,6 +83,11 @@ struct Params {
     int states_overlap;          // the states kernel takes each segment as the stream ends it
     int final_direct;            // with per-token states, the stream writes the final states
                                  // too (final_state does not alias initial_state)
+    // prep beside the chain: prep_items > 0 makes the prep grid persistent over that many
+    // items; CTAs on SMs below prep_stay_sms keep claiming after prep_limit items, and
+    // every record's flag in ready is set once the record is complete
+    int32_t *ready;              // [chunks][HV] or null (the chain waits for the prep grid)
+    int prep_items, prep_limit, prep_stay_sms;
 };
 
 // ------------------------------------------------------------------ shared helpers
@@ -183,6 +188,7 @@ __device__ __forceinline__ void store_half_row_bf16(uint8_t *img, int row, int c
 //   rk, rq | per head: G, G log2(e), beta, beta gamma rk | barriers
 // After the last product the key and query tiles stage -W of the last head.
 constexpr int kPrepThreads = 128;
+constexpr int kPrepPerSm = 3;                                // CTAs per SM (launch bounds)
 constexpr int LDA = C + 4;
 constexpr int LDX = 36;                                      // X scratch rows (32 columns used)
 constexpr int kXHead = 2 * 16 * LDX;                         // == 32 * LDX floats per head
@@ -192,6 +198,7 @@ constexpr size_t prep_smem_bytes() {
     return 1024 /*align*/ + 32768 + (size_t)HPC * C * LDA * 4 +
            (size_t)(2 + HPC * kPrepVecHead) * C * 4 + 64;
 }
+static_assert(5 * 8 + 5 * 4 <= 64, "barriers, TMEM slot, item, pending item and ticket words");
 static_assert(2 * kXHead * 4 <= 16384, "solve scratch of two heads fits the query tile");
 static_assert(2 * C * LDA * 4 >= 32768 && C * LDA * 4 >= 16384, "A/T tiles stage the images");
 static_assert(REC_T2LO == REC_T2HI + 8192 && REC_WLO == REC_WHI + 16384, "record layout");
@@ -343,8 +350,88 @@ __device__ __forceinline__ void stage_minus_w(uint32_t taddr, uint8_t *img, int 
     }
 }
 
+// Persistent prep (beside the chain kernel): a work item is a (chunk, value-head group).
+// Items below p.prep_limit are handed out by one counter in the workspace header, the rest
+// by a second one.  Every CTA takes items from the first; once it runs dry, a CTA on an SM
+// whose index is below p.prep_stay_sms goes on with the second until no item is left, while
+// the others leave, which frees their SMs for the chain's CTAs.  A CTA leaves only once some
+// staying CTA has registered, so every item is always taken.  Plain atomic increments (a
+// compare-and-swap loop starved the CTAs that lost its races for the whole grid).
+// Where a prep item's chunk lies: the item number of the persistent prep (items chunk-major:
+// the first chunk of every sequence and head group, then the second, ...; equal-length
+// batches), else the CTA's grid position.  False for a chunk past the batch's end (a packed
+// batch's chunk table may hold fewer chunks than the grid) or after a bad chunk table.
+struct PrepChunk {
+    int c, h0, len;
+    int64_t t0;
+};
 template <int HPC>
-__global__ void __launch_bounds__(kPrepThreads, 3)
+__device__ __forceinline__ bool prep_chunk(const Params &p, bool persist, int item, PrepChunk &w) {
+    if (persist) {
+        const int ny = p.HV / HPC, per = p.N * ny;
+        const int local = item / per, r = item - local * per, sq = r / ny;
+        w.c = sq * ((p.T_seq + C - 1) / C) + local;
+        w.h0 = (r - sq * ny) * HPC;
+    } else {
+        w.c = blockIdx.x;
+        w.h0 = blockIdx.y * HPC;
+    }
+    if (p.cu_seqlens) {
+        if (p.status[kStatusWord] != GDN_OK || w.c >= p.status[kChunkCountWord]) return false;
+        const int s = p.chunk_seq[w.c];
+        w.t0 = p.cu_seqlens[s] + (int64_t)(w.c - p.chunk_first[s]) * C;
+        w.len = (int)min((int64_t)C, (int64_t)p.cu_seqlens[s + 1] - w.t0);
+    } else {
+        const int cps = (p.T_seq + C - 1) / C;
+        if (cps == 0 || w.c >= p.N * cps) return false;
+        const int s = w.c / cps, local = w.c - s * cps;
+        w.t0 = (int64_t)s * p.T_seq + (int64_t)local * C;
+        w.len = min(C, p.T_seq - local * C);
+    }
+    return true;
+}
+
+// The key and query tiles of a chunk (key head j) into the prep's tiles, completing bar.
+__device__ __forceinline__ void prep_load_tiles(const CUtensorMap *mapK, const CUtensorMap *mapQ, uint8_t *sK,
+                                                uint8_t *sQ, uint64_t *bar, int j, int64_t t0) {
+    mbar_arrive_expect_tx(bar, 32768);
+    tma_load_3d(sK, mapK, bar, 0, j, (int)t0);
+    tma_load_3d(sK + 8192, mapK, bar, 64, j, (int)t0);
+    tma_load_3d(sQ, mapQ, bar, 0, j, (int)t0);
+    tma_load_3d(sQ + 8192, mapQ, bar, 64, j, (int)t0);
+}
+
+// An item is claimed in two steps, so that the atomic's round trip overlaps the item
+// before: a ticket from the first counter, then the item it stands for.
+__device__ __forceinline__ int prep_ticket(const Params &p) {
+    return atomicAdd(&p.status[kPrepClaimWord], 1);
+}
+__device__ __forceinline__ int prep_item(const Params &p, int ticket, bool stay) {
+    if (ticket < p.prep_limit) return ticket;
+    if (!stay && *reinterpret_cast<volatile int32_t *>(&p.status[kPrepStayWord]) > 0) return -1;
+    if (*reinterpret_cast<volatile int32_t *>(&p.status[kPrepClaimPastWord]) >= p.prep_items - p.prep_limit)
+        return -1;
+    const int k = p.prep_limit + atomicAdd(&p.status[kPrepClaimPastWord], 1);
+    return k < p.prep_items ? k : -1;
+}
+
+// Sets the ready flags of the HPC records of item (c, h0) once its bulk stores are complete
+// in global memory (the factor rows the other threads stored came before a CTA barrier).
+template <int HPC>
+__device__ __forceinline__ void prep_publish(const Params &p, int c, int h0) {
+    bulk_wait_all();
+    fence_async_global();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < HPC; ++i)
+        asm volatile("st.relaxed.gpu.global.s32 [%0], 1;" ::"l"(p.ready + (size_t)c * p.HV + h0 + i) : "memory");
+}
+
+// PERSIST == false: one CTA per item, launched as a (chunk, head group) grid.  PERSIST ==
+// true: the persistent prep beside the chain (items claimed in chunk order, records'
+// ready flags set).  Each schedule compiles only its own loop code.
+template <int HPC, bool PERSIST>
+__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm)
 prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
             Params p) {
     static_assert(HPC == 1 || HPC == 2, "one or two value heads per CTA");
@@ -362,6 +449,11 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     float *sV = sRq + C;                                // [HPC][4][64] per-head vectors
     uint64_t *bar = reinterpret_cast<uint64_t *>(sV + HPC * kPrepVecHead * C);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    volatile int *s_item = reinterpret_cast<volatile int *>(tslot + 1);
+    // thread 0's bookkeeping of the persistent prep (kept out of registers): the item whose
+    // records are written but whose flags are not yet set (chunk, first value head; chunk -1
+    // for none), and the ticket of the next item
+    volatile int *s_pend = s_item + 1, *s_ticket = s_item + 3;
     // per-head vectors: decay prefix (natural log), the same times log2(e), beta,
     // beta gamma rk (0 past the chunk end)
     auto vG = [&](int i) { return sV + (i * kPrepVecHead + 0) * C; };
@@ -369,313 +461,359 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
     auto vB = [&](int i) { return sV + (i * kPrepVecHead + 2) * C; };
     auto vC1 = [&](int i) { return sV + (i * kPrepVecHead + 3) * C; };
 
-    // the chain kernel may be scheduled as soon as every prep CTA has started; it waits for
-    // this grid's completion before it reads a record
+    // the chain kernel may be scheduled as soon as every prep CTA has started; it takes a
+    // record once its ready flag is set (persistent prep), or after this grid completes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int c = blockIdx.x, h0 = blockIdx.y * HPC;
-    const int j = h0 / (p.HV / p.HK);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // chunk -> (sequence, first token, length)
-    int64_t t0;
-    int len;
-    if (p.cu_seqlens) {
-        if (p.status[kStatusWord] != GDN_OK || c >= p.status[kChunkCountWord]) return;
-        const int s = p.chunk_seq[c];
-        t0 = p.cu_seqlens[s] + (int64_t)(c - p.chunk_first[s]) * C;
-        len = (int)min((int64_t)C, (int64_t)p.cu_seqlens[s + 1] - t0);
-    } else {
-        const int cps = (p.T_seq + C - 1) / C;
-        if (cps == 0 || c >= p.N * cps) return;
-        const int s = c / cps, local = c - s * cps;
-        t0 = (int64_t)s * p.T_seq + (int64_t)local * C;
-        len = min(C, p.T_seq - local * C);
+    const bool stay = PERSIST && sm_id() < (uint32_t)p.prep_stay_sms;
+    PrepChunk w;
+    if constexpr (!PERSIST) {
+        if (!prep_chunk<HPC>(p, false, 0, w)) return;
     }
-    auto record = [&](int i) {
-        return reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h0 + i) * kRecBytes;
-    };
-
+    // thread 0 starts the tile loads of an item as early as it can: the first item's at once,
+    // (persistent prep) each later one's as soon as the item before has left the tiles; the
+    // persistent prep sets an item's flags while the next item's tiles load, and takes the
+    // next item's ticket before the current one ends
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(&bar[b], 1);
         fence_mbar_init();
         prefetch_tensormap(&mapK);
         prefetch_tensormap(&mapQ);
-        mbar_arrive_expect_tx(&bar[0], 32768);
-        tma_load_3d(sK, &mapK, &bar[0], 0, j, (int)t0);
-        tma_load_3d(sK + 8192, &mapK, &bar[0], 64, j, (int)t0);
-        tma_load_3d(sQ, &mapQ, &bar[0], 0, j, (int)t0);
-        tma_load_3d(sQ + 8192, &mapQ, &bar[0], 64, j, (int)t0);
+        if constexpr (PERSIST) {
+            if (stay) atomicAdd(&p.status[kPrepStayWord], 1);
+            s_pend[0] = -1;
+            const int first = prep_item(p, prep_ticket(p), stay);
+            PrepChunk w1;
+            if (first >= 0 && prep_chunk<HPC>(p, true, first, w1)) {
+                prep_load_tiles(&mapK, &mapQ, sK, sQ, &bar[0], w1.h0 / (p.HV / p.HK), w1.t0);
+                *s_item = first;
+            } else {
+                *s_item = -1;
+            }
+        } else {
+            prep_load_tiles(&mapK, &mapQ, sK, sQ, &bar[0], w.h0 / (p.HV / p.HK), w.t0);
+        }
     }
     if (warp == 0) { tmem_alloc(tslot, kPrepTmemCols); tmem_relinquish(); }
-    // gate thread (head gh, token gt): its gate and beta are requested before anything
-    // waits, and it scans the decay prefix of its head (two warps per head)
-    const int gh = tid >> 6, gt = tid & 63;
-    const bool gthr = gh < HPC;
-    const bool gin = gthr && gt < len;
-    float g_in = 0.f, b_in = 0.f;
-    if (gin) {
-        const size_t gi = (size_t)(t0 + gt) * p.HV + h0 + gh;
-        g_in = p.g[gi];
-        b_in = p.beta[gi];
-    }
-    float Gx = g_in;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, Gx, o);
-        if (lane >= o) Gx += y;
-    }
-    if (gthr) vG(gh)[gt] = Gx;                          // inclusive within the warp
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t lb = (uint32_t)(warp * 32) << 16;    // this warp's TMEM lanes
-    const int trow = warp * 16 + (lane & 15), tcb = lane >> 4;   // row / column half of
-                                                                  // the M = 64 results
-    const int hrow = tid >> 1, hhalf = tid & 1;         // row / column half, 2 threads a row
-    float gr[32], qk[32];                               // Gram and Q K^T: row trow, 32 columns
+    if constexpr (PERSIST) __syncthreads();             // the first item, claimed by thread 0
     bool ok = true;
-
-    if (gthr) {
-        if (gt >= 32) {
-            Gx += vG(gh)[31];
-            vG(gh)[gt] = Gx;
+    uint32_t par = 0;                                   // parity of every barrier's phase
+    for (;;) {
+        // the item (its tiles are on their way); every thread finds its chunk
+        if constexpr (PERSIST) {
+            if (*s_item < 0 || !prep_chunk<HPC>(p, true, *s_item, w)) break;
         }
-        vG2(gh)[gt] = Gx * kLog2e;
-        vB(gh)[gt] = b_in;
-    }
-    ok = mbar_wait(&bar[0], 0);
-    if (__syncthreads_or(!ok)) goto teardown;
-    tc_fence_after();
-    if (lane == 0 && warp < 2) {
-        // Gram K K^T into columns 0-63 (thread 0), Q K^T into columns 64-127 (thread 32);
-        // M = N = 64, K = 128
-        const uint32_t idesc = instr_desc(64, 64, kFmtBF16, 0, 0);
-        const uint8_t *aop = warp ? sQ : sK;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t o = (ks >> 2) * 8192 + (ks & 3) * 32;
-            mma_bf16(tmem + warp * 64, smem_desc(smem_u32(aop + o), 16, 1024, kSwizzle128B),
-                     smem_desc(smem_u32(sK + o), 16, 1024, kSwizzle128B), idesc, ks > 0);
-        }
-        mma_commit(&bar[1 + 2 * warp]);
-    }
-    // query normalisers: two threads per row; the 16-byte chunks are visited in an order
-    // that keeps the eight lanes of a quarter-warp on distinct banks
-    {
-        const uint8_t *src = sQ + hhalf * 8192 + hrow * 128;
-        float ss = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int pc = q ^ (hrow & 7) ^ (hhalf * 4);
-            const uint4 w4 = *reinterpret_cast<const uint4 *>(src + pc * 16);
-            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(b2[e]);
-                ss += f.x * f.x + f.y * f.y;
+        const int c = w.c, h0 = w.h0, len = w.len;
+        const int64_t t0 = w.t0;
+        auto record = [&](int i) {
+            return reinterpret_cast<uint8_t *>(p.rec) + ((size_t)c * p.HV + h0 + i) * kRecBytes;
+        };
+        {
+            // gate thread (head gh, token gt): its gate and beta are requested before anything
+            // waits, and it scans the decay prefix of its head (two warps per head)
+            const int gh = tid >> 6, gt = tid & 63;
+            const bool gthr = gh < HPC;
+            const bool gin = gthr && gt < len;
+            float g_in = 0.f, b_in = 0.f;
+            if (gin) {
+                const size_t gi = (size_t)(t0 + gt) * p.HV + h0 + gh;
+                g_in = p.g[gi];
+                b_in = p.beta[gi];
             }
-        }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (hhalf == 0) sRq[hrow] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
-    }
-    ok = mbar_wait(&bar[1], 0) && mbar_wait(&bar[3], 0);
-    if (__syncthreads_or(!ok)) goto teardown;
-    tc_fence_after();
-    // Gram and Q K^T rows into registers; the key normaliser from the Gram diagonal
-    tmem_row_split(tmem + lb, gr);
-    tmem_row_split(tmem + lb + 64, qk);
-    {
-        float diag = 0.f;
+            float Gx = g_in;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) diag = (tcb * 32 + q == trow) ? gr[q] : diag;
-        if ((trow >> 5) == tcb) sRk[trow] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (gthr) vC1(gh)[gt] = gin ? b_in * expf(Gx) * sRk[gt] : 0.f;
-    {
-        // per head: A_tj = beta_t e^{G_t-G_j} rk_t rk_j k_t.k_j (j < t) into shared memory
-        // and P_tj = e^{G_t-G_j} rq_t rk_j q_t.k_j (j <= t) as an image in the free query
-        // tile, one exponential for both
-        const bool live = trow < len;
-        const float rkt = sRk[trow], pt = sRq[trow];
-#pragma unroll
-        for (int i = 0; i < HPC; ++i) {
-            const float *G2 = vG2(i);
-            const float G2t = G2[trow], at = vB(i)[trow] * rkt;
-            float av[32], pv[32];
-            const uint64_t G2t2 = f2pack(G2t, G2t), at2 = f2pack(at, at), pt2 = f2pack(pt, pt);
-#pragma unroll
-            for (int q4 = 0; q4 < 32; q4 += 4) {
-                const float4 g4 = lds4(G2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
-                const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-                for (int qq = 0; qq < 4; qq += 2) {             // column pairs
-                    const int q = q4 + qq, jj = tcb * 32 + q;
-                    float d0, d1;                               // G_t - G_j (log2 units)
-                    f2unpack(ffma2(f2pack(-1.f, -1.f), f2pack(gv[qq], gv[qq + 1]), G2t2), d0, d1);
-                    // the exponent is selected before any product (past t it may be inf)
-                    const float e0 = (jj <= trow && jj < len) ? ex2_fast(d0) : 0.f;
-                    const float e1 = (jj + 1 <= trow && jj + 1 < len) ? ex2_fast(d1) : 0.f;
-                    const uint64_t e2 = fmul2(f2pack(e0, e1), f2pack(rv[qq], rv[qq + 1]));
-                    float a0, a1;
-                    f2unpack(fmul2(fmul2(at2, e2), f2pack(gr[q], gr[q + 1])), a0, a1);
-                    av[q] = (live && jj < trow) ? a0 : 0.f;
-                    av[q + 1] = (live && jj + 1 < trow) ? a1 : 0.f;
-                    f2unpack(fmul2(fmul2(pt2, e2), f2pack(qk[q], qk[q + 1])), pv[q], pv[q + 1]);
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, Gx, o);
+                if (lane >= o) Gx += y;
+            }
+            if (gthr) vG(gh)[gt] = Gx;                          // inclusive within the warp
+            __syncthreads();
+            tc_fence_after();
+            const uint32_t tmem = *tslot;
+            const uint32_t lb = (uint32_t)(warp * 32) << 16;    // this warp's TMEM lanes
+            const int trow = warp * 16 + (lane & 15), tcb = lane >> 4;   // row / column half of
+                                                                          // the M = 64 results
+            const int hrow = tid >> 1, hhalf = tid & 1;         // row / column half, 2 threads a row
+            float gr[32], qk[32];                               // Gram and Q K^T: row trow, 32 columns
+
+            if (gthr) {
+                if (gt >= 32) {
+                    Gx += vG(gh)[31];
+                    vG(gh)[gt] = Gx;
+                }
+                vG2(gh)[gt] = Gx * kLog2e;
+                vB(gh)[gt] = b_in;
+            }
+            // the previous item's flags, while the tiles load
+            if constexpr (PERSIST) {
+                if (tid == 0 && s_pend[0] >= 0) {
+                    prep_publish<HPC>(p, s_pend[0], s_pend[1]);
+                    s_pend[0] = -1;
                 }
             }
-            float *sA = sAT + i * C * LDA;
+            ok = mbar_wait(&bar[0], par);
+            if (__syncthreads_or(!ok)) goto item_fail;
+            tc_fence_after();
+            if (lane == 0 && warp < 2) {
+                // Gram K K^T into columns 0-63 (thread 0), Q K^T into columns 64-127 (thread 32);
+                // M = N = 64, K = 128
+                const uint32_t idesc = instr_desc(64, 64, kFmtBF16, 0, 0);
+                const uint8_t *aop = warp ? sQ : sK;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                sts4(sA + trow * LDA + tcb * 32 + 4 * q, av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
-            store_half_row_bf16(sQ + i * 8192, trow, tcb * 4, pv);
-        }
-    }
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-#pragma unroll
-        for (int i = 0; i < HPC; ++i) bulk_store(record(i) + REC_P, sQ + i * 8192, 8192);
-        bulk_commit();
-    }
-
-    // ---- T = (I + A)^{-1}, in place: the four 16 x 16 diagonal blocks of each head by
-    // forward substitution (one thread per column), written once every thread has read A
-    {
-        const int dh = tid >> 6, b = (tid >> 4) & 3, cc = tid & 15, base = b * 16;
-        float *sA = sAT + (dh < HPC ? dh : 0) * C * LDA;
-        float x[16];
-        if (dh < HPC) {
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-                for (int k4 = 0; k4 < r; k4 += 4) {
-                    const float4 a4 = lds4(sA + (base + r) * LDA + base + k4);
-                    const float aw[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        if (k4 + kk < r) acc -= aw[kk] * x[k4 + kk];
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t o = (ks >> 2) * 8192 + (ks & 3) * 32;
+                    mma_bf16(tmem + warp * 64, smem_desc(smem_u32(aop + o), 16, 1024, kSwizzle128B),
+                             smem_desc(smem_u32(sK + o), 16, 1024, kSwizzle128B), idesc, ks > 0);
                 }
-                x[r] = (r < cc) ? 0.f : acc;
+                mma_commit(&bar[1 + 2 * warp]);
             }
-        }
-        // the P images have left the query tile before it becomes the solve's scratch
-        if (tid == 0) bulk_wait_read_all();
-        __syncthreads();
-        if (dh < HPC) {
+            // query normalisers: two threads per row; the 16-byte chunks are visited in an order
+            // that keeps the eight lanes of a quarter-warp on distinct banks
+            {
+                const uint8_t *src = sQ + hhalf * 8192 + hrow * 128;
+                float ss = 0.f;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sA[(base + r) * LDA + base + cc] = x[r];
-        }
-        __syncthreads();
-    }
-    // ---- then by doubling, 64 threads per head: blocks (1,0) and (3,2) of 16 x 16 (a warp
-    // each, 2 x 4 tiles), then block (1,0) of 32 x 32 (4 x 4 tiles): T_ij = -T_ii A_ij T_jj
-    if ((tid >> 6) < HPC) {
-        const int i = tid >> 6, pb = (tid >> 5) & 1;
-        float *sATi = sAT + i * C * LDA, *sXi = sX + i * kXHead;
-        solve_tile<16, 2>(sATi, sXi + pb * 16 * LDX, 16 + 32 * pb, 32 * pb, lane >> 2, lane & 3);
-    }
-    __syncthreads();
-    if ((tid >> 6) < HPC) {
-        const int i = tid >> 6, pb = (tid >> 5) & 1;
-        float *sATi = sAT + i * C * LDA, *sXi = sX + i * kXHead;
-        apply_tile<16, 2>(sATi, sXi + pb * 16 * LDX, 16 + 32 * pb, 32 * pb, lane >> 2, lane & 3);
-    }
-    __syncthreads();
-    if ((tid >> 6) < HPC) {
-        const int i = tid >> 6, t = tid & 63;
-        solve_tile<32, 4>(sAT + i * C * LDA, sX + i * kXHead, 32, 0, t >> 3, t & 7);
-    }
-    __syncthreads();
-    if ((tid >> 6) < HPC) {
-        const int i = tid >> 6, t = tid & 63;
-        apply_tile<32, 4>(sAT + i * C * LDA, sX + i * kXHead, 32, 0, t >> 3, t & 7);
-    }
-    __syncthreads();
+                for (int q = 0; q < 8; ++q) {
+                    const int pc = q ^ (hrow & 7) ^ (hhalf * 4);
+                    const uint4 w4 = *reinterpret_cast<const uint4 *>(src + pc * 16);
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&w4);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(b2[e]);
+                        ss += f.x * f.x + f.y * f.y;
+                    }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (hhalf == 0) sRq[hrow] = p.l2norm ? p.scale * rsqrtf(ss + kL2Eps) : p.scale;
+            }
+            ok = mbar_wait(&bar[1], par) && mbar_wait(&bar[3], par);
+            if (__syncthreads_or(!ok)) goto item_fail;
+            tc_fence_after();
+            // Gram and Q K^T rows into registers; the key normaliser from the Gram diagonal
+            tmem_row_split(tmem + lb, gr);
+            tmem_row_split(tmem + lb + 64, qk);
+            {
+                float diag = 0.f;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) diag = (tcb * 32 + q == trow) ? gr[q] : diag;
+                if ((trow >> 5) == tcb) sRk[trow] = p.l2norm ? rsqrtf(diag + kL2Eps) : 1.f;
+            }
+            tc_fence_before();
+            __syncthreads();
+            if (gthr) vC1(gh)[gt] = gin ? b_in * expf(Gx) * sRk[gt] : 0.f;
+            {
+                // per head: A_tj = beta_t e^{G_t-G_j} rk_t rk_j k_t.k_j (j < t) into shared memory
+                // and P_tj = e^{G_t-G_j} rq_t rk_j q_t.k_j (j <= t) as an image in the free query
+                // tile, one exponential for both
+                const bool live = trow < len;
+                const float rkt = sRk[trow], pt = sRq[trow];
+#pragma unroll
+                for (int i = 0; i < HPC; ++i) {
+                    const float *G2 = vG2(i);
+                    const float G2t = G2[trow], at = vB(i)[trow] * rkt;
+                    float av[32], pv[32];
+                    const uint64_t G2t2 = f2pack(G2t, G2t), at2 = f2pack(at, at), pt2 = f2pack(pt, pt);
+#pragma unroll
+                    for (int q4 = 0; q4 < 32; q4 += 4) {
+                        const float4 g4 = lds4(G2 + tcb * 32 + q4), r4 = lds4(sRk + tcb * 32 + q4);
+                        const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                        for (int qq = 0; qq < 4; qq += 2) {             // column pairs
+                            const int q = q4 + qq, jj = tcb * 32 + q;
+                            float d0, d1;                               // G_t - G_j (log2 units)
+                            f2unpack(ffma2(f2pack(-1.f, -1.f), f2pack(gv[qq], gv[qq + 1]), G2t2), d0, d1);
+                            // the exponent is selected before any product (past t it may be inf)
+                            const float e0 = (jj <= trow && jj < len) ? ex2_fast(d0) : 0.f;
+                            const float e1 = (jj + 1 <= trow && jj + 1 < len) ? ex2_fast(d1) : 0.f;
+                            const uint64_t e2 = fmul2(f2pack(e0, e1), f2pack(rv[qq], rv[qq + 1]));
+                            float a0, a1;
+                            f2unpack(fmul2(fmul2(at2, e2), f2pack(gr[q], gr[q + 1])), a0, a1);
+                            av[q] = (live && jj < trow) ? a0 : 0.f;
+                            av[q + 1] = (live && jj + 1 < trow) ? a1 : 0.f;
+                            f2unpack(fmul2(fmul2(pt2, e2), f2pack(qk[q], qk[q + 1])), pv[q], pv[q + 1]);
+                        }
+                    }
+                    float *sA = sAT + i * C * LDA;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        sts4(sA + trow * LDA + tcb * 32 + 4 * q, av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
+                    store_half_row_bf16(sQ + i * 8192, trow, tcb * 4, pv);
+                }
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+#pragma unroll
+                for (int i = 0; i < HPC; ++i) bulk_store(record(i) + REC_P, sQ + i * 8192, 8192);
+                bulk_commit();
+            }
 
-    {
-        // rows of T (two threads a row, 32 columns each) into registers, then:
-        // T' = T diag(beta gamma rk) of head 0 as operand images for W in the query tile,
-        // T'' = T diag(beta) of every head as images in place of its T, bulk-copied out
-        float tv[HPC][32];
+            // ---- T = (I + A)^{-1}, in place: the four 16 x 16 diagonal blocks of each head by
+            // forward substitution (one thread per column), written once every thread has read A
+            {
+                const int dh = tid >> 6, b = (tid >> 4) & 3, cc = tid & 15, base = b * 16;
+                float *sA = sAT + (dh < HPC ? dh : 0) * C * LDA;
+                float x[16];
+                if (dh < HPC) {
 #pragma unroll
-        for (int i = 0; i < HPC; ++i)
+                    for (int r = 0; r < 16; ++r) {
+                        float acc = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int q = 0; q < 32; q += 4) {
-                const float4 t4 = lds4(sAT + i * C * LDA + hrow * LDA + hhalf * 32 + q);
-                tv[i][q] = t4.x; tv[i][q + 1] = t4.y; tv[i][q + 2] = t4.z; tv[i][q + 3] = t4.w;
+                        for (int k4 = 0; k4 < r; k4 += 4) {
+                            const float4 a4 = lds4(sA + (base + r) * LDA + base + k4);
+                            const float aw[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                if (k4 + kk < r) acc -= aw[kk] * x[k4 + kk];
+                        }
+                        x[r] = (r < cc) ? 0.f : acc;
+                    }
+                }
+                // the P images have left the query tile before it becomes the solve's scratch
+                if (tid == 0) bulk_wait_read_all();
+                __syncthreads();
+                if (dh < HPC) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) sA[(base + r) * LDA + base + cc] = x[r];
+                }
+                __syncthreads();
             }
-        store_scaled_row(tv[0], vC1(0), hrow, hhalf, sT1, sT1 + 8192);
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) issue_w(tmem, sK, sT1, &bar[2]);
+            // ---- then by doubling, 64 threads per head: blocks (1,0) and (3,2) of 16 x 16 (a warp
+            // each, 2 x 4 tiles), then block (1,0) of 32 x 32 (4 x 4 tiles): T_ij = -T_ii A_ij T_jj
+            if ((tid >> 6) < HPC) {
+                const int i = tid >> 6, pb = (tid >> 5) & 1;
+                float *sATi = sAT + i * C * LDA, *sXi = sX + i * kXHead;
+                solve_tile<16, 2>(sATi, sXi + pb * 16 * LDX, 16 + 32 * pb, 32 * pb, lane >> 2, lane & 3);
+            }
+            __syncthreads();
+            if ((tid >> 6) < HPC) {
+                const int i = tid >> 6, pb = (tid >> 5) & 1;
+                float *sATi = sAT + i * C * LDA, *sXi = sX + i * kXHead;
+                apply_tile<16, 2>(sATi, sXi + pb * 16 * LDX, 16 + 32 * pb, 32 * pb, lane >> 2, lane & 3);
+            }
+            __syncthreads();
+            if ((tid >> 6) < HPC) {
+                const int i = tid >> 6, t = tid & 63;
+                solve_tile<32, 4>(sAT + i * C * LDA, sX + i * kXHead, 32, 0, t >> 3, t & 7);
+            }
+            __syncthreads();
+            if ((tid >> 6) < HPC) {
+                const int i = tid >> 6, t = tid & 63;
+                apply_tile<32, 4>(sAT + i * C * LDA, sX + i * kXHead, 32, 0, t >> 3, t & 7);
+            }
+            __syncthreads();
+
+            {
+                // the ticket of the next item (its round trip overlaps the rest of this one)
+                if constexpr (PERSIST) {
+                    if (tid == 0) *s_ticket = prep_ticket(p);
+                }
+                // rows of T (two threads a row, 32 columns each) into registers, then:
+                // T' = T diag(beta gamma rk) of head 0 as operand images for W in the query tile,
+                // T'' = T diag(beta) of every head as images in place of its T, bulk-copied out
+                float tv[HPC][32];
 #pragma unroll
-        for (int i = 0; i < HPC; ++i)
-            store_scaled_row(tv[i], vB(i), hrow, hhalf, sAT8 + i * C * LDA * 4, sAT8 + i * C * LDA * 4 + 8192);
-        // ---- per-token factors of every head (one coalesced row each)
-        if (gthr) {
-            float *sc = reinterpret_cast<float *>(record(gh) + REC_F);
-            const float Gl = vG(gh)[len - 1], rk = sRk[gt];
-            sc[SC_QD * C + gt] = gin ? sRq[gt] * expf(Gx) : 0.f;
-            sc[SC_KD * C + gt] = gin ? rk * expf(Gl - Gx) : 0.f;
-            sc[SC_RK * C + gt] = gin ? rk : 0.f;
-            sc[SC_ALPHA * C + gt] = gin ? expf(g_in) : 0.f;
-            sc[SC_MISC * C + gt] = gt == 0 ? expf(Gl) : (gt == 1 ? (float)len : 0.f);
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+                for (int i = 0; i < HPC; ++i)
 #pragma unroll
-            for (int i = 0; i < HPC; ++i)
-                bulk_store(record(i) + REC_T2HI, sAT8 + i * C * LDA * 4, 16384);
-            bulk_commit();
-        }
-        ok = mbar_wait(&bar[2], 0);
-        if (__syncthreads_or(!ok)) goto teardown;
-        tc_fence_after();
-        if constexpr (HPC == 2) {
-            // W of head 1 into columns 64-127 while -W of head 0 is staged in place of the
-            // T'' images (once their copies have read them)
-            store_scaled_row(tv[1], vC1(1), hrow, hhalf, sT1, sT1 + 8192);
+                    for (int q = 0; q < 32; q += 4) {
+                        const float4 t4 = lds4(sAT + i * C * LDA + hrow * LDA + hhalf * 32 + q);
+                        tv[i][q] = t4.x; tv[i][q + 1] = t4.y; tv[i][q + 2] = t4.z; tv[i][q + 3] = t4.w;
+                    }
+                store_scaled_row(tv[0], vC1(0), hrow, hhalf, sT1, sT1 + 8192);
+                fence_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+                if (tid == 0) issue_w(tmem, sK, sT1, &bar[2]);
+#pragma unroll
+                for (int i = 0; i < HPC; ++i)
+                    store_scaled_row(tv[i], vB(i), hrow, hhalf, sAT8 + i * C * LDA * 4, sAT8 + i * C * LDA * 4 + 8192);
+                // ---- per-token factors of every head (one coalesced row each)
+                if (gthr) {
+                    float *sc = reinterpret_cast<float *>(record(gh) + REC_F);
+                    const float Gl = vG(gh)[len - 1], rk = sRk[gt];
+                    sc[SC_QD * C + gt] = gin ? sRq[gt] * expf(Gx) : 0.f;
+                    sc[SC_KD * C + gt] = gin ? rk * expf(Gl - Gx) : 0.f;
+                    sc[SC_RK * C + gt] = gin ? rk : 0.f;
+                    sc[SC_ALPHA * C + gt] = gin ? expf(g_in) : 0.f;
+                    sc[SC_MISC * C + gt] = gt == 0 ? expf(Gl) : (gt == 1 ? (float)len : 0.f);
+                }
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+#pragma unroll
+                    for (int i = 0; i < HPC; ++i)
+                        bulk_store(record(i) + REC_T2HI, sAT8 + i * C * LDA * 4, 16384);
+                    bulk_commit();
+                }
+                ok = mbar_wait(&bar[2], par);
+                if (__syncthreads_or(!ok)) goto item_fail;
+                tc_fence_after();
+                if constexpr (HPC == 2) {
+                    // W of head 1 into columns 64-127 while -W of head 0 is staged in place of the
+                    // T'' images (once their copies have read them)
+                    store_scaled_row(tv[1], vC1(1), hrow, hhalf, sT1, sT1 + 8192);
+                    fence_async_smem();
+                    tc_fence_before();
+                    __syncthreads();
+                    tc_fence_after();
+                    if (tid == 0) {
+                        issue_w(tmem + 64, sK, sT1, &bar[4]);
+                        bulk_wait_read_all();
+                    }
+                    __syncthreads();
+                    stage_minus_w(tmem + lb, sAT8, tid);
+                    fence_async_smem();
+                    __syncthreads();
+                    if (tid == 0) {
+                        bulk_store(record(0) + REC_WHI, sAT8, 32768);
+                        bulk_commit();
+                    }
+                    ok = mbar_wait(&bar[4], par);
+                    if (__syncthreads_or(!ok)) goto item_fail;
+                    tc_fence_after();
+                }
+            }
+            // the next item (persistent prep), announced before the barrier below
+            if constexpr (PERSIST) {
+                if (tid == 0) *s_item = prep_item(p, *s_ticket, stay);
+            }
+            // -W of the last head, staged in the key and query tiles (free once its product is done)
+            stage_minus_w(tmem + lb + (HPC - 1) * 64, sm, tid);
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
-            tc_fence_after();
             if (tid == 0) {
-                issue_w(tmem + 64, sK, sT1, &bar[4]);
-                bulk_wait_read_all();
-            }
-            __syncthreads();
-            stage_minus_w(tmem + lb, sAT8, tid);
-            fence_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                bulk_store(record(0) + REC_WHI, sAT8, 32768);
+                bulk_store(record(HPC - 1) + REC_WHI, sm, 32768);
                 bulk_commit();
+                if constexpr (PERSIST) {
+                    // the next item's tiles overwrite what the copies read; the records'
+                    // flags are set once the copies are complete
+                    bulk_wait_read_all();
+                    s_pend[0] = c;
+                    s_pend[1] = h0;
+                    PrepChunk nw;
+                    if (*s_item >= 0 && prep_chunk<HPC>(p, true, *s_item, nw))
+                        prep_load_tiles(&mapK, &mapQ, sK, sQ, &bar[0], nw.h0 / (p.HV / p.HK), nw.t0);
+                }
             }
-            ok = mbar_wait(&bar[4], 0);
-            if (__syncthreads_or(!ok)) goto teardown;
-            tc_fence_after();
         }
+        if constexpr (!PERSIST) break;
+        par ^= 1u;
+        continue;
+    item_fail:
+        ok = false;
+        break;
     }
-    // -W of the last head, staged in the key and query tiles (free once its product is done)
-    stage_minus_w(tmem + lb + (HPC - 1) * 64, sm, tid);
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_store(record(HPC - 1) + REC_WHI, sm, 32768);
-        bulk_commit();
-    }
-teardown:
     if (!ok && tid == 0) set_error(p, GDN_ERR_TIMEOUT);
+    if constexpr (PERSIST) {
+        if (tid == 0 && s_pend[0] >= 0) prep_publish<HPC>(p, s_pend[0], s_pend[1]);
+    }
     // shared memory stays until every bulk copy has read it
     if (tid == 0) bulk_wait_read_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+    if (warp == 0) tmem_dealloc(*tslot, kPrepTmemCols);
 }
 
 // ================================================================== chain kernel
@@ -856,6 +994,13 @@ __device__ __forceinline__ int32_t flag_acquire(const int32_t *f) {
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
     return v;
 }
+__device__ __forceinline__ int32_t flag_relaxed(const int32_t *f) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// record-ready flags read ahead by the chain's producer in one round trip
+constexpr int kReadyAhead = 8;
 // wait until *f >= want; gives up (false) after limit_ns
 __device__ __forceinline__ bool flag_wait(const int32_t *f, int32_t want, uint64_t limit_ns = 1000000000ull) {
     if (flag_acquire(f) >= want) return true;
@@ -867,13 +1012,34 @@ __device__ __forceinline__ bool flag_wait(const int32_t *f, int32_t want, uint64
     }
 }
 
+// The chain's wait for the record of chunk c (flags every `stride` words from `ready`):
+// acquires its flag, reads the flags of up to kReadyAhead - 1 chunks after it in the same
+// round trip, and returns the first chunk not known complete (-1 after a timeout).  Kept
+// out of line: the chain kernel's speed depends on the size of its loop code.
+__device__ __noinline__ int ready_wait(const int32_t *ready, int stride, int c, int nch) {
+    if (!flag_wait(ready + (size_t)c * stride, 1)) return -1;
+    int32_t f[kReadyAhead - 1];
+#pragma unroll
+    for (int i = 0; i < kReadyAhead - 1; ++i)
+        f[i] = c + 1 + i < nch ? flag_relaxed(ready + (size_t)(c + 1 + i) * stride) : 0;
+    int to = c + 1;
+#pragma unroll
+    for (int i = 0; i < kReadyAhead - 1; ++i)
+        if (to == c + 1 + i && f[i] >= 1) to = c + 2 + i;
+    // the flags read relaxed order the records' reads after this fence
+    if (to > c + 1) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    return to;
+}
+
 // UNITS == false: one CTA per chain, launched as a (value slice, value head, sequence)
 // grid, packed batches' chains longest first (the hardware starts the CTAs in order).
 // UNITS == true: the persistent work-unit stream above (equal-length batches whose chains
 // outnumber the SMs).  The per-chunk work is the same code; only the loops around it and
 // the source of a chunk's coordinates differ, and each schedule compiles only its own
 // loops (the kernel's speed depends on the size of its loop code: instruction fetch).
-template <bool STATES, bool UNITS>
+// READY: the records come from the persistent prep beside the chain, each taken once its
+// ready flag is set (one CTA per chain), instead of after the whole prep grid.
+template <bool STATES, bool UNITS, bool READY>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapQ,
              const __grid_constant__ CUtensorMap mapV, Params p) {
@@ -1001,9 +1167,13 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                 bulk_load(sb + kBP, rec + REC_P, kStageB - kBP, fb);
             };
             bool issued = false;
-            // the records come from the prep grid, which may still be running
-            asm volatile("griddepcontrol.wait;" ::: "memory");
+            // the records come from the prep grid, which may still be running: with the
+            // persistent prep beside the chain each record is taken once its ready flag is
+            // set, otherwise once the whole prep grid has completed
+            if constexpr (!READY) asm volatile("griddepcontrol.wait;" ::: "memory");
             if constexpr (!UNITS) {
+                // records known complete: chunks below ready_to
+                int ready_to = 0;
                 // iteration cc: (once -W S of chunk cc - 2 is done) T'' V of chunk cc - 1, then
                 // the loads of chunk cc; the last iteration only issues T'' V of chunk nch - 1.
                 // T'' V of chunk 0 waits for its inputs, so it follows the loads of chunk 1.
@@ -1018,6 +1188,15 @@ chain_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ C
                     const int tok = (int)(sr.t0 + (int64_t)cc * C);
                     const uint8_t *rec = reinterpret_cast<const uint8_t *>(p.rec) +
                                          ((size_t)(sr.first + cc) * p.HV + h) * kRecBytes;
+                    if constexpr (READY) {
+                        if (cc >= ready_to) {
+                            // acquire the record's flag, then read the record with bulk copies;
+                            // the flags of the next chunks are read in the same round trip
+                            ready_to = ready_wait(p.ready + (size_t)sr.first * p.HV + h, p.HV, cc, nch);
+                            if (ready_to < 0) { fail(); break; }
+                            fence_async_global();
+                        }
+                    }
                     load_a(cc, rec, tok, h, vs);
                     if (u >= 1 && !wait(B_EMPTYB0 + st, (u - 1) & 1)) break;
                     load_b(cc, rec, tok, j);
@@ -1833,6 +2012,45 @@ static ChainPlan plan_chain(const PrefillParams &pp, int n_sm) {
     return c;
 }
 
+// The prep beside the chain.  When an equal-length batch runs one chain CTA per chain and
+// leaves SMs free, the prep grid is made persistent (one CTA per prep slot, `per_sm` to an
+// SM) and the chain kernel starts at once: the prep CTAs on the SMs the chain leaves free
+// produce every record, in chunk order, while the others leave at the start (the limit of
+// items they may take is zero).  This pays where those CTAs keep ahead of the chain: one
+// item time for the first chunk's records, then a chunk's records in less than a chunk
+// period.  Otherwise (fewer free SMs than that, e.g. 24 beside the 128 chains of 32 value
+// heads) every prep CTA takes items until none is left and the chain starts after them.
+// The estimate uses costs measured on GB300 at T = 4096 (microseconds): a prep item with
+// three CTAs to an SM (one value head, two value heads), a chunk of the chain.
+constexpr double kPrepItemUs[2] = {11.0, 17.0};
+constexpr double kChainChunkUs = 1.5;
+constexpr double kPrepMargin = 0.8;        // the staying CTAs' rate is taken at 80% of that
+
+struct PrepPlan {
+    int items, limit, stay_sms, grid;
+};
+
+// limit == items: no prep beside the chain
+static PrepPlan plan_prep(int n_items, int items_per_chunk, int chunks_per_seq, int chain_ctas,
+                          int n_sm, int per_sm, int hpc) {
+    PrepPlan pl;
+    pl.items = n_items;
+    pl.limit = n_items;
+    pl.stay_sms = 0;
+    pl.grid = n_items < per_sm * n_sm ? n_items : per_sm * n_sm;
+    const int stay = n_sm - chain_ctas;
+    if (stay <= 0 || n_items <= 0 || per_sm <= 0) return pl;
+    const double item_us = kPrepItemUs[hpc - 1];
+    const double rate = kPrepMargin * per_sm * stay / item_us;       // items per microsecond
+    const double chain_us = (chunks_per_seq - 1) * kChainChunkUs;
+    if (rate * kChainChunkUs >= items_per_chunk && per_sm * stay >= items_per_chunk &&
+        rate * (item_us + chain_us) >= n_items) {
+        pl.limit = 0;
+        pl.stay_sms = stay;
+    }
+    return pl;
+}
+
 }  // namespace tc
 
 size_t tc_record_bytes() { return (size_t)tc::kRecBytes; }
@@ -1846,14 +2064,61 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     cudaError_t e;
     // the caller sized the workspace for records of rec_floats floats
     if ((size_t)pp.rec_floats * sizeof(float) < (size_t)kRecBytes) return cudaErrorInvalidValue;
+    // the chain's schedule (equal-length batches): the work-unit stream where the chains are
+    // cut into segments, else one CTA per chain; with per-token states the stream runs
+    // beside the states kernel (see below)
+    const bool overlap = pp.states && !pp.cu_seqlens && pp.max_chunks > 0;
+    const int hpc = (pp.HV / pp.HK) % 2 == 0 ? 2 : 1;
+    ChainPlan plan = {0, 1, 0, 1};
+    int n_sm = 0;
+    if (!pp.cu_seqlens && pp.N > 0) {
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        plan = overlap ? plan_overlap(pp, n_sm) : plan_chain(pp, n_sm);
+    }
+    const bool units = overlap || plan.n_units > plan.n_chains;
+    // the prep kernel of a schedule: one CTA per item, or the persistent prep beside the chain
+    auto prep_fn = [&](bool persist) {
+        return hpc == 2 ? (persist ? prep_kernel<2, true> : prep_kernel<2, false>)
+                        : (persist ? prep_kernel<1, true> : prep_kernel<1, false>);
+    };
+    const size_t prep_smem = hpc == 2 ? prep_smem_bytes<2>() : prep_smem_bytes<1>();
+    // the prep beside the chain: equal-length batches with one CTA per chain
+    bool beside = !pp.cu_seqlens && !units && pp.max_chunks > 0 && pp.N > 0;
+    PrepPlan prep = {0, 0, 0, 0};
+    if (beside) {
+        // prep CTAs an SM holds, from the kernel's registers and shared memory (the
+        // occupancy calculator answered one where three run)
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, prep_fn(true));
+        int dev = 0, smem_sm = 0, regs_sm = 0, reserved = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        if (e != cudaSuccess) return e;
+        const size_t smem_cta = prep_smem + fa.sharedSizeBytes + (size_t)reserved;
+        const int regs_cta = (fa.numRegs * 32 + 255) / 256 * 256 * (kPrepThreads / 32);
+        int per_sm = kPrepPerSm;
+        if (smem_cta > 0 && (int)((size_t)smem_sm / smem_cta) < per_sm) per_sm = (int)((size_t)smem_sm / smem_cta);
+        if (regs_cta > 0 && regs_sm / regs_cta < per_sm) per_sm = regs_sm / regs_cta;
+        const int ny = pp.HV / hpc;
+        if (per_sm >= 1)
+            prep = plan_prep(pp.max_chunks * ny, pp.N * ny, (pp.T_seq + C - 1) / C, plan.n_chains, n_sm,
+                             per_sm, hpc);
+        beside = per_sm >= 1 && prep.limit < prep.items;
+    }
     if (pp.cu_seqlens) {
         if ((e = launch_chunk_table(pp, st)) != cudaSuccess) return e;
     } else {
         // the kernels only ever move the status word from GDN_OK to an error code, so it
         // starts clean here (a reused workspace may hold the last call's error), with the
-        // work-unit stream's claim counter and hand-off flags (right after the header)
+        // claim counters, the work-unit stream's hand-off flags (right after the header) and,
+        // with the prep beside the chain, the record-ready flags (right after those)
         const size_t clear = (size_t)((const char *)pp.chain_flags - (const char *)pp.status) +
-                             chain_flag_bytes(pp.N, pp.HV);
+                             chain_flag_bytes(pp.N, pp.HV) +
+                             (beside ? ready_flag_bytes(pp.max_chunks, pp.HV) : 0);
         if ((e = cudaMemsetAsync(pp.status, 0, clear, st)) != cudaSuccess) return e;
     }
     Params p;
@@ -1865,6 +2130,12 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     p.max_chunks = pp.max_chunks; p.status = pp.status; p.chunk_seq = pp.chunk_seq;
     p.chunk_first = pp.chunk_first; p.seq_order = pp.seq_order; p.rec = pp.rec;
     p.chain_flags = pp.chain_flags;
+    if (beside) {
+        p.ready = pp.ready;
+        p.prep_items = prep.items;
+        p.prep_limit = prep.limit;
+        p.prep_stay_sms = prep.stay_sms;
+    }
     CUtensorMap mk, mq, mv;
     if (pp.T_total > 0) {
         if (!make_map(&mk, pp.k, pp.HK, pp.T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1875,20 +2146,16 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         memset(&mk, 0, sizeof mk); memset(&mq, 0, sizeof mq); memset(&mv, 0, sizeof mv);
     }
     if (pp.max_chunks > 0) {
-        // value heads in pairs when each key head serves an even number of them
-        if ((pp.HV / pp.HK) % 2 == 0) {
-            constexpr size_t smem = prep_smem_bytes<2>();
-            if ((e = cudaFuncSetAttribute(prep_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)smem)) != cudaSuccess)
-                return e;
-            prep_kernel<2><<<dim3(pp.max_chunks, pp.HV / 2), kPrepThreads, smem, st>>>(mk, mq, p);
-        } else {
-            constexpr size_t smem = prep_smem_bytes<1>();
-            if ((e = cudaFuncSetAttribute(prep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)smem)) != cudaSuccess)
-                return e;
-            prep_kernel<1><<<dim3(pp.max_chunks, pp.HV), kPrepThreads, smem, st>>>(mk, mq, p);
-        }
+        // value heads in pairs when each key head serves an even number of them; one CTA
+        // per item, or the persistent grid of the prep beside the chain.  All of the SM's
+        // unified memory as shared memory, so that three prep CTAs fit.
+        const auto kern = prep_fn(beside);
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return e;
+        const dim3 grid = beside ? dim3(prep.grid) : dim3(pp.max_chunks, pp.HV / hpc);
+        kern<<<grid, kPrepThreads, prep_smem, st>>>(mk, mq, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (pp.N > 0) {
@@ -1898,22 +2165,14 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         // With per-token states (equal-length batches) the stream runs on half the SMs and
         // the states kernel beside it on the other half, taking each segment as the stream
         // publishes it: the states are bound by HBM writes, the stream by its latency.
-        const bool overlap = pp.states && !pp.cu_seqlens && pp.max_chunks > 0;
-        ChainPlan plan = {0, 1, 0, 1};
-        if (!pp.cu_seqlens) {
-            int dev = 0, n_sm = 0;
-            if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-            if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-            plan = overlap ? plan_overlap(pp, n_sm) : plan_chain(pp, n_sm);
-        }
-        const bool units = overlap || plan.n_units > plan.n_chains;
         p.n_chains = plan.n_chains;
         p.seg_len = plan.seg_len;
         p.n_units = plan.n_units;
         p.states_overlap = overlap ? 1 : 0;
         p.final_direct = overlap && pp.s_final != pp.s0 ? 1 : 0;
-        auto kern = units ? (pp.states ? chain_kernel<true, true> : chain_kernel<false, true>)
-                          : (pp.states ? chain_kernel<true, false> : chain_kernel<false, false>);
+        auto kern = units ? (pp.states ? chain_kernel<true, true, false> : chain_kernel<false, true, false>)
+                          : pp.states ? chain_kernel<true, false, false>
+                                      : (beside ? chain_kernel<false, false, true> : chain_kernel<false, false, false>);
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kChainSmem)) != cudaSuccess)
             return e;
