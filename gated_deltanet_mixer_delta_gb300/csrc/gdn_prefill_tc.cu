@@ -88,6 +88,7 @@ struct Params {
     // every record's flag in ready is set once the record is complete
     int32_t *ready;              // [chunks][HV] or null (the chain waits for the prep grid)
     int prep_items, prep_limit, prep_stay_sms;
+    int prep_slots;              // prep CTAs resident at once (one CTA per item: L2 prefetch distance)
 };
 
 // ------------------------------------------------------------------ shared helpers
@@ -359,12 +360,40 @@ __device__ __forceinline__ void stage_minus_w(uint32_t taddr, uint8_t *img, int 
 // compare-and-swap loop starved the CTAs that lost its races for the whole grid).
 // Where a prep item's chunk lies: the item number of the persistent prep (items chunk-major:
 // the first chunk of every sequence and head group, then the second, ...; equal-length
-// batches), else the CTA's grid position.  False for a chunk past the batch's end (a packed
-// batch's chunk table may hold fewer chunks than the grid) or after a bad chunk table.
+// batches), else the CTA's grid position -- (head group, chunk counted from the last), so
+// that the hardware starts the CTAs chunk-major from the last chunk and the records the
+// chain reads first are the ones written last (most likely still in L2).  False for a
+// chunk past the batch's end (a packed batch's chunk table may hold fewer chunks than the
+// grid) or after a bad chunk table.
+constexpr unsigned kGridY = 65535;                          // grid y limit: chunks beyond it in z
 struct PrepChunk {
     int c, h0, len;
     int64_t t0;
 };
+template <int HPC>
+__device__ __forceinline__ bool prep_chunk_locate(const Params &p, PrepChunk &w) {
+    if (p.cu_seqlens) {
+        if (p.status[kStatusWord] != GDN_OK || w.c < 0 || w.c >= p.status[kChunkCountWord]) return false;
+        const int s = p.chunk_seq[w.c];
+        w.t0 = p.cu_seqlens[s] + (int64_t)(w.c - p.chunk_first[s]) * C;
+        w.len = (int)min((int64_t)C, (int64_t)p.cu_seqlens[s + 1] - w.t0);
+    } else {
+        const int cps = (p.T_seq + C - 1) / C;
+        if (cps == 0 || w.c < 0 || w.c >= p.N * cps) return false;
+        const int s = w.c / cps, local = w.c - s * cps;
+        w.t0 = (int64_t)s * p.T_seq + (int64_t)local * C;
+        w.len = min(C, p.T_seq - local * C);
+    }
+    return true;
+}
+// grid position (x = head group, y = chunk counted from the last)
+template <int HPC>
+__device__ __forceinline__ bool prep_chunk_at(const Params &p, unsigned gx, unsigned gy, PrepChunk &w) {
+    w.h0 = (int)gx * HPC;
+    const int count = p.cu_seqlens ? p.status[kChunkCountWord] : p.N * ((p.T_seq + C - 1) / C);
+    w.c = count - 1 - (int)gy;
+    return prep_chunk_locate<HPC>(p, w);
+}
 template <int HPC>
 __device__ __forceinline__ bool prep_chunk(const Params &p, bool persist, int item, PrepChunk &w) {
     if (persist) {
@@ -372,23 +401,9 @@ __device__ __forceinline__ bool prep_chunk(const Params &p, bool persist, int it
         const int local = item / per, r = item - local * per, sq = r / ny;
         w.c = sq * ((p.T_seq + C - 1) / C) + local;
         w.h0 = (r - sq * ny) * HPC;
-    } else {
-        w.c = blockIdx.x;
-        w.h0 = blockIdx.y * HPC;
+        return prep_chunk_locate<HPC>(p, w);
     }
-    if (p.cu_seqlens) {
-        if (p.status[kStatusWord] != GDN_OK || w.c >= p.status[kChunkCountWord]) return false;
-        const int s = p.chunk_seq[w.c];
-        w.t0 = p.cu_seqlens[s] + (int64_t)(w.c - p.chunk_first[s]) * C;
-        w.len = (int)min((int64_t)C, (int64_t)p.cu_seqlens[s + 1] - w.t0);
-    } else {
-        const int cps = (p.T_seq + C - 1) / C;
-        if (cps == 0 || w.c >= p.N * cps) return false;
-        const int s = w.c / cps, local = w.c - s * cps;
-        w.t0 = (int64_t)s * p.T_seq + (int64_t)local * C;
-        w.len = min(C, p.T_seq - local * C);
-    }
-    return true;
+    return prep_chunk_at<HPC>(p, blockIdx.x, blockIdx.y + kGridY * blockIdx.z, w);
 }
 
 // The key and query tiles of a chunk (key head j) into the prep's tiles, completing bar.
@@ -492,6 +507,25 @@ prep_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CU
             }
         } else {
             prep_load_tiles(&mapK, &mapQ, sK, sQ, &bar[0], w.h0 / (p.HV / p.HK), w.t0);
+            // the tiles of the item the next wave of CTAs starts with (the CTA p.prep_slots
+            // further on) into L2, so that its load does not wait for HBM.  Only the first
+            // two waves do this: later the L2 is full of the records written since, and a
+            // tile fetched a wave early is evicted before its load (measured at B = 2,
+            // T = 65536: prep 2.5% slower with every wave prefetching).  Equal-length batches
+            // only: a packed batch's chunk takes a chain of dependent loads to find.
+            const unsigned b0 = blockIdx.x + gridDim.x * (blockIdx.y + kGridY * blockIdx.z);
+            if (p.prep_slots > 0 && !p.cu_seqlens && b0 < 2u * (unsigned)p.prep_slots) {
+                const unsigned b = b0 + p.prep_slots;
+                PrepChunk w2;
+                if (b < gridDim.x * gridDim.y * gridDim.z &&
+                    prep_chunk_at<HPC>(p, b % gridDim.x, b / gridDim.x, w2)) {
+                    const int j2 = w2.h0 / (p.HV / p.HK);
+                    tma_prefetch_3d(&mapK, 0, j2, (int)w2.t0);
+                    tma_prefetch_3d(&mapK, 64, j2, (int)w2.t0);
+                    tma_prefetch_3d(&mapQ, 0, j2, (int)w2.t0);
+                    tma_prefetch_3d(&mapQ, 64, j2, (int)w2.t0);
+                }
+            }
         }
     }
     if (warp == 0) { tmem_alloc(tslot, kPrepTmemCols); tmem_relinquish(); }
@@ -2070,13 +2104,10 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
     const bool overlap = pp.states && !pp.cu_seqlens && pp.max_chunks > 0;
     const int hpc = (pp.HV / pp.HK) % 2 == 0 ? 2 : 1;
     ChainPlan plan = {0, 1, 0, 1};
-    int n_sm = 0;
-    if (!pp.cu_seqlens && pp.N > 0) {
-        int dev = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        plan = overlap ? plan_overlap(pp, n_sm) : plan_chain(pp, n_sm);
-    }
+    int dev = 0, n_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (!pp.cu_seqlens && pp.N > 0) plan = overlap ? plan_overlap(pp, n_sm) : plan_chain(pp, n_sm);
     const bool units = overlap || plan.n_units > plan.n_chains;
     // the prep kernel of a schedule: one CTA per item, or the persistent prep beside the chain
     auto prep_fn = [&](bool persist) {
@@ -2084,25 +2115,29 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
                         : (persist ? prep_kernel<1, true> : prep_kernel<1, false>);
     };
     const size_t prep_smem = hpc == 2 ? prep_smem_bytes<2>() : prep_smem_bytes<1>();
+    // prep CTAs an SM holds, from the kernel's registers and shared memory (the occupancy
+    // calculator answered one where three run)
+    auto ctas_per_sm = [&](bool persist, int &per_sm) -> cudaError_t {
+        cudaFuncAttributes fa;
+        int smem_sm = 0, regs_sm = 0, reserved = 0;
+        cudaError_t r = cudaFuncGetAttributes(&fa, prep_fn(persist));
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        if (r != cudaSuccess) return r;
+        const size_t smem_cta = prep_smem + fa.sharedSizeBytes + (size_t)reserved;
+        const int regs_cta = (fa.numRegs * 32 + 255) / 256 * 256 * (kPrepThreads / 32);
+        per_sm = kPrepPerSm;
+        if (smem_cta > 0 && (int)((size_t)smem_sm / smem_cta) < per_sm) per_sm = (int)((size_t)smem_sm / smem_cta);
+        if (regs_cta > 0 && regs_sm / regs_cta < per_sm) per_sm = regs_sm / regs_cta;
+        return cudaSuccess;
+    };
     // the prep beside the chain: equal-length batches with one CTA per chain
     bool beside = !pp.cu_seqlens && !units && pp.max_chunks > 0 && pp.N > 0;
     PrepPlan prep = {0, 0, 0, 0};
     if (beside) {
-        // prep CTAs an SM holds, from the kernel's registers and shared memory (the
-        // occupancy calculator answered one where three run)
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, prep_fn(true));
-        int dev = 0, smem_sm = 0, regs_sm = 0, reserved = 0;
-        if (e == cudaSuccess) e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-        if (e != cudaSuccess) return e;
-        const size_t smem_cta = prep_smem + fa.sharedSizeBytes + (size_t)reserved;
-        const int regs_cta = (fa.numRegs * 32 + 255) / 256 * 256 * (kPrepThreads / 32);
-        int per_sm = kPrepPerSm;
-        if (smem_cta > 0 && (int)((size_t)smem_sm / smem_cta) < per_sm) per_sm = (int)((size_t)smem_sm / smem_cta);
-        if (regs_cta > 0 && regs_sm / regs_cta < per_sm) per_sm = regs_sm / regs_cta;
+        int per_sm = 0;
+        if ((e = ctas_per_sm(true, per_sm)) != cudaSuccess) return e;
         const int ny = pp.HV / hpc;
         if (per_sm >= 1)
             prep = plan_prep(pp.max_chunks * ny, pp.N * ny, (pp.T_seq + C - 1) / C, plan.n_chains, n_sm,
@@ -2135,6 +2170,10 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
         p.prep_items = prep.items;
         p.prep_limit = prep.limit;
         p.prep_stay_sms = prep.stay_sms;
+    } else if (pp.max_chunks > 0 && !pp.cu_seqlens) {
+        int per_sm = 0;
+        if ((e = ctas_per_sm(false, per_sm)) != cudaSuccess) return e;
+        p.prep_slots = per_sm * n_sm;
     }
     CUtensorMap mk, mq, mv;
     if (pp.T_total > 0) {
@@ -2154,7 +2193,9 @@ cudaError_t launch_prefill_tc(const PrefillParams &pp, cudaStream_t st) {
             (e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                       (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
             return e;
-        const dim3 grid = beside ? dim3(prep.grid) : dim3(pp.max_chunks, pp.HV / hpc);
+        const unsigned mc = (unsigned)pp.max_chunks;
+        const dim3 grid = beside ? dim3(prep.grid)
+                                 : dim3(pp.HV / hpc, mc < kGridY ? mc : kGridY, (mc + kGridY - 1) / kGridY);
         kern<<<grid, kPrepThreads, prep_smem, st>>>(mk, mq, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
