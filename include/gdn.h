@@ -341,7 +341,8 @@ size_t gdn_prefill_workspace_size(int64_t T_total, int n_seqs, int HV, int Dk, i
 /*
  * The same for a given dtype: exactly what the path that shape and dtype take needs
  * (128 x 128 bf16 heads take the tensor-core path, 58 KiB per (chunk, value head);
- * the other shapes and fp32 the CUDA-core path, 4 * (64 (Dk + Dv + 64) + 320) bytes).
+ * the other shapes and fp32 the CUDA-core path, 4 * (64 (Dk + Dv + 64) + 320) bytes;
+ * either path also a 4-byte flag per (chunk, value head) and a few KiB of header).
  * A workspace of this size is accepted by calls with that dtype.  Host-only.
  * Returns 0 for invalid sizes or dtype.
  */
