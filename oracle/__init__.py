@@ -25,7 +25,8 @@ normalised row; the convolution of the step before the rule by its impulse
 response (causal, depthwise, width 4), continuation through the carried conv
 state and packed-vs-separate runs; the gates by closed forms and the
 softplus odd-part identity; the regroup of the fused projections against a
-hand-listed column layout.
+hand-listed column layout; the split of the conv output into queries, keys
+and values against a hand-listed channel layout.
 """
 import ctypes
 import os
